@@ -1,0 +1,410 @@
+"""Pins of the CPU oracle to things other than itself (no GPU needed).
+
+Each group below checks one oracle function against brute force, a closed
+form, an invariant the definition fixes, or a value printed on the pages, so
+that a dropped term, a wrong sign or index, or a transposed operand fails.
+"""
+import itertools
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+rng = np.random.default_rng(1234)
+
+
+def bf16_bits(x):
+    return synth.f32_to_bf16(np.asarray(x, dtype=np.float32))
+
+
+def f32_of_bf16(bits):
+    return synth.bf16_to_f32(bits)
+
+
+# ------------------------------------------------------------------ bf16 rounding
+def test_bf16_rne_known_values():
+    assert oracle.bf16_rne(1.0) == 0x3F80
+    assert oracle.bf16_rne(-2.0) == 0xC000
+    assert oracle.bf16_rne(1.0 + 2.0 ** -8) == 0x3F80      # tie -> even
+    assert oracle.bf16_rne(1.0 + 3 * 2.0 ** -8) == 0x3F82  # tie -> even (up)
+    assert oracle.bf16_rne(1.0 + 2.0 ** -8 + 2.0 ** -30) == 0x3F81  # just above the tie
+    assert oracle.bf16_rne(0.0) == 0 and oracle.bf16_rne(-0.0) == 0x8000
+    assert oracle.bf16_rne(1e39) == 0x7F80
+    assert oracle.bf16_rne(2.0 ** -133) == 0x0001           # smallest bf16 subnormal
+
+
+def test_bf16_rne_matches_independent_fp32_path():
+    # for fp32-representable inputs the direct fp64 rounding must equal the
+    # generator's independent fp32 bit-trick rounding
+    x = rng.standard_normal(4000).astype(np.float32) * np.float32(3.0)
+    a = np.array([oracle.bf16_rne(float(v)) for v in x], dtype=np.uint16)
+    assert np.array_equal(a, synth.f32_to_bf16(x))
+
+
+# ------------------------------------------------------------------ a-1 summaries
+def _block(hkv, B, D, fill=None):
+    blk = np.zeros((hkv, 2, B, D), dtype=np.uint16)
+    if fill is not None:
+        blk[...] = fill
+    return blk
+
+
+def test_summary_constant_block_is_exact():
+    for n in (1, 3, 16, 64):
+        blk = _block(2, 64, 8, bf16_bits(0.3)[()])
+        km = oracle.block_summary(blk, n)
+        # exact for power-of-two n; within 1 ulp-ish for others
+        ref = np.float32(f32_of_bf16(bf16_bits(0.3)))
+        if n & (n - 1) == 0:
+            assert np.all(km == ref)
+        else:
+            assert np.all(np.abs(km - ref) <= 4 * np.spacing(ref))
+
+
+def test_summary_uses_keys_of_its_head_and_valid_tokens_only():
+    hkv, B, D = 3, 16, 8
+    blk = _block(hkv, B, D)
+    for g in range(hkv):
+        blk[g, 0, :5] = bf16_bits(float(g + 1))     # K of head g = g+1 on valid tokens
+        blk[g, 0, 5:] = bf16_bits(1000.0)           # tokens past n_valid must be ignored
+        blk[g, 1] = bf16_bits(-77.0)                # V must be ignored
+    km = oracle.block_summary(blk, 5)
+    for g in range(hkv):
+        assert np.all(km[g] == np.float32(g + 1))
+
+
+def test_summary_exact_rational_mean():
+    # small multiples of 1/8: every partial sum is exact in fp32, so the result is
+    # the correctly rounded exact mean
+    B, D = 32, 4
+    vals = rng.integers(-40, 40, size=(B, D)) / 8.0
+    blk = _block(1, B, D)
+    blk[0, 0] = bf16_bits(vals)
+    for n in (1, 7, 32):
+        km = oracle.block_summary(blk, n)
+        for d in range(D):
+            exact = Fraction(sum(Fraction(int(v * 8), 8) for v in vals[:n, d]), n)
+            assert km[0, d] == np.float32(float(exact))
+
+
+def test_summary_error_bound_random():
+    B, D = 64, 128
+    x = rng.standard_normal((B, D)).astype(np.float32)
+    blk = _block(1, B, D)
+    blk[0, 0] = bf16_bits(x)
+    xf = f32_of_bf16(blk[0, 0]).astype(np.float64)
+    km = oracle.block_summary(blk, B)
+    u = 2.0 ** -24
+    for d in range(D):
+        exact = xf[:, d].sum() / B
+        bound = (B - 1) * u * np.abs(xf[:, d]).sum() / B + u * abs(exact) + 1e-30
+        assert abs(km[0, d] - exact) <= bound
+
+
+def test_region_summaries_tail_block():
+    reg = synth.kv_region(3, 0, 0, 100, 8, 2, 16, 8)
+    km = oracle.region_summaries(reg, 100)
+    assert km.shape == (7, 2, 8)
+    # tail block 6 holds 4 tokens
+    direct = f32_of_bf16(reg[6, :, 0, :4]).astype(np.float64).mean(axis=1)
+    assert np.allclose(km[6], direct, rtol=1e-6, atol=1e-7)
+
+
+# ------------------------------------------------------------------ a-2 score
+def test_score_integer_inputs_equal_per_head_definition():
+    """Exact small integers: the grouped fp32 score must equal the per-head integer
+    sum  sum_h q_h . kmean[b, h // G]  computed with Python ints."""
+    hq, hkv, D = 8, 2, 32
+    G = hq // hkv
+    q = rng.integers(-3, 4, size=(hq, D))
+    km = rng.integers(-3, 4, size=(hkv, D))
+    exact = sum(int(q[h, d]) * int(km[h // G, d]) for h in range(hq) for d in range(D))
+    qs = oracle.qsum(bf16_bits(q.astype(np.float32)), hkv)
+    s = oracle.score(qs, km.astype(np.float32))
+    assert s == float(exact)
+
+
+def test_score_one_hot_picks_element():
+    E = 256
+    km = rng.standard_normal(E).astype(np.float32)
+    for e in (0, 5, 127, 128, 200, 255):
+        qs = np.zeros(E, dtype=np.float32)
+        qs[e] = 1.0
+        assert oracle.score(qs, km) == km[e]
+
+
+def test_score_error_bound_random():
+    for E in (64, 128, 1024):
+        qs = rng.standard_normal(E).astype(np.float32)
+        km = (rng.standard_normal(E) / 8).astype(np.float32)
+        exact = float(np.dot(qs.astype(np.float64), km.astype(np.float64)))
+        bound = E * 2.0 ** -24 * float(np.abs(qs.astype(np.float64) * km).sum())
+        assert abs(oracle.score(qs, km) - exact) <= bound
+
+
+# ------------------------------------------------------------------ a-2 top-k
+def _brute_topk(scores, k):
+    """Among all k-subsets of the candidates, the one with the largest score sum
+    (exact rationals); ties broken by the lexicographically smallest index tuple."""
+    n = len(scores)
+    best, best_key = None, None
+    fr = [Fraction(float(s)) for s in scores]
+    for comb in itertools.combinations(range(n), k):
+        key = (-sum(fr[i] for i in comb), comb)
+        if best_key is None or key < best_key:
+            best, best_key = comb, key
+    return list(best)
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_topk_matches_brute_force_with_ties(seed):
+    r = np.random.default_rng(seed)
+    nb = int(r.integers(1, 11))
+    W = int(r.integers(0, 3))
+    k = int(r.integers(0, nb + 2))
+    scores = r.integers(-2, 3, size=nb).astype(np.float32)  # many ties
+    sel = oracle.select_topk(scores, nb, k, W)
+    ncand = max(nb - W, 0)
+    kk = min(k, ncand)
+    want = sorted(_brute_topk(scores[:ncand], kk) + list(range(ncand, nb)))
+    assert list(sel) == want
+
+
+def test_topk_invariant_random_large():
+    for seed in range(20):
+        r = np.random.default_rng(100 + seed)
+        nb, W, k = 513, 2, 32
+        scores = r.standard_normal(nb).astype(np.float32)
+        scores[r.integers(0, nb, 50)] = scores[0]  # some ties
+        sel = oracle.select_topk(scores, nb, k, W)
+        assert list(sel) == sorted(sel) and len(sel) == k + W
+        assert set(range(nb - W, nb)) <= set(sel)
+        T = [b for b in sel if b < nb - W]
+        rest = [b for b in range(nb - W) if b not in set(T)]
+        worst_in = max(T, key=lambda b: (-scores[b], b))
+        best_out = min(rest, key=lambda b: (-scores[b], b))
+        assert (-scores[worst_in], worst_in) < (-scores[best_out], best_out)
+
+
+def test_topk_zero_query_takes_lowest_indices():
+    q = np.zeros((8, 64), dtype=np.uint16)
+    km = rng.standard_normal((256, 2, 64)).astype(np.float32)
+    sel = oracle.select_shared(q, km, 32, 4)
+    assert list(sel) == list(range(32)) + [252, 253, 254, 255]
+
+
+def test_topk_negative_zero_ties_plus_zero():
+    scores = np.array([0.0, -0.0, 0.0, -1.0], dtype=np.float32)
+    assert list(oracle.select_topk(scores, 4, 2, 0)) == [0, 1]
+    scores = np.array([-0.0, 0.0, -1.0], dtype=np.float32)
+    assert list(oracle.select_topk(scores, 3, 1, 0)) == [0]
+
+
+def test_topk_degenerate_sizes():
+    s = np.arange(10, dtype=np.float32)
+    assert list(oracle.select_topk(s, 10, 100, 2)) == list(range(10))  # k >= candidates
+    assert list(oracle.select_topk(s, 3, 5, 4)) == [0, 1, 2]           # nb <= W
+    assert list(oracle.select_topk(s, 10, 0, 2)) == [8, 9]             # k = 0
+    assert list(oracle.select_topk(s, 0, 4, 2)) == []                  # empty
+
+
+def test_headwise_equals_shared_when_one_kv_head():
+    q = bf16_bits(rng.standard_normal((4, 128)))
+    km = rng.standard_normal((300, 1, 128)).astype(np.float32)
+    hw = oracle.select_headwise(q, km, 20, 2)
+    sh = oracle.select_shared(q, km, 20, 2)
+    assert list(hw[0]) == list(sh)
+
+
+def test_headwise_uses_its_own_head():
+    # head 1 summaries favour blocks 0..4; head 0 favours 10..14
+    hq, hkv, D, nb = 4, 2, 64, 20
+    q = bf16_bits(np.ones((hq, D)))
+    km = np.zeros((nb, hkv, D), dtype=np.float32)
+    km[10:15, 0] = 1.0
+    km[0:5, 1] = 1.0
+    hw = oracle.select_headwise(q, km, 5, 0)
+    assert list(hw[0]) == list(range(10, 15)) and list(hw[1]) == list(range(0, 5))
+
+
+def test_fragmentation_worked_example():
+    """PulseInfer Guide, "SoloHead Sparse Selection": 3 heads x 3 blocks -> 7 unique."""
+    sets, union = [], None
+    with open(os.path.join(GOLD, "solohead_fragmentation.txt")) as f:
+        for line in f:
+            if line.startswith("head"):
+                sets.append([int(x) for x in line.split(":")[1].split()])
+            elif line.startswith("union_blocks"):
+                union = int(line.split(":")[1])
+    assert oracle.union_fragments(sets) == union == 7
+
+
+# ------------------------------------------------------------------ sizes
+def test_kv_and_block_sizes_printed_on_pages():
+    vals = {}
+    with open(os.path.join(GOLD, "kv_sizes.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                k, v = line.split()
+                vals[k] = float(v)
+    b8 = oracle.kv_cache_bytes(int(vals["kv8b_layers"]), int(vals["kv8b_hkv"]), int(vals["kv8b_d"]), int(vals["kv8b_seq"]))
+    assert round(b8 / 1e9, 1) == vals["kv8b_gb_printed"]
+    b70 = oracle.kv_cache_bytes(int(vals["kv70b_layers"]), int(vals["kv70b_hkv"]), int(vals["kv70b_d"]), int(vals["kv70b_seq"]))
+    assert b70 / 1e9 > vals["kv70b_gb_printed_lower_bound"] and round(b70 / 1e9, 1) == 41.9
+    assert oracle.block_bytes(int(vals["block_hkv"]), int(vals["block_tokens"]), int(vals["block_d"])) == 65536
+    # Llama-3-70B slice of 8 layers, batch 16, 131072 tokens: "~69 GB" of host KV
+    assert round(16 * oracle.kv_cache_bytes(8, 8, 128, 131072) / 1e9, 1) == 68.7
+
+
+# ------------------------------------------------------------------ a-3 plan
+def test_plan_hand_worked_example():
+    # pool of 4 slots holding blocks 5, 7, 9 in slots 0..2; select [1, 7, 8]
+    sob = np.full(16, -1, dtype=np.int32)
+    bos = np.array([5, 7, 9, -1], dtype=np.int32)
+    for s, b in enumerate(bos):
+        if b >= 0:
+            sob[b] = s
+    table, mb, ms, ev = oracle.recall_plan(np.array([1, 7, 8]), sob, bos)
+    # missing [1, 8]; free slots ascending [0 (5 unselected), 2 (9 unselected), 3 (empty)]
+    assert list(mb) == [1, 8] and list(ms) == [0, 2] and list(ev) == [5, 9]
+    assert list(table) == [0, 1, 2]
+    assert list(bos) == [1, 7, 8, -1]
+    assert sob[5] == -1 and sob[9] == -1 and sob[1] == 0 and sob[7] == 1 and sob[8] == 2
+
+
+def test_plan_pool_too_small_leaves_maps():
+    sob = np.full(8, -1, dtype=np.int32)
+    bos = np.full(2, -1, dtype=np.int32)
+    assert oracle.recall_plan(np.array([0, 1, 2]), sob, bos) is None
+    assert np.all(sob == -1) and np.all(bos == -1)
+
+
+def test_plan_invariants_random_sequence():
+    r = np.random.default_rng(7)
+    nb, P = 200, 40
+    sob = np.full(nb, -1, dtype=np.int32)
+    bos = np.full(P, -1, dtype=np.int32)
+    for step in range(60):
+        sel = np.sort(r.choice(nb, size=int(r.integers(0, P + 1)), replace=False)).astype(np.int32)
+        before = {int(b): int(s) for s, b in enumerate(bos) if b >= 0}
+        out = oracle.recall_plan(sel, sob, bos)
+        assert out is not None
+        table, mb, ms, ev = out
+        assert set(mb) == set(int(b) for b in sel) - set(before)          # only missing move
+        for b in sel:                                                    # hits stay put
+            if int(b) in before:
+                assert sob[b] == before[int(b)]
+        assert all(e not in set(sel.tolist()) for e in ev if e >= 0)      # evict unselected only
+        assert list(table) == [sob[b] for b in sel]
+        for s in range(P):                                               # maps inverse
+            if bos[s] >= 0:
+                assert sob[bos[s]] == s
+        assert (sob >= 0).sum() == (bos >= 0).sum()
+
+
+# ------------------------------------------------------------------ a-5 attention
+def _dense_inputs(reg, ntok, hkv, sel):
+    B = reg.shape[3]
+    Ks, Vs = [], []
+    for g in range(hkv):
+        kk, vv = [], []
+        for b in sel:
+            nv = min(B, ntok - b * B)
+            kk.append(oracle.bf16_to_f64(reg[b, g, 0, :nv]))
+            vv.append(oracle.bf16_to_f64(reg[b, g, 1, :nv]))
+        Ks.append(np.concatenate(kk))
+        Vs.append(np.concatenate(vv))
+    return np.stack(Ks), np.stack(Vs)
+
+
+@pytest.mark.parametrize("ntok", [4096, 1000, 17])
+def test_attention_all_blocks_equals_dense(ntok):
+    hq, hkv, B, D = 8, 2, 16, 64
+    nbmax = -(-ntok // B) + 1
+    reg = synth.kv_region(5, 0, 0, ntok, nbmax, hkv, B, D)
+    q = synth.normal_bf16(5, synth.KIND_MISC, 0, 0, hq * D).reshape(hq, D)
+    nb = -(-ntok // B)
+    km = oracle.region_summaries(reg, ntok)
+    sel = oracle.select_shared(q, km, nb, 4)        # k >= candidates: every block
+    assert list(sel) == list(range(nb))
+    out, lse, _ = oracle.attention(q, reg, sel, ntok, hkv)
+    K, V = _dense_inputs(reg, ntok, hkv, sel)
+    dout, dlse = oracle.dense_attention_fp64(oracle.bf16_to_f64(q), K, V)
+    assert np.array_equal(out, np.array([[oracle.bf16_rne(v) for v in row] for row in dout], dtype=np.uint16))
+    assert np.allclose(lse, dlse, rtol=1e-12, atol=1e-12)
+    torch = pytest.importorskip("torch")
+    G = hq // hkv
+    qt = torch.tensor(oracle.bf16_to_f64(q)).reshape(1, hq, 1, D)
+    kt = torch.tensor(K).repeat_interleave(G, 0).reshape(1, hq, -1, D)
+    vt = torch.tensor(V).repeat_interleave(G, 0).reshape(1, hq, -1, D)
+    ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt).reshape(hq, D).numpy()
+    assert np.max(np.abs(oracle.bf16_to_f64(out) - ref)) <= 2.0 ** -8 * np.max(np.abs(ref)) + 1e-12
+
+
+def test_attention_weights_sum_to_one_and_gqa_mapping():
+    hq, hkv, B, D, ntok = 8, 2, 16, 64, 300
+    reg = synth.kv_region(6, 0, 0, ntok, 20, hkv, B, D)
+    for g in range(hkv):
+        reg[:, g, 1] = np.where(np.arange(B)[None, :, None] >= 0, bf16_bits(float(g + 1)), 0)
+    q = synth.normal_bf16(6, synth.KIND_MISC, 0, 0, hq * D).reshape(hq, D)
+    sel = np.array([0, 3, 7, 18], dtype=np.int32)
+    out, _, _ = oracle.attention(q, reg, sel, ntok, hkv)
+    G = hq // hkv
+    for h in range(hq):
+        assert np.all(oracle.bf16_to_f64(out[h]) == h // G + 1)   # convex weights sum to 1
+
+
+def test_attention_single_token_and_equal_logits():
+    hq, hkv, B, D = 4, 1, 16, 64
+    reg = synth.kv_region(8, 0, 0, 33, 4, hkv, B, D)
+    q = synth.normal_bf16(8, synth.KIND_MISC, 0, 0, hq * D).reshape(hq, D)
+    out, lse, lg = oracle.attention(q, reg, np.array([2], dtype=np.int32), 33, hkv, want_logits=True)
+    assert np.array_equal(out, np.repeat(reg[2, 0, 1, 0][None], hq, 0))   # one valid token: out = V
+    # logits of that token equal the plain dot product / sqrt(D)
+    k = oracle.bf16_to_f64(reg[2, 0, 0, 0])
+    for h in range(hq):
+        assert math.isclose(lg[h, 0, 0], float(oracle.bf16_to_f64(q[h]) @ k) / 8.0, rel_tol=1e-12)
+        assert math.isclose(lse[h], lg[h, 0, 0], rel_tol=1e-12)
+    q0 = np.zeros((hq, D), dtype=np.uint16)
+    sel = np.array([0, 1], dtype=np.int32)
+    out, lse, _ = oracle.attention(q0, reg, sel, 33, hkv)
+    mean = oracle.bf16_to_f64(reg[0:2, 0, 1].reshape(-1, D)).mean(axis=0)
+    assert np.array_equal(out[0], np.array([oracle.bf16_rne(v) for v in mean], dtype=np.uint16))
+    assert math.isclose(lse[0], math.log(32), rel_tol=1e-12)
+
+
+def test_attention_ignores_tokens_past_ntok():
+    hq, hkv, B, D, ntok = 8, 2, 16, 64, 40   # tail block 2 holds 8 tokens
+    reg = synth.kv_region(9, 0, 0, ntok, 4, hkv, B, D)
+    q = synth.normal_bf16(9, synth.KIND_MISC, 0, 0, hq * D).reshape(hq, D)
+    sel = np.array([0, 2], dtype=np.int32)
+    a, la, _ = oracle.attention(q, reg, sel, ntok, hkv)
+    reg2 = reg.copy()
+    reg2[2, :, :, 8:] = bf16_bits(50.0)
+    b, lb, _ = oracle.attention(q, reg2, sel, ntok, hkv)
+    assert np.array_equal(a, b) and np.array_equal(la, lb)
+
+
+def test_attention_empty_selection():
+    reg = synth.kv_region(1, 0, 0, 16, 2, 1, 16, 64)
+    q = synth.normal_bf16(1, synth.KIND_MISC, 0, 0, 4 * 64).reshape(4, 64)
+    out, lse, _ = oracle.attention(q, reg, np.zeros(0, dtype=np.int32), 16, 1)
+    assert np.all(out == 0) and np.all(np.isneginf(lse))
+
+
+def test_attention_headwise_selection_per_head():
+    hq, hkv, B, D, ntok = 8, 2, 16, 64, 160
+    reg = synth.kv_region(2, 0, 0, ntok, 10, hkv, B, D)
+    q = synth.normal_bf16(2, synth.KIND_MISC, 0, 0, hq * D).reshape(hq, D)
+    sels = [np.array([1, 4], dtype=np.int32), np.array([0, 2, 9], dtype=np.int32)]
+    out, lse, _ = oracle.attention(q, reg, sels, ntok, hkv)
+    for g in range(hkv):
+        o1, l1, _ = oracle.attention(q, reg, sels[g], ntok, hkv)
+        G = hq // hkv
+        assert np.array_equal(out[g * G:(g + 1) * G], o1[g * G:(g + 1) * G])
