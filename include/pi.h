@@ -1,0 +1,286 @@
+/*
+ * pi.h -- C ABI of the GB300 sparse KV-cache offloading decode path.
+ *
+ * One GPU, one process. The library owns a pool: a pinned, GPU-mapped host KV
+ * store (most blocks live here), a device block pool of recalled blocks, the
+ * per-block key summaries, the slot maps and all scratch. Callers own the
+ * per-call device buffers (queries, selections, tables, outputs), typically
+ * PyTorch tensors, and pass raw device pointers and CUDA streams.
+ *
+ * Method (page title, section):
+ *  - "PulseInfer: I/O-Centric Sparse KV Cache Offloading for Efficient
+ *    Long-Context LLM Decoding", Abstract: KV blocks stay in CPU DRAM, selected
+ *    blocks are recalled on demand; SoloHead selection and a gather-scatter I/O
+ *    engine turn many small head-wise transfers into one coalesced recall;
+ *    recall is overlapped with decode layer by layer.
+ *  - "PulseInfer Guide: I/O-Centric Sparse KV Cache Offloading":
+ *    "SoloHead Sparse Selection" (one block set shared by all heads of a layer),
+ *    "The Gather-Scatter I/O Engine" (blocks land in pool page slots),
+ *    "The Small-Packet PCIe DMA Tax" (paged blocks of B tokens),
+ *    "Interruptible Layer-Wise Scheduling" (recall of one layer hides behind
+ *    compute of another).
+ * The pages name SoloHead but never define its block score. This library fixes
+ * one definition (see pi_select_topk).
+ *
+ * Notation: L layers, R requests (batch), Hq query heads, Hkv KV heads,
+ * G = Hq/Hkv, D head_dim, B tokens per block, P pool slots per (request, layer),
+ * cap = k_max + window, bf16 = IEEE bfloat16 bit patterns (uint16).
+ *
+ * Layouts (row-major, innermost last):
+ *  host store, per (layer, request):  [max_blocks][Hkv][2 (K,V)][B][D] bf16
+ *    -> a block is BB = 2*Hkv*B*D*2 contiguous bytes, one head's K+V of a block
+ *       (a "fragment") FB = 2*B*D*2 contiguous bytes.
+ *  device pool: one slot = one block in the same [Hkv][2][B][D] layout.
+ *  q: [R][Hq][D] bf16; out: [R][Hq][D] bf16; lse: [R][Hq] fp32 (natural log).
+ *  sel / table: [R][cap] int32 (shared mode) or [R][Hkv][cap] (head-wise mode);
+ *  nsel: [R] or [R][Hkv] int32.
+ *
+ * Errors: every call checks its arguments on the host and returns a status; no
+ * call aborts. Kernels never trap: a bad index or a wait that runs out sets a
+ * sticky device status word, read by pi_get_device_status. Calls are
+ * asynchronous on the given stream unless stated. Calls of the same kind on the
+ * same layer must be stream-ordered; different layers may run concurrently.
+ */
+#ifndef PI_H
+#define PI_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PI_ABI_VERSION 1
+
+/* cudaStream_t without pulling in CUDA headers; NULL = legacy default stream. */
+typedef struct CUstream_st* pi_stream;
+
+typedef enum {
+  PI_OK = 0,
+  PI_ERR_INVALID = 1,        /* bad argument or size; nothing was enqueued */
+  PI_ERR_CUDA = 2,           /* a CUDA runtime call failed */
+  PI_ERR_OOM = 3,            /* device allocation failed */
+  PI_ERR_HOST_ALLOC = 4,     /* pinned host allocation failed */
+  PI_ERR_POOL_FULL = 5,      /* more missing blocks than free slots */
+  PI_ERR_TIMEOUT = 6,        /* a bounded device wait ran out */
+  PI_ERR_DEVICE = 7,         /* a kernel flagged an out-of-range index */
+  PI_ERR_STATE = 8,          /* call not valid in the pool's state/mode */
+  PI_ERR_FAULT_INJECTED = 9  /* host-side fault injection fired */
+} pi_status;
+
+enum { PI_SHARED = 0, PI_HEADWISE = 1 };
+enum { PI_RECALL_UVA = 0, PI_RECALL_MEMCPY = 1, PI_RECALL_STAGED = 2 };
+
+typedef struct pi_config {
+  int layers, batch, hq, hkv, head_dim, block_tokens;
+  int max_blocks;            /* host/summary capacity per (layer, request), blocks */
+  int pool_slots;            /* P per (request, layer); must be >= k_max + window */
+  int k_max;                 /* largest top-k a call may ask for */
+  int window;                /* W most recent blocks always selected */
+  int select_mode;           /* PI_SHARED (one block set per request and layer) or
+                                PI_HEADWISE (one per KV head: the comparison arm) */
+  int host_layers;           /* 0 = layers. Else the host store holds host_layers
+                                layers and layer l reads host layer l % host_layers
+                                (capacity fallback; appends must then carry the same
+                                tokens for aliased layers). */
+  int staging_blocks;        /* staged recall arm: staging capacity in copy units
+                                (0 = as many as fit in 256 MiB) */
+  int gather_ctas;           /* UVA gather kernel grid (0 = 2 per SM) */
+  const int* pool_slots_per_req; /* optional host [batch]: per-request P (each
+                                >= k_max + window); NULL = pool_slots for all */
+} pi_config;
+
+typedef struct pi_pool pi_pool;
+
+typedef struct pi_recall_stats {
+  long long bytes;           /* bytes copied host -> pool */
+  long long fragments;       /* copy units moved (blocks; block-heads head-wise) */
+  long long runs;            /* contiguous runs after merging adjacent units */
+  long long api_calls;       /* cudaMemcpyAsync calls issued (0 for the UVA kernel) */
+  long long hits;            /* selected units already resident */
+  double host_wait_ms;       /* host time blocked on the plan (memcpy, staged arms) */
+  double cpu_gather_ms;      /* staged arm: CPU gather time */
+} pi_recall_stats;
+
+typedef struct pi_step_stats {
+  pi_recall_stats recall;    /* summed over layers */
+  long long selected;        /* selected units summed over layers and requests */
+} pi_step_stats;
+
+/* Pointers into library-owned device state, for inspection and tests. */
+typedef struct pi_pool_views {
+  void* pool;                /* device pool base (slots of BB bytes) */
+  const long long* slot_base;/* host [batch]: first global slot of (r, layer 0);
+                                global slot of (r, l, s) = slot_base[r] + l*P_r + s */
+  const int* slots_per_req;  /* host [batch]: P_r */
+  float* kmean;              /* device [R][L][max_blocks][Hkv][D] fp32 summaries */
+  int* ntok;                 /* device [R][L] tokens held */
+  int* slot_of_block;        /* device [R][L][U][max_blocks], U = 1 or Hkv; -1 = absent */
+  int* block_of_slot;        /* device [R][L][U][P_max]; -1 = empty */
+  int p_max;
+  int* step_sel;             /* device [L][R][U][cap]: selections of pi_decode_step */
+  int* step_nsel;            /* device [L][R][U] */
+  int* step_table;           /* device [L][R][U][cap] */
+  size_t block_bytes, frag_bytes, host_region_bytes;
+} pi_pool_views;
+
+/* ------------------------------------------------------------------ lifetime */
+int pi_abi_version(void);
+const char* pi_status_str(pi_status s);
+
+/* Create a pool on the current CUDA device. Allocates the pinned mapped host
+ * store (host_layers*batch*max_blocks*BB bytes, zero-filled), the device pool
+ * (zeroed; all slots empty), summaries, maps and scratch. Honors the host-side
+ * fault hook PI_FAULT=pinned_alloc_fail (environment) for tests.
+ * Errors: PI_ERR_INVALID (sizes: head_dim in {64,128}, block_tokens in
+ * {16,32,64,128}, Hq % Hkv == 0, Hq/Hkv <= 8, max_blocks <= 65536, P >= cap),
+ * PI_ERR_HOST_ALLOC, PI_ERR_OOM. On error *out is NULL and nothing leaks. */
+pi_status pi_pool_create(const pi_config* cfg, pi_pool** out);
+pi_status pi_pool_destroy(pi_pool* p);   /* synchronizes the device first */
+pi_status pi_pool_get_config(const pi_pool* p, pi_config* out);
+pi_status pi_pool_get_views(pi_pool* p, pi_pool_views* out);
+
+/* Host pointer (pinned, writable by the caller) to the KV region of (layer,
+ * request): [max_blocks][Hkv][2][B][D] bf16. Aliased layers share a region.
+ * Fill it before pi_update_summaries; later changes go through pi_append_kv.
+ * NULL on a bad index. */
+void* pi_host_kv(pi_pool* p, int layer, int req);
+
+/* ------------------------------------------------------------------ a-1 summaries */
+/* Set the token count of every request of `layer` (host array ntok[R]) and
+ * compute the block summaries kmean[b][g][:] = (sum over the block's valid
+ * tokens, in token order, of K in fp32) / valid, for blocks
+ * [block_begin, block_end) clipped to each request's block count. Keys are read
+ * from k_dev (device, same layout as the host region of that layer, per request
+ * consecutive) or, if k_dev is NULL, from the host store through the GPU's
+ * mapping of it. Also seeds the running sum of each request's last block.
+ * Score definition: PulseInfer Guide, "SoloHead Sparse Selection" names a
+ * per-block importance; the per-KV-head mean key is this library's reading.
+ * Errors: PI_ERR_INVALID (layer, range, ntok > max_blocks*B). */
+pi_status pi_update_summaries(pi_pool* p, int layer, const void* k_dev, int block_begin, int block_end,
+                              const int* ntok_host, pi_stream s);
+
+/* ------------------------------------------------------------------ a-7 append */
+/* Append one decoded token per request to `layer`: k_new/v_new device
+ * [R][Hkv][D] bf16. Writes through to the host store and, if the token's block
+ * is resident, to its pool slot; updates that block's summary from the running
+ * fp32 sum (bit-identical to recomputing it in token order) and the token
+ * count. Errors: PI_ERR_INVALID when a request would exceed max_blocks*B. */
+pi_status pi_append_kv(pi_pool* p, int layer, const void* k_new, const void* v_new, pi_stream s);
+
+/* ------------------------------------------------------------------ a-2 select */
+/* SoloHead-style shared block selection of `layer` for every request.
+ * score(b) = sum over query heads h of q_h . kmean[b, h / G], evaluated in fp32
+ * as sum_g qsum_g . kmean[b, g] with qsum_g = sum_{h in g} q_h (head order) and
+ * a fixed 32-lane order: lane i accumulates elements 128c+4i+j with fused
+ * multiply-add (c, then j ascending), then a xor-butterfly 16,8,4,2,1.
+ * Candidates: blocks 0 .. nb-W-1 (nb = ceil(ntok/B)); pick min(k_r, candidates)
+ * by (score descending, block index ascending; -0.0 equals +0.0), add the W most
+ * recent blocks, write ascending to sel[r][0..nsel[r]). k_per_req: device [R],
+ * each clamped to [0, k_max]. Head-wise pools (PI_HEADWISE) select per KV head g
+ * with score_g(b) = qsum_g . kmean[b, g] into sel[r][g][..]. `mode` must equal
+ * the pool's select_mode. Scores must be finite (NaN inputs are a caller error).
+ * Source: PulseInfer Guide, "SoloHead Sparse Selection"; the abstract of the
+ * PulseInfer paper (SoloHead coalesces head-wise fragmented recalls). */
+pi_status pi_select_topk(pi_pool* p, int layer, const void* q, const int* k_per_req, int mode, int* sel,
+                         int* nsel, pi_stream s);
+
+/* ------------------------------------------------------------------ a-3/a-4 recall */
+/* Make every selected unit of `layer` resident and write its slot to table.
+ * Plan (per request, or per request and KV head in head-wise pools): missing =
+ * selected units without a slot, ascending; free = slots empty or holding an
+ * unselected unit, ascending; the i-th missing unit takes the i-th free slot.
+ * Copy: each missing unit's bytes (a BB block, or an FB fragment head-wise) go
+ * from the host store to its slot, by
+ *   PI_RECALL_UVA    one gather kernel reading the mapped host store (no host
+ *                    sync; the plan stays on the device),
+ *   PI_RECALL_MEMCPY one cudaMemcpyAsync per run of adjacent units (the plan is
+ *                    read back: one device->host copy and one host sync),
+ *   PI_RECALL_STAGED CPU threads gather into a pinned staging buffer, one bulk
+ *                    cudaMemcpyAsync, a GPU scatter kernel (the guide's three
+ *                    phases; host sync as above).
+ * Maps are committed only after the copy is enqueued: an error (including an
+ * injected fault) leaves them unchanged. stats (optional) is filled after the
+ * call's work completes (this adds a host sync to the UVA arm).
+ * Source: PulseInfer Guide, "The Gather-Scatter I/O Engine" and "The Small-Packet
+ * PCIe DMA Tax"; the PulseInfer abstract (gather-scatter I/O engine).
+ * Errors: PI_ERR_INVALID, PI_ERR_CUDA, PI_ERR_FAULT_INJECTED (PI_FAULT=recall_fail@N
+ * fails the N-th recall call, counted from 1, before any map change). */
+pi_status pi_recall(pi_pool* p, int layer, const int* sel, const int* nsel, int method, int* table,
+                    pi_recall_stats* stats, pi_stream s);
+
+/* Place blocks[0..n) (ascending, host array) of (layer, req) in slots 0..n-1
+ * and copy their bytes from the host store (initial residency). Synchronous.
+ * Errors: PI_ERR_INVALID (n > P_r, unsorted, out of range, head-wise pool). */
+pi_status pi_pool_preload(pi_pool* p, int layer, int req, const int* blocks, int n, pi_stream s);
+
+/* Forget residency of `layer` (-1 = all layers): every slot empty. Bytes stay. */
+pi_status pi_pool_flush(pi_pool* p, int layer, pi_stream s);
+
+/* ------------------------------------------------------------------ a-5 attention */
+/* GQA sparse decode attention of `layer` over the resident selected blocks:
+ * for query head h (KV head g = h / G) the tokens of sel[..][0..nsel) (ascending
+ * block, then token; a block b holds min(B, ntok - b*B) valid tokens) read from
+ * the pool through table; z = q_h . K / sqrt(D) in fp32 from bf16 products;
+ * softmax and the weighted sum of V accumulate in fp32 (weights enter the PV
+ * product as bf16); out rounded to bf16. lse (optional) = log-sum-exp of z.
+ * logits (optional, debugging) fp32 [R][Hq][cap][B] receives z of valid tokens.
+ * An empty selection gives out = 0, lse = -inf.
+ * Source: PulseInfer Guide, "PulseInfer Architectural Foundations" (attention
+ * over the recalled pool blocks) and "SoloHead Sparse Selection" (GQA).
+ * Errors: PI_ERR_INVALID. */
+pi_status pi_sparse_decode(pi_pool* p, int layer, const void* q, const int* sel, const int* table,
+                           const int* nsel, void* out, float* lse, float* logits, pi_stream s);
+
+/* ------------------------------------------------------------------ a-6 pipeline */
+/* One decode step over all layers with the recall of layer l+1 overlapped with
+ * attention of layer l: compute stream runs append, select and attention; the
+ * copy stream runs recall; events order them (no host sync with PI_RECALL_UVA).
+ * q_all [L][R][Hq][D] bf16, k_new_all/v_new_all [L][R][Hkv][D] bf16 (both NULL:
+ * no append), k_budget [L][R] int32, out_all [L][R][Hq][D] bf16, lse_all
+ * [L][R][Hq] fp32 (optional); all device. Selections and tables land in the
+ * pool's per-layer step buffers (pi_pool_views). stats: optional (adds a sync).
+ * Source: PulseInfer abstract and Guide, "Interruptible Layer-Wise Scheduling". */
+pi_status pi_decode_step(pi_pool* p, const void* q_all, const void* k_new_all, const void* v_new_all,
+                         const int* k_budget, int method, void* out_all, float* lse_all, pi_stream compute,
+                         pi_stream copy, pi_step_stats* stats);
+
+/* pi_decode_step with HOST inputs and outputs (pinned or pageable): copies
+ * q_all, k_new_all, v_new_all, k_budget host->device into pool-owned buffers,
+ * runs the step and copies out_all (and lse_all if non-NULL) back. Returns after
+ * the outputs are on the host. */
+pi_status pi_decode_step_host(pi_pool* p, const void* q_all, const void* k_new_all, const void* v_new_all,
+                              const int* k_budget, int method, void* out_all, float* lse_all,
+                              pi_stream compute, pi_stream copy);
+
+/* ------------------------------------------------------------------ timing */
+enum { PI_K_APPEND = 0, PI_K_SELECT = 1, PI_K_PLAN = 2, PI_K_GATHER = 3, PI_K_ATTENTION = 4, PI_K_KINDS = 5 };
+
+typedef struct pi_kernel_timing {
+  long long launches;        /* kernels of this kind timed */
+  double total_ms;           /* sum of their CUDA-event durations */
+} pi_kernel_timing;
+
+/* Enable per-kernel CUDA-event timing inside pi_decode_step for the next
+ * max_steps steps (0 disables and frees the events). Each kernel launch of the
+ * step is bracketed by two events on the stream it runs on. */
+pi_status pi_pool_set_timing(pi_pool* p, int max_steps);
+/* Synchronizes, sums the recorded durations per kind into out[PI_K_KINDS] and
+ * resets the recording. */
+pi_status pi_pool_get_timing(pi_pool* p, pi_kernel_timing* out);
+
+/* ------------------------------------------------------------------ status */
+/* Synchronizes the device, returns PI_OK or the first device-side error
+ * (PI_ERR_DEVICE, PI_ERR_TIMEOUT, PI_ERR_POOL_FULL) recorded since the last clear. */
+pi_status pi_get_device_status(pi_pool* p);
+pi_status pi_clear_device_status(pi_pool* p);
+
+/* Host-side fault injection for tests: "recall_fail@N" or "" (off). The
+ * environment variable PI_FAULT is read once at pool creation. */
+pi_status pi_set_fault(pi_pool* p, const char* spec);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PI_H */

@@ -1,0 +1,381 @@
+// GQA sparse decode attention over the pool, read through the block table.
+//
+// "PulseInfer Guide: I/O-Centric Sparse KV Cache Offloading", section
+// "PulseInfer Architectural Foundations": recalled blocks land in a paged KV
+// pool in HBM and attention runs over them; "SoloHead Sparse Selection": the
+// selected block set is shared by the query heads of a GQA group.
+//
+// Design (GB300): one CTA per (request, KV head, split of the selected blocks).
+// A producer warp streams each selected block's K and V of that head (one slot =
+// [Hkv][K|V][B][D], so a head's K+V is 4*B*D contiguous bytes) into a ring of
+// shared-memory stages with 2D TMA loads (128-byte swizzle) signalled on
+// mbarriers. Four consumer warps each take 16-token tiles and run bf16
+// mma.sync with the tokens on the M side and the G query heads of the group on
+// the N side (N = 8, padded when G < 8):
+//   S^T[tok][h]  = K[tok][:] . q[h][:]          (fp32 accumulate)
+//   O^T[d][h]   += V^T[d][tok] . P^T[tok][h]     (P in bf16, fp32 accumulate)
+// P^T's operand fragment is the register transpose (movmatrix) of S^T's
+// accumulator fragment, so P never touches shared memory. Online softmax in the
+// log2 domain, fp32. Warps merge in shared memory; splits merge through a small
+// global partial buffer, finalised by the last CTA of the unit.
+#include <cstdio>
+
+#include "pi_internal.cuh"
+
+namespace {
+
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+
+struct AttnParams {
+  const uint16_t* q;
+  const int* sel;
+  const int* table;
+  const int* nsel;
+  const int* ntok;
+  const long long* slot_base;
+  const int* P;
+  float* part_o;      // this layer: [R*Hkv][splits_max][G][D]
+  float2* part_ml;    // this layer: [R*Hkv][splits_max][G]
+  unsigned* counter;  // this layer: [R*Hkv]
+  uint16_t* out;
+  float* lse;
+  float* logits;
+  unsigned* status;
+  int layer, L, Hq, Hkv, G, U, cap, splits, splits_max, bps;
+  float scale, scale_log2;
+};
+
+template <int D, int B>
+struct AttnShape {
+  static constexpr int kStage = 4 * B * D;  // K + V of one head of one block, bytes
+  static constexpr int kNS = (98304 / kStage) < 2 ? 2 : ((98304 / kStage) > 8 ? 8 : (98304 / kStage));
+  static constexpr int kSub = B * 128;      // one 64-column swizzled sub-tile
+  static constexpr int kSmem = kNS * kStage + 1024 + 2 * kNS * 8 + 64;
+};
+
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+template <int D, int B>
+__global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ CUtensorMap tmap, AttnParams p) {
+  using S = AttnShape<D, B>;
+  constexpr int NS = S::kNS;
+  constexpr int TPB = B / 16;
+  constexpr int KS = D / 16;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = pi_smem_addr(smem_raw);
+  uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + NS * S::kStage);
+  uint64_t* empty = full + NS;
+  int* flags = reinterpret_cast<int*>(empty + NS);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int u = blockIdx.y;
+  const int r = u / p.Hkv, g = u % p.Hkv;
+  const int su = (p.U == 1) ? r : u;
+  const int* selu = p.sel + (size_t)su * p.cap;
+  const int* tabu = p.table + (size_t)su * p.cap;
+  int n = p.nsel[su];
+  if (n < 0 || n > p.cap) {
+    if (threadIdx.x == 0) pi_flag(p.status, PI_DEV_BAD_INDEX);
+    n = 0;
+  }
+  const int split = blockIdx.x;
+  const int i0 = split * p.bps;
+  const int nblk = max(0, min(n, i0 + p.bps) - i0);
+  const int nt = p.ntok[(size_t)r * p.L + p.layer];
+  const int Pr = p.P[r];
+  const long long gbase = p.slot_base[r] + (long long)p.layer * Pr;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; s++) {
+      pi_mbar_init(&full[s], 1);
+      pi_mbar_init(&empty[s], kConsumerWarps);
+    }
+    flags[0] = 0;
+    pi_fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int issued = 0;
+      for (int it = 0; it < nblk; it++) {
+        const int s = it % NS;
+        if (it >= NS && !pi_mbar_wait_bounded(&empty[s], ((it / NS) - 1) & 1, p.status)) break;
+        int slot = tabu[i0 + it];
+        if (slot < 0 || slot >= Pr) {
+          pi_flag(p.status, PI_DEV_BAD_INDEX);
+          slot = 0;  // keep the barrier accounting whole; the unit's output is flagged
+        }
+        const int row_k = (int)(((gbase + slot) * p.Hkv + g) * 2 * B);
+        uint8_t* ks = smem + s * S::kStage;
+        uint8_t* vs = ks + B * D * 2;
+        pi_mbar_arrive_expect_tx(&full[s], S::kStage);
+#pragma unroll
+        for (int h = 0; h < D / 64; h++) {
+          pi_tma_load_2d(ks + h * S::kSub, &tmap, h * 64, row_k, &full[s]);
+          pi_tma_load_2d(vs + h * S::kSub, &tmap, h * 64, row_k + B, &full[s]);
+        }
+        issued = it + 1;
+      }
+      // drain: every issued load has landed before the CTA may exit
+      for (int it = max(0, issued - NS); it < issued; it++) pi_mbar_wait_bounded(&full[it % NS], (it / NS) & 1, p.status);
+    }
+  } else {
+    // ------------------------------------------------------------ consumers
+    const int gid = lane >> 2, tig = lane & 3;
+    uint32_t qb[KS][2];
+    {
+      const uint16_t* qrow = p.q + ((size_t)r * p.Hq + (size_t)g * p.G + gid) * D;
+#pragma unroll
+      for (int ks = 0; ks < KS; ks++) {
+        qb[ks][0] = (gid < p.G) ? *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * tig) : 0u;
+        qb[ks][1] = (gid < p.G) ? *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 8 + 2 * tig) : 0u;
+      }
+    }
+    float o[KS][4];
+#pragma unroll
+    for (int mt = 0; mt < KS; mt++) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.0f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
+    const int h0 = 2 * tig, h1 = 2 * tig + 1;
+    const int mat = lane >> 3, r8 = lane & 7;
+
+    for (int it = 0; it < nblk; it++) {
+      const int s = it % NS;
+      if (!pi_mbar_wait_bounded(&full[s], (it / NS) & 1, p.status)) break;
+      const int b = selu[i0 + it];
+      int nv = nt - b * B;
+      nv = nv > B ? B : nv;
+      if (b < 0) nv = 0;
+      const uint32_t ks_base = pi_smem_addr(smem + s * S::kStage);
+      const uint32_t vs_base = ks_base + B * D * 2;
+#pragma unroll
+      for (int j = 0; j < TPB; j++) {
+        if (((it * TPB + j) & (kConsumerWarps - 1)) != warp) continue;
+        const int t0 = j * 16;
+        float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        {
+          const int tok = t0 + r8 + ((mat & 1) << 3);
+#pragma unroll
+          for (int ks = 0; ks < KS; ks++) {
+            const int chunk = ((ks * 16) & 63) / 8 + (mat >> 1);
+            const uint32_t addr = ks_base + ((ks * 16) / 64) * S::kSub + tok * 128 + ((chunk ^ (tok & 7)) << 4);
+            uint32_t a[4];
+            pi_ldmatrix_x4(a, addr);
+            pi_mma_bf16(c, a, qb[ks][0], qb[ks][1]);
+          }
+        }
+        const int ta = t0 + gid, tb = t0 + gid + 8;
+        if (p.logits) {
+          float* lg = p.logits + ((size_t)r * p.Hq + (size_t)g * p.G) * p.cap * B + (size_t)(i0 + it) * B;
+          const size_t hs = (size_t)p.cap * B;
+          if (h0 < p.G && ta < nv) lg[h0 * hs + ta] = c[0] * p.scale;
+          if (h1 < p.G && ta < nv) lg[h1 * hs + ta] = c[1] * p.scale;
+          if (h0 < p.G && tb < nv) lg[h0 * hs + tb] = c[2] * p.scale;
+          if (h1 < p.G && tb < nv) lg[h1 * hs + tb] = c[3] * p.scale;
+        }
+        const float z0 = (ta < nv) ? c[0] * p.scale_log2 : -INFINITY;
+        const float z1 = (ta < nv) ? c[1] * p.scale_log2 : -INFINITY;
+        const float z2 = (tb < nv) ? c[2] * p.scale_log2 : -INFINITY;
+        const float z3 = (tb < nv) ? c[3] * p.scale_log2 : -INFINITY;
+        float mx0 = fmaxf(z0, z2), mx1 = fmaxf(z1, z3);
+#pragma unroll
+        for (int off = 4; off <= 16; off <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float al0 = (mn0 == -INFINITY) ? 1.0f : pi_exp2(m0 - mn0);
+        const float al1 = (mn1 == -INFINITY) ? 1.0f : pi_exp2(m1 - mn1);
+        const float p0 = (mn0 == -INFINITY) ? 0.0f : pi_exp2(z0 - mn0);
+        const float p1 = (mn1 == -INFINITY) ? 0.0f : pi_exp2(z1 - mn1);
+        const float p2 = (mn0 == -INFINITY) ? 0.0f : pi_exp2(z2 - mn0);
+        const float p3 = (mn1 == -INFINITY) ? 0.0f : pi_exp2(z3 - mn1);
+        m0 = mn0;
+        m1 = mn1;
+        const uint32_t x0 = pi_pack_bf16(p0, p1);  // tokens t0+gid:   heads 2tig, 2tig+1
+        const uint32_t x1 = pi_pack_bf16(p2, p3);  // tokens t0+gid+8
+        l0 = l0 * al0 + (pi_bf16_lo(x0) + pi_bf16_lo(x1));
+        l1 = l1 * al1 + (pi_bf16_hi(x0) + pi_bf16_hi(x1));
+        const uint32_t b0 = pi_movmatrix_trans(x0);
+        const uint32_t b1 = pi_movmatrix_trans(x1);
+        {
+          const int tok = t0 + r8 + ((mat >> 1) << 3);
+#pragma unroll
+          for (int mt = 0; mt < KS; mt++) {
+            o[mt][0] *= al0;
+            o[mt][1] *= al1;
+            o[mt][2] *= al0;
+            o[mt][3] *= al1;
+            const int chunk = ((mt * 16) & 63) / 8 + (mat & 1);
+            const uint32_t addr = vs_base + ((mt * 16) / 64) * S::kSub + tok * 128 + ((chunk ^ (tok & 7)) << 4);
+            uint32_t a[4];
+            pi_ldmatrix_x4_trans(a, addr);
+            pi_mma_bf16(o[mt], a, b0, b1);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) pi_mbar_arrive(&empty[s]);
+    }
+    // row sums over the 8 lanes holding the other tokens of the same heads
+#pragma unroll
+    for (int off = 4; off <= 16; off <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    }
+    consumer_sync();  // every consumer is done reading the stages
+    float* ow = reinterpret_cast<float*>(smem);                 // [4][G][D]
+    float* mlw = ow + kConsumerWarps * p.G * D;                 // [4][G][2]
+#pragma unroll
+    for (int mt = 0; mt < KS; mt++) {
+      const int d = mt * 16 + gid;
+      if (h0 < p.G) {
+        ow[(warp * p.G + h0) * D + d] = o[mt][0];
+        ow[(warp * p.G + h0) * D + d + 8] = o[mt][2];
+      }
+      if (h1 < p.G) {
+        ow[(warp * p.G + h1) * D + d] = o[mt][1];
+        ow[(warp * p.G + h1) * D + d + 8] = o[mt][3];
+      }
+    }
+    if (gid == 0) {
+      if (h0 < p.G) { mlw[(warp * p.G + h0) * 2] = m0; mlw[(warp * p.G + h0) * 2 + 1] = l0; }
+      if (h1 < p.G) { mlw[(warp * p.G + h1) * 2] = m1; mlw[(warp * p.G + h1) * 2 + 1] = l1; }
+    }
+    consumer_sync();
+    const int au = r * p.Hkv + g;
+    float* po = p.part_o + ((size_t)au * p.splits_max + split) * p.G * D;
+    float2* pml = p.part_ml + ((size_t)au * p.splits_max + split) * p.G;
+    for (int e = threadIdx.x; e < p.G * D; e += 128) {
+      const int h = e / D, d = e % D;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; w++) M = fmaxf(M, mlw[(w * p.G + h) * 2]);
+      float acc = 0.0f, lsum = 0.0f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; w++) {
+          const float f = pi_exp2(mlw[(w * p.G + h) * 2] - M);
+          acc += f * ow[(w * p.G + h) * D + d];
+          lsum += f * mlw[(w * p.G + h) * 2 + 1];
+        }
+      }
+      po[h * D + d] = acc;
+      if (d == 0) pml[h] = make_float2(M, lsum);
+    }
+    __threadfence();
+    consumer_sync();
+    if (threadIdx.x == 0) {
+      const unsigned done = atomicAdd(p.counter + au, 1u);
+      flags[0] = (done == (unsigned)p.splits - 1) ? 1 : 0;
+    }
+    consumer_sync();
+    if (flags[0]) {
+      if (threadIdx.x == 0) p.counter[au] = 0;
+      __threadfence();
+      const float* pob = p.part_o + (size_t)au * p.splits_max * p.G * D;
+      const float2* pmb = p.part_ml + (size_t)au * p.splits_max * p.G;
+      for (int e = threadIdx.x; e < p.G * D; e += 128) {
+        const int h = e / D, d = e % D;
+        float M = -INFINITY;
+        for (int s = 0; s < p.splits; s++) M = fmaxf(M, __ldcg(&pmb[s * p.G + h]).x);
+        float acc = 0.0f, lsum = 0.0f;
+        if (M != -INFINITY) {
+          for (int s = 0; s < p.splits; s++) {
+            const float2 ml = __ldcg(&pmb[s * p.G + h]);
+            const float f = pi_exp2(ml.x - M);
+            acc += f * __ldcg(&pob[(s * p.G + h) * D + d]);
+            lsum += f * ml.y;
+          }
+        }
+        const int hq = g * p.G + h;
+        const float v = (lsum > 0.0f) ? acc / lsum : 0.0f;
+        const __nv_bfloat16 bv = __float2bfloat16_rn(v);
+        p.out[((size_t)r * p.Hq + hq) * D + d] = *reinterpret_cast<const uint16_t*>(&bv);
+        if (p.lse && d == 0) p.lse[(size_t)r * p.Hq + hq] = (lsum > 0.0f) ? (M + log2f(lsum)) * 0.69314718055994530942f : -INFINITY;
+      }
+    }
+  }
+  __syncthreads();
+}
+
+template <int D, int B>
+cudaError_t launch_attn(pi_pool* p, const AttnParams& ap, cudaStream_t s) {
+  using S = AttnShape<D, B>;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(attn_kernel<D, B>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  dim3 grid(ap.splits, p->R * p->Hkv);
+  attn_kernel<D, B><<<grid, kThreads, S::kSmem, s>>>(p->tmap, ap);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t pi_launch_attention(pi_pool* p, int layer, const void* q, const int* sel, const int* table,
+                                const int* nsel, void* out, float* lse, float* logits, cudaStream_t s) {
+  AttnParams ap;
+  ap.q = (const uint16_t*)q;
+  ap.sel = sel;
+  ap.table = table;
+  ap.nsel = nsel;
+  ap.ntok = p->ntok;
+  ap.slot_base = p->slot_base;
+  ap.P = p->P;
+  const size_t units = (size_t)p->R * p->Hkv;
+  ap.part_o = p->attn_o + (size_t)layer * units * p->attn_max_splits * p->G * p->D;
+  ap.part_ml = p->attn_ml + (size_t)layer * units * p->attn_max_splits * p->G;
+  ap.counter = p->attn_counter + (size_t)layer * units;
+  ap.out = (uint16_t*)out;
+  ap.lse = lse;
+  ap.logits = logits;
+  ap.status = p->dev_status;
+  ap.layer = layer;
+  ap.L = p->L;
+  ap.Hq = p->Hq;
+  ap.Hkv = p->Hkv;
+  ap.G = p->G;
+  ap.U = p->U;
+  ap.cap = p->cap;
+  ap.splits_max = p->attn_max_splits;
+  // split the selection so that about two CTAs per SM have work
+  int splits = (int)((2LL * p->num_sms + (long long)units - 1) / (long long)units);
+  splits = max(1, min(splits, p->attn_max_splits));
+  int bps = (p->cap + splits - 1) / splits;
+  splits = (p->cap + bps - 1) / bps;
+  ap.splits = splits;
+  ap.bps = bps;
+  ap.scale = 1.0f / sqrtf((float)p->D);
+  ap.scale_log2 = ap.scale * 1.4426950408889634f;
+  if (p->D == 128) {
+    switch (p->B) {
+      case 16: return launch_attn<128, 16>(p, ap, s);
+      case 32: return launch_attn<128, 32>(p, ap, s);
+      case 64: return launch_attn<128, 64>(p, ap, s);
+      case 128: return launch_attn<128, 128>(p, ap, s);
+    }
+  } else if (p->D == 64) {
+    switch (p->B) {
+      case 16: return launch_attn<64, 16>(p, ap, s);
+      case 32: return launch_attn<64, 32>(p, ap, s);
+      case 64: return launch_attn<64, 64>(p, ap, s);
+      case 128: return launch_attn<64, 128>(p, ap, s);
+    }
+  }
+  return cudaErrorInvalidValue;
+}
+
+extern "C" pi_status pi_sparse_decode(pi_pool* p, int layer, const void* q, const int* sel, const int* table,
+                                      const int* nsel, void* out, float* lse, float* logits, pi_stream s) {
+  if (!p || layer < 0 || layer >= p->L || !q || !sel || !table || !nsel || !out) return PI_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(q) & 3) return PI_ERR_INVALID;
+  if (!p->tmap_ok) return PI_ERR_STATE;
+  PI_CUDA_TRY(pi_launch_attention(p, layer, q, sel, table, nsel, out, lse, logits, reinterpret_cast<cudaStream_t>(s)));
+  return PI_OK;
+}

@@ -1,0 +1,227 @@
+// Internal declarations of the GB300 sparse KV-cache offloading library.
+// Host-side pool state, device-side helpers (status word, bounded waits, TMA,
+// mma) and the kernel launchers shared by the translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include <algorithm>
+#include <string>
+#include <vector>
+
+#include "../../include/pi.h"
+
+// --------------------------------------------------------------- device status
+// Sticky error bits, OR-ed by kernels; never a trap.
+enum : unsigned {
+  PI_DEV_BAD_INDEX = 1u,   // an index read from memory was out of range (access skipped)
+  PI_DEV_TIMEOUT = 2u,     // a bounded wait ran out
+  PI_DEV_POOL_FULL = 4u,   // plan found fewer free slots than missing units
+};
+
+#define PI_CUDA_TRY(expr)                                   \
+  do {                                                      \
+    cudaError_t _e = (expr);                                \
+    if (_e != cudaSuccess) {                                \
+      pi_note_cuda_error(_e, #expr, __FILE__, __LINE__);    \
+      return PI_ERR_CUDA;                                   \
+    }                                                       \
+  } while (0)
+
+void pi_note_cuda_error(cudaError_t e, const char* what, const char* file, int line);
+
+// --------------------------------------------------------------- pool
+struct pi_pool {
+  pi_config cfg{};
+  int L = 0, R = 0, Hq = 0, Hkv = 0, D = 0, B = 0, G = 0;
+  int max_blocks = 0, cap = 0, W = 0, k_max = 0, mode = PI_SHARED, U = 1, host_layers = 0;
+  int p_max = 0;
+  size_t block_bytes = 0, frag_bytes = 0, copy_bytes = 0, region_bytes = 0;
+  int device = 0, num_sms = 0;
+
+  // host store (pinned, mapped)
+  uint8_t* host = nullptr;       // host address
+  uint8_t* host_dev = nullptr;   // device address of the same memory
+  size_t host_bytes = 0;
+
+  // device state
+  uint8_t* pool = nullptr;       // all slots
+  long long total_slots = 0;
+  std::vector<long long> slot_base_h;
+  std::vector<int> P_h;
+  long long* slot_base = nullptr; // device [R]
+  int* P = nullptr;               // device [R]
+  float* kmean = nullptr;         // [R][L][max_blocks][Hkv][D]
+  float* tail_sum = nullptr;      // [R][L][Hkv][D]
+  int* ntok = nullptr;            // [R][L]
+  std::vector<int> ntok_h;        // host mirror [R][L]
+  int* slot_of = nullptr;         // [R][L][U][max_blocks]
+  int* block_of = nullptr;        // [R][L][U][p_max]
+  unsigned* dev_status = nullptr;
+
+  // per-layer scratch
+  float* sel_scores = nullptr;    // [L][R*U][max_blocks]
+  unsigned* sel_counter = nullptr;// [L][R*U]
+  int* plan_n = nullptr;          // [L][R*U]
+  int4* plan = nullptr;           // [L][R*U][cap]  (unit block, slot, evicted block, 0)
+  long long* recall_counts = nullptr; // [L][4]: misses, hits (device-accumulated per call)
+  int attn_max_splits = 0;
+  float* attn_o = nullptr;        // [L][R*Hkv][max_splits][G][D]
+  float2* attn_ml = nullptr;      // [L][R*Hkv][max_splits][G]  (m log2-domain, l)
+  unsigned* attn_counter = nullptr; // [L][R*Hkv]
+
+  // decode-step buffers
+  int* step_sel = nullptr;        // [L][R][U][cap]
+  int* step_nsel = nullptr;       // [L][R][U]
+  int* step_table = nullptr;      // [L][R][U][cap]
+  uint8_t* step_in = nullptr;     // host-variant staging of q/k/v/budget on device
+  uint8_t* step_out = nullptr;    // host-variant device out/lse
+  size_t step_in_bytes = 0, step_out_bytes = 0;
+  std::vector<cudaEvent_t> ev_sel, ev_rec;
+  cudaEvent_t ev_start = nullptr;
+  int* ntok_stage = nullptr;      // [L][R] token counts staged by pi_update_summaries
+
+  // staged arm
+  uint8_t* stage_host = nullptr;  // pinned
+  uint8_t* stage_dev = nullptr;
+  long long stage_units = 0;
+  std::vector<int4> plan_h;       // host copy of a plan
+  std::vector<int> plan_n_h;
+
+  // attention tensor map over the whole device pool (rows of D bf16)
+  CUtensorMap tmap{};
+  bool tmap_ok = false;
+
+  // per-kernel timing inside pi_decode_step: events [step][layer][kind][2]
+  std::vector<cudaEvent_t> tev;
+  int timing_steps = 0, timing_used = 0;
+
+  // fault injection
+  long long fault_recall_at = 0;
+  long long recall_calls = 0;
+};
+
+// --------------------------------------------------------------- helpers
+static inline long long pi_global_slot(const pi_pool* p, int r, int l, int s) {
+  return p->slot_base_h[r] + (long long)l * p->P_h[r] + s;
+}
+
+// kernel launchers (return cudaGetLastError of the launch)
+cudaError_t pi_launch_summaries(pi_pool* p, int layer, const uint8_t* src, bool src_is_host, int b0, int b1,
+                                cudaStream_t s, const int* ntok_new);
+cudaError_t pi_launch_append(pi_pool* p, int layer, const void* k_new, const void* v_new, cudaStream_t s);
+cudaError_t pi_launch_select(pi_pool* p, int layer, const void* q, const int* k_per_req, int* sel, int* nsel,
+                             cudaStream_t s);
+cudaError_t pi_launch_plan(pi_pool* p, int layer, const int* sel, const int* nsel, int* table, cudaStream_t s);
+cudaError_t pi_launch_gather(pi_pool* p, int layer, const uint8_t* stage_src, bool copy, bool commit,
+                             cudaStream_t s);
+cudaError_t pi_launch_attention(pi_pool* p, int layer, const void* q, const int* sel, const int* table,
+                                const int* nsel, void* out, float* lse, float* logits, cudaStream_t s);
+bool pi_make_tmap(pi_pool* p);
+
+// --------------------------------------------------------------- device helpers
+#ifdef __CUDACC__
+__device__ __forceinline__ void pi_flag(unsigned* status, unsigned bit) { atomicOr(status, bit); }
+
+__device__ __forceinline__ float pi_bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float pi_bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint32_t pi_smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void pi_mbar_init(uint64_t* bar, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(pi_smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void pi_mbar_arrive(uint64_t* bar) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(pi_smem_addr(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void pi_mbar_arrive_expect_tx(uint64_t* bar, unsigned bytes) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(
+                   pi_smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool pi_mbar_try_wait(uint64_t* bar, unsigned parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(pi_smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase of `parity` to complete; gives up after ~`limit` cycles
+// (about a second), flags PI_DEV_TIMEOUT and returns false.
+__device__ __forceinline__ bool pi_mbar_wait_bounded(uint64_t* bar, unsigned parity, unsigned* status,
+                                                     long long limit = 2000000000LL) {
+  if (pi_mbar_try_wait(bar, parity)) return true;
+  long long t0 = clock64();
+  while (!pi_mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > limit) {
+      pi_flag(status, PI_DEV_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ void pi_fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// 2D tiled TMA load global -> shared, completion on an mbarrier.
+__device__ __forceinline__ void pi_tma_load_2d(void* smem_dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+          "r"(pi_smem_addr(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(pi_smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void pi_ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void pi_ldmatrix_x4_trans(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ uint32_t pi_movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+// D(16x8 fp32) += A(16x16 bf16, row) * B(16x8 bf16, col)
+__device__ __forceinline__ void pi_mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pi_pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float pi_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+#endif

@@ -1,0 +1,374 @@
+// Pool lifetime, views, residency control, device status and fault injection.
+//
+// The pool follows the architecture of "PulseInfer Guide: I/O-Centric Sparse
+// KV Cache Offloading", section "PulseInfer Architectural Foundations": a
+// global offloaded KV store in host DRAM (here pinned and mapped into the GPU's
+// address space so kernels can read it directly), and a paged KV block pool in
+// HBM that recalled blocks are written into.
+#include <cudaTypedefs.h>
+
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+
+#include "pi_internal.cuh"
+
+static thread_local char g_last_cuda_error[256];
+
+void pi_note_cuda_error(cudaError_t e, const char* what, const char* file, int line) {
+  snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "%s: %s (%s:%d)", cudaGetErrorString(e), what, file, line);
+  if (getenv("PI_VERBOSE")) fprintf(stderr, "[pi] %s\n", g_last_cuda_error);
+}
+
+extern "C" int pi_abi_version(void) { return PI_ABI_VERSION; }
+
+extern "C" const char* pi_status_str(pi_status s) {
+  switch (s) {
+    case PI_OK: return "ok";
+    case PI_ERR_INVALID: return "invalid argument";
+    case PI_ERR_CUDA: return "CUDA error";
+    case PI_ERR_OOM: return "device out of memory";
+    case PI_ERR_HOST_ALLOC: return "pinned host allocation failed";
+    case PI_ERR_POOL_FULL: return "pool has fewer free slots than missing blocks";
+    case PI_ERR_TIMEOUT: return "bounded device wait timed out";
+    case PI_ERR_DEVICE: return "device-side index check failed";
+    case PI_ERR_STATE: return "call not valid in this pool state or mode";
+    case PI_ERR_FAULT_INJECTED: return "injected fault";
+  }
+  return "unknown status";
+}
+
+static void pool_free(pi_pool* p) {
+  if (!p) return;
+  for (auto e : p->ev_sel) cudaEventDestroy(e);
+  for (auto e : p->ev_rec) cudaEventDestroy(e);
+  if (p->ev_start) cudaEventDestroy(p->ev_start);
+  for (auto e : p->tev) cudaEventDestroy(e);
+  void* dev_ptrs[] = {p->pool,       p->slot_base,  p->P,          p->kmean,       p->tail_sum,    p->ntok,
+                      p->slot_of,    p->block_of,   p->dev_status, p->sel_scores,  p->sel_counter, p->plan_n,
+                      p->plan,       p->recall_counts, p->attn_o,  p->attn_ml,     p->attn_counter, p->step_sel,
+                      p->step_nsel,  p->step_table, p->step_in,    p->step_out,    p->stage_dev,
+                      p->ntok_stage};
+  for (void* d : dev_ptrs)
+    if (d) cudaFree(d);
+  if (p->host) cudaFreeHost(p->host);
+  if (p->stage_host) cudaFreeHost(p->stage_host);
+  delete p;
+}
+
+static pi_status parse_fault(pi_pool* p, const char* spec) {
+  p->fault_recall_at = 0;
+  if (!spec || !*spec) return PI_OK;
+  long long n = 0;
+  if (sscanf(spec, "recall_fail@%lld", &n) == 1 && n > 0) {
+    p->fault_recall_at = n;
+    p->recall_calls = 0;
+    return PI_OK;
+  }
+  if (strcmp(spec, "pinned_alloc_fail") == 0) return PI_OK;  // only meaningful at creation
+  return PI_ERR_INVALID;
+}
+
+static bool valid_config(const pi_config& c) {
+  if (c.layers <= 0 || c.batch <= 0 || c.hq <= 0 || c.hkv <= 0) return false;
+  if (c.hq % c.hkv != 0 || c.hq / c.hkv > 8) return false;
+  if (c.head_dim != 64 && c.head_dim != 128) return false;
+  if (c.block_tokens != 16 && c.block_tokens != 32 && c.block_tokens != 64 && c.block_tokens != 128) return false;
+  if (c.max_blocks <= 0 || c.max_blocks > 65536) return false;
+  if (c.k_max < 0 || c.window < 0 || c.k_max + c.window <= 0) return false;
+  if ((long long)c.max_blocks * c.block_tokens > (1LL << 30)) return false;
+  if (c.select_mode != PI_SHARED && c.select_mode != PI_HEADWISE) return false;
+  if (c.host_layers < 0 || c.host_layers > c.layers) return false;
+  if (c.hkv * c.head_dim > 1024) return false;  // selection keeps one block's summary per warp pass
+  int cap = c.k_max + c.window;
+  if (c.pool_slots_per_req) {
+    for (int r = 0; r < c.batch; r++)
+      if (c.pool_slots_per_req[r] < cap) return false;
+  } else if (c.pool_slots < cap) {
+    return false;
+  }
+  return true;
+}
+
+template <typename T>
+static pi_status dalloc(T** ptr, size_t count, bool zero = true, int fill_byte = 0) {
+  size_t bytes = count * sizeof(T);
+  if (bytes == 0) bytes = sizeof(T);
+  if (cudaMalloc(reinterpret_cast<void**>(ptr), bytes) != cudaSuccess) {
+    cudaGetLastError();
+    *ptr = nullptr;
+    return PI_ERR_OOM;
+  }
+  if (zero && cudaMemset(*ptr, fill_byte, bytes) != cudaSuccess) return PI_ERR_CUDA;
+  return PI_OK;
+}
+
+extern "C" pi_status pi_pool_create(const pi_config* cfg, pi_pool** out) {
+  if (!cfg || !out) return PI_ERR_INVALID;
+  *out = nullptr;
+  if (!valid_config(*cfg)) return PI_ERR_INVALID;
+  pi_pool* p = new pi_pool();
+  p->cfg = *cfg;
+  p->cfg.pool_slots_per_req = nullptr;  // do not keep the caller's pointer
+  p->L = cfg->layers;
+  p->R = cfg->batch;
+  p->Hq = cfg->hq;
+  p->Hkv = cfg->hkv;
+  p->D = cfg->head_dim;
+  p->B = cfg->block_tokens;
+  p->G = p->Hq / p->Hkv;
+  p->max_blocks = cfg->max_blocks;
+  p->k_max = cfg->k_max;
+  p->W = cfg->window;
+  p->cap = p->k_max + p->W;
+  p->mode = cfg->select_mode;
+  p->U = (p->mode == PI_HEADWISE) ? p->Hkv : 1;
+  p->host_layers = cfg->host_layers > 0 ? cfg->host_layers : p->L;
+  p->frag_bytes = (size_t)2 * p->B * p->D * 2;
+  p->block_bytes = p->frag_bytes * p->Hkv;
+  p->copy_bytes = (p->mode == PI_HEADWISE) ? p->frag_bytes : p->block_bytes;
+  p->region_bytes = p->block_bytes * (size_t)p->max_blocks;
+  p->ntok_h.assign((size_t)p->R * p->L, 0);
+
+  if (cudaGetDevice(&p->device) != cudaSuccess) { pool_free(p); return PI_ERR_CUDA; }
+  cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device);
+  if (p->num_sms <= 0) p->num_sms = 148;
+
+  const char* fault = getenv("PI_FAULT");
+  if (parse_fault(p, fault) != PI_OK) { pool_free(p); return PI_ERR_INVALID; }
+
+  // per-request slot counts and global slot offsets
+  p->P_h.resize(p->R);
+  p->slot_base_h.resize(p->R);
+  long long acc = 0;
+  for (int r = 0; r < p->R; r++) {
+    p->P_h[r] = cfg->pool_slots_per_req ? cfg->pool_slots_per_req[r] : cfg->pool_slots;
+    p->p_max = p->P_h[r] > p->p_max ? p->P_h[r] : p->p_max;
+    p->slot_base_h[r] = acc;
+    acc += (long long)p->L * p->P_h[r];
+  }
+  p->total_slots = acc;
+
+  // host store: pinned and mapped
+  p->host_bytes = p->region_bytes * (size_t)p->host_layers * (size_t)p->R;
+  if (fault && strcmp(fault, "pinned_alloc_fail") == 0) { pool_free(p); return PI_ERR_HOST_ALLOC; }
+  if (cudaHostAlloc(reinterpret_cast<void**>(&p->host), p->host_bytes, cudaHostAllocMapped | cudaHostAllocPortable) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    p->host = nullptr;
+    pool_free(p);
+    return PI_ERR_HOST_ALLOC;
+  }
+  memset(p->host, 0, p->host_bytes);
+  if (cudaHostGetDevicePointer(reinterpret_cast<void**>(&p->host_dev), p->host, 0) != cudaSuccess) {
+    pool_free(p);
+    return PI_ERR_CUDA;
+  }
+
+  pi_status st = PI_OK;
+  const size_t RL = (size_t)p->R * p->L, RU = (size_t)p->R * p->U;
+#define TRY_ALLOC(expr)      \
+  do {                       \
+    st = (expr);             \
+    if (st != PI_OK) {       \
+      pool_free(p);          \
+      return st;             \
+    }                        \
+  } while (0)
+  TRY_ALLOC(dalloc(&p->pool, (size_t)p->total_slots * p->block_bytes));
+  TRY_ALLOC(dalloc(&p->slot_base, (size_t)p->R, false));
+  TRY_ALLOC(dalloc(&p->P, (size_t)p->R, false));
+  TRY_ALLOC(dalloc(&p->kmean, RL * p->max_blocks * p->Hkv * p->D));
+  TRY_ALLOC(dalloc(&p->tail_sum, RL * p->Hkv * p->D));
+  TRY_ALLOC(dalloc(&p->ntok, RL));
+  TRY_ALLOC(dalloc(&p->ntok_stage, RL));
+  TRY_ALLOC(dalloc(&p->slot_of, RL * p->U * p->max_blocks, true, 0xFF));
+  TRY_ALLOC(dalloc(&p->block_of, RL * p->U * p->p_max, true, 0xFF));
+  TRY_ALLOC(dalloc(&p->dev_status, 1));
+  TRY_ALLOC(dalloc(&p->sel_scores, (size_t)p->L * RU * p->max_blocks));
+  TRY_ALLOC(dalloc(&p->sel_counter, (size_t)p->L * RU));
+  TRY_ALLOC(dalloc(&p->plan_n, (size_t)p->L * RU));
+  TRY_ALLOC(dalloc(&p->plan, (size_t)p->L * RU * p->cap));
+  TRY_ALLOC(dalloc(&p->recall_counts, (size_t)p->L * 4));
+  // attention split-K partials: enough splits to give every SM work at any batch
+  {
+    int units = p->R * p->Hkv;
+    int s = (4 * p->num_sms + units - 1) / units;
+    if (s < 1) s = 1;
+    if (s > p->cap) s = p->cap;
+    p->attn_max_splits = s;
+  }
+  TRY_ALLOC(dalloc(&p->attn_o, (size_t)p->L * p->R * p->Hkv * p->attn_max_splits * p->G * p->D, false));
+  TRY_ALLOC(dalloc(&p->attn_ml, (size_t)p->L * p->R * p->Hkv * p->attn_max_splits * p->G, false));
+  TRY_ALLOC(dalloc(&p->attn_counter, (size_t)p->L * p->R * p->Hkv));
+  TRY_ALLOC(dalloc(&p->step_sel, (size_t)p->L * RU * p->cap));
+  TRY_ALLOC(dalloc(&p->step_nsel, (size_t)p->L * RU));
+  TRY_ALLOC(dalloc(&p->step_table, (size_t)p->L * RU * p->cap));
+  p->step_in_bytes = (size_t)p->L * p->R * ((size_t)p->Hq * p->D * 2 + (size_t)2 * p->Hkv * p->D * 2 + 4);
+  p->step_out_bytes = (size_t)p->L * p->R * ((size_t)p->Hq * p->D * 2 + (size_t)p->Hq * 4);
+  TRY_ALLOC(dalloc(&p->step_in, p->step_in_bytes, false));
+  TRY_ALLOC(dalloc(&p->step_out, p->step_out_bytes, false));
+#undef TRY_ALLOC
+
+  if (cudaMemcpy(p->slot_base, p->slot_base_h.data(), sizeof(long long) * p->R, cudaMemcpyHostToDevice) !=
+          cudaSuccess ||
+      cudaMemcpy(p->P, p->P_h.data(), sizeof(int) * p->R, cudaMemcpyHostToDevice) != cudaSuccess) {
+    pool_free(p);
+    return PI_ERR_CUDA;
+  }
+
+  if (cudaEventCreateWithFlags(&p->ev_start, cudaEventDisableTiming) != cudaSuccess) {
+    pool_free(p);
+    return PI_ERR_CUDA;
+  }
+  p->ev_sel.resize(p->L);
+  p->ev_rec.resize(p->L);
+  for (int l = 0; l < p->L; l++) {
+    if (cudaEventCreateWithFlags(&p->ev_sel[l], cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&p->ev_rec[l], cudaEventDisableTiming) != cudaSuccess) {
+      pool_free(p);
+      return PI_ERR_CUDA;
+    }
+  }
+  if (!pi_make_tmap(p)) {
+    pool_free(p);
+    return PI_ERR_CUDA;
+  }
+  if (cudaDeviceSynchronize() != cudaSuccess) {
+    pool_free(p);
+    return PI_ERR_CUDA;
+  }
+  *out = p;
+  return PI_OK;
+}
+
+extern "C" pi_status pi_pool_destroy(pi_pool* p) {
+  if (!p) return PI_ERR_INVALID;
+  cudaDeviceSynchronize();
+  pool_free(p);
+  return PI_OK;
+}
+
+extern "C" pi_status pi_pool_get_config(const pi_pool* p, pi_config* out) {
+  if (!p || !out) return PI_ERR_INVALID;
+  *out = p->cfg;
+  return PI_OK;
+}
+
+extern "C" pi_status pi_pool_get_views(pi_pool* p, pi_pool_views* v) {
+  if (!p || !v) return PI_ERR_INVALID;
+  v->pool = p->pool;
+  v->slot_base = p->slot_base_h.data();
+  v->slots_per_req = p->P_h.data();
+  v->kmean = p->kmean;
+  v->ntok = p->ntok;
+  v->slot_of_block = p->slot_of;
+  v->block_of_slot = p->block_of;
+  v->p_max = p->p_max;
+  v->step_sel = p->step_sel;
+  v->step_nsel = p->step_nsel;
+  v->step_table = p->step_table;
+  v->block_bytes = p->block_bytes;
+  v->frag_bytes = p->frag_bytes;
+  v->host_region_bytes = p->region_bytes;
+  return PI_OK;
+}
+
+extern "C" void* pi_host_kv(pi_pool* p, int layer, int req) {
+  if (!p || layer < 0 || layer >= p->L || req < 0 || req >= p->R) return nullptr;
+  int hl = layer % p->host_layers;
+  return p->host + ((size_t)hl * p->R + req) * p->region_bytes;
+}
+
+extern "C" pi_status pi_set_fault(pi_pool* p, const char* spec) {
+  if (!p) return PI_ERR_INVALID;
+  return parse_fault(p, spec);
+}
+
+extern "C" pi_status pi_get_device_status(pi_pool* p) {
+  if (!p) return PI_ERR_INVALID;
+  PI_CUDA_TRY(cudaDeviceSynchronize());
+  unsigned w = 0;
+  PI_CUDA_TRY(cudaMemcpy(&w, p->dev_status, sizeof(unsigned), cudaMemcpyDeviceToHost));
+  if (w & PI_DEV_BAD_INDEX) return PI_ERR_DEVICE;
+  if (w & PI_DEV_TIMEOUT) return PI_ERR_TIMEOUT;
+  if (w & PI_DEV_POOL_FULL) return PI_ERR_POOL_FULL;
+  return PI_OK;
+}
+
+extern "C" pi_status pi_clear_device_status(pi_pool* p) {
+  if (!p) return PI_ERR_INVALID;
+  PI_CUDA_TRY(cudaDeviceSynchronize());
+  PI_CUDA_TRY(cudaMemset(p->dev_status, 0, sizeof(unsigned)));
+  return PI_OK;
+}
+
+extern "C" pi_status pi_pool_flush(pi_pool* p, int layer, pi_stream s) {
+  if (!p || layer < -1 || layer >= p->L) return PI_ERR_INVALID;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(s);
+  for (int r = 0; r < p->R; r++)
+    for (int l = 0; l < p->L; l++) {
+      if (layer >= 0 && l != layer) continue;
+      size_t rl = (size_t)r * p->L + l;
+      PI_CUDA_TRY(cudaMemsetAsync(p->slot_of + rl * p->U * p->max_blocks, 0xFF,
+                                  sizeof(int) * p->U * p->max_blocks, st));
+      PI_CUDA_TRY(cudaMemsetAsync(p->block_of + rl * p->U * p->p_max, 0xFF, sizeof(int) * p->U * p->p_max, st));
+    }
+  return PI_OK;
+}
+
+extern "C" pi_status pi_pool_preload(pi_pool* p, int layer, int req, const int* blocks, int n, pi_stream s) {
+  if (!p || layer < 0 || layer >= p->L || req < 0 || req >= p->R || n < 0 || (n > 0 && !blocks))
+    return PI_ERR_INVALID;
+  if (p->mode != PI_SHARED) return PI_ERR_STATE;
+  if (n > p->P_h[req]) return PI_ERR_INVALID;
+  for (int i = 0; i < n; i++) {
+    if (blocks[i] < 0 || blocks[i] >= p->max_blocks) return PI_ERR_INVALID;
+    if (i > 0 && blocks[i] <= blocks[i - 1]) return PI_ERR_INVALID;
+  }
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(s);
+  PI_CUDA_TRY(cudaStreamSynchronize(st));
+  size_t rl = (size_t)req * p->L + layer;
+  std::vector<int> sob(p->max_blocks, -1), bos(p->p_max, -1);
+  for (int i = 0; i < n; i++) {
+    sob[blocks[i]] = i;
+    bos[i] = blocks[i];
+  }
+  PI_CUDA_TRY(cudaMemcpy(p->slot_of + rl * p->max_blocks, sob.data(), sizeof(int) * p->max_blocks,
+                         cudaMemcpyHostToDevice));
+  PI_CUDA_TRY(cudaMemcpy(p->block_of + rl * p->p_max, bos.data(), sizeof(int) * p->p_max, cudaMemcpyHostToDevice));
+  const uint8_t* src = (const uint8_t*)pi_host_kv(p, layer, req);
+  for (int i = 0; i < n; i++) {
+    uint8_t* dst = p->pool + (size_t)pi_global_slot(p, req, layer, i) * p->block_bytes;
+    PI_CUDA_TRY(cudaMemcpyAsync(dst, src + (size_t)blocks[i] * p->block_bytes, p->block_bytes,
+                                cudaMemcpyHostToDevice, st));
+  }
+  PI_CUDA_TRY(cudaStreamSynchronize(st));
+  return PI_OK;
+}
+
+// Tensor map over the device pool seen as rows of D bf16 (one row = one token of
+// one head's K or V). Row of (global slot gs, head g, kv, token t) =
+// ((gs * Hkv + g) * 2 + kv) * B + t. Boxes are 64 elements (128 bytes) wide and
+// B rows high, 128-byte swizzled, so a block's K or V of one head is D/64 boxes.
+bool pi_make_tmap(pi_pool* p) {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn) {
+    cudaGetLastError();
+    return false;
+  }
+  auto encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  unsigned long long rows = (unsigned long long)p->total_slots * p->Hkv * 2 * p->B;
+  if (rows >= (1ULL << 31)) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)p->D, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)p->D * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)p->B};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = encode(&p->tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->pool, dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  p->tmap_ok = (r == CUDA_SUCCESS);
+  return p->tmap_ok;
+}

@@ -1,0 +1,470 @@
+// Block summaries, token append and SoloHead-style shared top-k selection.
+//
+// "PulseInfer Guide: I/O-Centric Sparse KV Cache Offloading", section "SoloHead
+// Sparse Selection": one block set is chosen for all heads of a layer so a
+// recall moves whole blocks instead of per-head fragments. The guide leaves the
+// per-block importance undefined; this library scores a block by
+// sum_h q_h . kmean[b, h/G] in fp32, where kmean is the per-KV-head mean key of
+// the block (the summary kept for every block), and keeps the W most recent
+// blocks unconditionally.
+//
+// Bit-exact contract with the CPU oracle: summaries are a sequential fp32 sum in
+// token order divided by the token count (IEEE division); the score uses one
+// fixed fp32 order (per-lane fused multiply-add over elements 128c+4*lane+j,
+// then a xor butterfly); ties go to the lower block index.
+#include "pi_internal.cuh"
+
+namespace {
+
+constexpr int kSelThreads = 256;
+
+__device__ __forceinline__ float bf16_at(const uint16_t* p) { return __uint_as_float((uint32_t)(*p) << 16); }
+
+// ------------------------------------------------------------------ a-1
+// grid (blocks in range, R); one thread per 8 consecutive elements of one head.
+__global__ void summaries_kernel(const uint8_t* __restrict__ src, long long src_req_stride,
+                                 const int* __restrict__ ntok_new, int* __restrict__ ntok, float* __restrict__ kmean,
+                                 float* __restrict__ tail_sum, int layer, int L, int Hkv, int B, int D, int max_blocks,
+                                 int b0) {
+  const int r = blockIdx.y;
+  const int nt = ntok_new[r];
+  if (blockIdx.x == 0 && threadIdx.x == 0) ntok[(size_t)r * L + layer] = nt;
+  const int nb = (nt + B - 1) / B;
+  const int b = b0 + blockIdx.x;
+  if (b >= nb) return;
+  const int nv = min(B, nt - b * B);
+  const int e = threadIdx.x * 8;
+  if (e >= Hkv * D) return;
+  const int g = e / D, d = e % D;
+  const size_t block_bytes = (size_t)Hkv * 2 * B * D * 2;
+  const uint8_t* row = src + (size_t)r * src_req_stride + (size_t)b * block_bytes + ((size_t)g * 2 * B * D + d) * 2;
+  float s[8];
+#pragma unroll
+  for (int j = 0; j < 8; j++) s[j] = 0.0f;
+  for (int t = 0; t < nv; t++) {
+    uint4 v = *reinterpret_cast<const uint4*>(row + (size_t)t * D * 2);
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+      s[2 * j] = __fadd_rn(s[2 * j], pi_bf16_lo(w[j]));
+      s[2 * j + 1] = __fadd_rn(s[2 * j + 1], pi_bf16_hi(w[j]));
+    }
+  }
+  const size_t rl = (size_t)r * L + layer;
+  float* km = kmean + ((rl * max_blocks + b) * Hkv + g) * D + d;
+  const float fn = (float)nv;
+#pragma unroll
+  for (int j = 0; j < 8; j++) km[j] = __fdiv_rn(s[j], fn);
+  if (b == nb - 1) {
+    float* ts = tail_sum + (rl * Hkv + g) * D + d;
+#pragma unroll
+    for (int j = 0; j < 8; j++) ts[j] = s[j];
+  }
+}
+
+// ------------------------------------------------------------------ a-7
+struct AppendParams {
+  const uint8_t* k_new;
+  const uint8_t* v_new;
+  uint8_t* host_dev;      // device address of the host store
+  uint8_t* pool;
+  const long long* slot_base;
+  const int* P;
+  const int* slot_of;
+  int* ntok;
+  float* kmean;
+  float* tail_sum;
+  unsigned* status;
+  int layer, L, R, Hkv, B, D, U, max_blocks, host_layer;
+};
+
+// grid R; one thread per 8 consecutive elements of one head
+__global__ void append_kernel(AppendParams a) {
+  const int r = blockIdx.x;
+  const size_t rl = (size_t)r * a.L + a.layer;
+  const int t = a.ntok[rl];
+  const int b = t / a.B, tp = t % a.B;
+  const int e = threadIdx.x * 8;
+  const bool active = e < a.Hkv * a.D;
+  if (b >= a.max_blocks) {
+    if (threadIdx.x == 0) pi_flag(a.status, PI_DEV_BAD_INDEX);
+    return;
+  }
+  if (active) {
+    const int g = e / a.D, d = e % a.D;
+    const size_t block_bytes = (size_t)a.Hkv * 2 * a.B * a.D * 2;
+    const uint4 kv = *reinterpret_cast<const uint4*>(a.k_new + (((size_t)r * a.Hkv + g) * a.D + d) * 2);
+    const uint4 vv = *reinterpret_cast<const uint4*>(a.v_new + (((size_t)r * a.Hkv + g) * a.D + d) * 2);
+    const size_t in_block_k = (((size_t)g * 2 + 0) * a.B + tp) * a.D * 2 + (size_t)d * 2;
+    const size_t in_block_v = (((size_t)g * 2 + 1) * a.B + tp) * a.D * 2 + (size_t)d * 2;
+    uint8_t* host_blk =
+        a.host_dev + (((size_t)a.host_layer * a.R + r) * a.max_blocks + b) * block_bytes;
+    *reinterpret_cast<uint4*>(host_blk + in_block_k) = kv;
+    *reinterpret_cast<uint4*>(host_blk + in_block_v) = vv;
+    const int u = (a.U == 1) ? 0 : g;
+    const int slot = a.slot_of[(rl * a.U + u) * a.max_blocks + b];
+    if (slot >= 0) {
+      if (slot >= a.P[r]) {
+        pi_flag(a.status, PI_DEV_BAD_INDEX);
+      } else {
+        const long long gs = a.slot_base[r] + (long long)a.layer * a.P[r] + slot;
+        uint8_t* pool_blk = a.pool + (size_t)gs * block_bytes;
+        *reinterpret_cast<uint4*>(pool_blk + in_block_k) = kv;
+        *reinterpret_cast<uint4*>(pool_blk + in_block_v) = vv;
+      }
+    }
+    // running fp32 sum of the block's keys in token order == a fresh sequential sum
+    float* ts = a.tail_sum + (rl * a.Hkv + g) * a.D + d;
+    float* km = a.kmean + ((rl * a.max_blocks + b) * a.Hkv + g) * a.D + d;
+    const uint32_t w[4] = {kv.x, kv.y, kv.z, kv.w};
+    const float fn = (float)(tp + 1);
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+      float s0 = (tp == 0) ? 0.0f : ts[2 * j];
+      float s1 = (tp == 0) ? 0.0f : ts[2 * j + 1];
+      s0 = __fadd_rn(s0, pi_bf16_lo(w[j]));
+      s1 = __fadd_rn(s1, pi_bf16_hi(w[j]));
+      ts[2 * j] = s0;
+      ts[2 * j + 1] = s1;
+      km[2 * j] = __fdiv_rn(s0, fn);
+      km[2 * j + 1] = __fdiv_rn(s1, fn);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) a.ntok[rl] = t + 1;
+}
+
+// ------------------------------------------------------------------ a-2
+struct SelParams {
+  const uint16_t* q;
+  const int* k_per_req;
+  int* sel;
+  int* nsel;
+  const float* kmean;
+  const int* ntok;
+  float* scores;       // [R*U][max_blocks] for this layer
+  unsigned* counter;   // [R*U] for this layer
+  unsigned* status;
+  int layer, L, Hq, Hkv, G, D, B, max_blocks, W, k_max, cap, U, bpc;
+};
+
+__device__ __forceinline__ uint32_t order_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  if ((u << 1) == 0) u = 0;  // -0.0 ranks as +0.0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// exclusive scan over the CTA (kSelThreads threads); returns the prefix, sets total
+__device__ __forceinline__ int cta_excl_scan(int v, int* warp_sums, int& total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sums[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    int s = (lane < kSelThreads / 32) ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    if (lane < kSelThreads / 32) warp_sums[lane] = s;  // inclusive warp prefix
+  }
+  __syncthreads();
+  const int before = (w == 0) ? 0 : warp_sums[w - 1];
+  total = warp_sums[kSelThreads / 32 - 1];
+  __syncthreads();
+  return before + x - v;
+}
+
+__global__ void __launch_bounds__(kSelThreads) select_kernel(SelParams p) {
+  __shared__ __align__(16) float qs[1024];
+  __shared__ int hist[256];
+  __shared__ int warp_sums[kSelThreads / 32];
+  __shared__ int bcast[4];
+  const int u = blockIdx.y;
+  const int r = u / p.U;
+  const int g = (p.U == 1) ? 0 : u % p.U;
+  const int E = (p.U == 1) ? p.Hkv * p.D : p.D;
+  const int goff = (p.U == 1) ? 0 : g * p.D;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const size_t rl = (size_t)r * p.L + p.layer;
+  const int nt = p.ntok[rl];
+  const int nb = (nt + p.B - 1) / p.B;
+  const int ncand = max(0, nb - p.W);
+
+  // qsum[e] = sum over the group's query heads (ascending) of q[h][d], fp32
+  for (int e = threadIdx.x; e < E; e += kSelThreads) {
+    const int gg = (p.U == 1) ? e / p.D : g;
+    const int d = e % p.D;
+    const uint16_t* qh = p.q + ((size_t)r * p.Hq + (size_t)gg * p.G) * p.D + d;
+    float s = 0.0f;
+    for (int j = 0; j < p.G; j++) s = __fadd_rn(s, bf16_at(qh + (size_t)j * p.D));
+    qs[e] = s;
+  }
+  __syncthreads();
+
+  // scores of this CTA's candidates: one warp per block, canonical lane order
+  const int b_begin = blockIdx.x * p.bpc;
+  const int b_end = min(ncand, b_begin + p.bpc);
+  float* sc = p.scores + (size_t)u * p.max_blocks;
+  const int chunks = (E + 127) / 128;
+  for (int b = b_begin + warp; b < b_end; b += kSelThreads / 32) {
+    const float* km = p.kmean + ((rl * p.max_blocks + b) * p.Hkv) * p.D + goff;
+    float4 kv[8];
+#pragma unroll
+    for (int c = 0; c < 8; c++) {
+      const int e = 128 * c + 4 * lane;
+      if (c < chunks && e < E) kv[c] = __ldg(reinterpret_cast<const float4*>(km + e));
+    }
+    float acc = 0.0f;
+#pragma unroll
+    for (int c = 0; c < 8; c++) {
+      const int e = 128 * c + 4 * lane;
+      if (c < chunks && e < E) {
+        const float4 qv = *reinterpret_cast<const float4*>(qs + e);
+        acc = __fmaf_rn(qv.x, kv[c].x, acc);
+        acc = __fmaf_rn(qv.y, kv[c].y, acc);
+        acc = __fmaf_rn(qv.z, kv[c].z, acc);
+        acc = __fmaf_rn(qv.w, kv[c].w, acc);
+      }
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, off));
+    if (lane == 0) sc[b] = acc;
+  }
+
+  // the last CTA of this unit to finish runs the top-k
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned done = atomicAdd(p.counter + u, 1u);
+    bcast[0] = (done == gridDim.x - 1) ? 1 : 0;
+  }
+  __syncthreads();
+  if (!bcast[0]) return;
+  if (threadIdx.x == 0) p.counter[u] = 0;  // ready for the next call
+  __threadfence();
+
+  int kreq = p.k_per_req[r];
+  kreq = max(0, min(kreq, p.k_max));
+  const int kk = min(kreq, ncand);
+  int* out = p.sel + (size_t)u * p.cap;
+
+  uint32_t T = 0;      // key of the kk-th largest candidate
+  int need_eq = 0;     // how many candidates equal to T to take (lowest indices)
+  const bool take_all = (kk == ncand);
+  if (kk > 0 && !take_all) {
+    uint32_t prefix = 0, mask = 0;
+    int remaining = kk;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      hist[threadIdx.x] = 0;  // kSelThreads == 256 bins
+      __syncthreads();
+      for (int b = threadIdx.x; b < ncand; b += kSelThreads) {
+        const uint32_t key = order_key(__ldcg(sc + b));
+        if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255], 1);
+      }
+      __syncthreads();
+      if (warp == 0) {
+        // lane owns digits 255-8*lane .. 248-8*lane (descending)
+        int cnt[8], own = 0;
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+          cnt[j] = hist[255 - 8 * lane - j];
+          own += cnt[j];
+        }
+        int incl = own;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const unsigned hit = __ballot_sync(0xffffffffu, incl >= remaining);
+        const int first = __ffs(hit) - 1;
+        if (lane == first) {
+          int before = incl - own;
+          int digit = 255 - 8 * lane - 7;
+#pragma unroll
+          for (int j = 0; j < 8; j++) {
+            if (before + cnt[j] >= remaining) {
+              digit = 255 - 8 * lane - j;
+              break;
+            }
+            before += cnt[j];
+          }
+          bcast[1] = digit;
+          bcast[2] = remaining - before;
+        }
+      }
+      __syncthreads();
+      prefix |= (uint32_t)bcast[1] << shift;
+      mask |= 0xFFu << shift;
+      remaining = bcast[2];
+      __syncthreads();
+    }
+    T = prefix;
+    need_eq = remaining;
+  }
+
+  // stable compaction in block order: all keys > T, then the first need_eq == T
+  int out_n = 0, eq_seen = 0;
+  if (kk > 0) {
+    for (int base = 0; base < ncand; base += kSelThreads) {
+      const int b = base + threadIdx.x;
+      int gt = 0, eq = 0;
+      if (b < ncand) {
+        if (take_all) {
+          gt = 1;
+        } else {
+          const uint32_t key = order_key(__ldcg(sc + b));
+          gt = key > T;
+          eq = key == T;
+        }
+      }
+      int eq_total;
+      const int eq_before = cta_excl_scan(eq, warp_sums, eq_total);
+      const int take = gt || (eq && (eq_seen + eq_before) < need_eq);
+      int take_total;
+      const int pos = cta_excl_scan(take, warp_sums, take_total);
+      if (take && out_n + pos < kk) out[out_n + pos] = b;
+      out_n += take_total;
+      eq_seen += eq_total;
+    }
+  }
+  // the W most recent blocks follow (they are the highest block ids)
+  const int nrecent = nb - ncand;
+  for (int j = threadIdx.x; j < nrecent; j += kSelThreads) out[kk + j] = ncand + j;
+  if (threadIdx.x == 0) {
+    if (out_n != kk) pi_flag(p.status, PI_DEV_BAD_INDEX);
+    p.nsel[u] = kk + nrecent;
+  }
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------- launchers
+cudaError_t pi_launch_summaries(pi_pool* p, int layer, const uint8_t* src, bool src_is_host, int b0, int b1,
+                                cudaStream_t s, const int* ntok_new) {
+  (void)src_is_host;
+  if (b1 <= b0) return cudaSuccess;
+  dim3 grid(b1 - b0, p->R);
+  int threads = (p->Hkv * p->D) / 8;
+  long long stride = (long long)p->region_bytes;
+  summaries_kernel<<<grid, threads, 0, s>>>(src, stride, ntok_new, p->ntok, p->kmean, p->tail_sum, layer, p->L,
+                                            p->Hkv, p->B, p->D, p->max_blocks, b0);
+  return cudaGetLastError();
+}
+
+cudaError_t pi_launch_append(pi_pool* p, int layer, const void* k_new, const void* v_new, cudaStream_t s) {
+  AppendParams a;
+  a.k_new = (const uint8_t*)k_new;
+  a.v_new = (const uint8_t*)v_new;
+  a.host_dev = p->host_dev;
+  a.pool = p->pool;
+  a.slot_base = p->slot_base;
+  a.P = p->P;
+  a.slot_of = p->slot_of;
+  a.ntok = p->ntok;
+  a.kmean = p->kmean;
+  a.tail_sum = p->tail_sum;
+  a.status = p->dev_status;
+  a.layer = layer;
+  a.L = p->L;
+  a.R = p->R;
+  a.Hkv = p->Hkv;
+  a.B = p->B;
+  a.D = p->D;
+  a.U = p->U;
+  a.max_blocks = p->max_blocks;
+  a.host_layer = layer % p->host_layers;
+  int threads = (p->Hkv * p->D) / 8;
+  append_kernel<<<p->R, threads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t pi_launch_select(pi_pool* p, int layer, const void* q, const int* k_per_req, int* sel, int* nsel,
+                             cudaStream_t s) {
+  SelParams sp;
+  sp.q = (const uint16_t*)q;
+  sp.k_per_req = k_per_req;
+  sp.sel = sel;
+  sp.nsel = nsel;
+  sp.kmean = p->kmean;
+  sp.ntok = p->ntok;
+  const size_t RU = (size_t)p->R * p->U;
+  sp.scores = p->sel_scores + (size_t)layer * RU * p->max_blocks;
+  sp.counter = p->sel_counter + (size_t)layer * RU;
+  sp.status = p->dev_status;
+  sp.layer = layer;
+  sp.L = p->L;
+  sp.Hq = p->Hq;
+  sp.Hkv = p->Hkv;
+  sp.G = p->G;
+  sp.D = p->D;
+  sp.B = p->B;
+  sp.max_blocks = p->max_blocks;
+  sp.W = p->W;
+  sp.k_max = p->k_max;
+  sp.cap = p->cap;
+  sp.U = p->U;
+  // candidates bounded by the largest token count of this layer (host mirror)
+  int nb_max = 0;
+  for (int r = 0; r < p->R; r++) {
+    int nt = p->ntok_h[(size_t)r * p->L + layer];
+    nb_max = max(nb_max, (nt + p->B - 1) / p->B);
+  }
+  const int ncand_max = max(0, nb_max - p->W);
+  // enough CTAs to cover every SM twice, at least 8 blocks (one per warp) each
+  long long target = 2LL * p->num_sms;
+  int chunks = (int)max(1LL, (target + (long long)RU - 1) / (long long)RU);
+  int bpc = (ncand_max + chunks - 1) / chunks;
+  bpc = ((max(bpc, 8) + 7) / 8) * 8;
+  chunks = max(1, (ncand_max + bpc - 1) / bpc);
+  sp.bpc = bpc;
+  dim3 grid(chunks, (unsigned)RU);
+  select_kernel<<<grid, kSelThreads, 0, s>>>(sp);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------- API
+extern "C" pi_status pi_update_summaries(pi_pool* p, int layer, const void* k_dev, int block_begin, int block_end,
+                                         const int* ntok_host, pi_stream s) {
+  if (!p || layer < 0 || layer >= p->L || !ntok_host || block_begin < 0 || block_end < block_begin)
+    return PI_ERR_INVALID;
+  for (int r = 0; r < p->R; r++)
+    if (ntok_host[r] < 0 || (long long)ntok_host[r] > (long long)p->max_blocks * p->B) return PI_ERR_INVALID;
+  if (block_end > p->max_blocks) block_end = p->max_blocks;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(s);
+  int* stage = p->ntok_stage + (size_t)layer * p->R;
+  PI_CUDA_TRY(cudaMemcpyAsync(stage, ntok_host, sizeof(int) * p->R, cudaMemcpyHostToDevice, st));
+  const uint8_t* src = k_dev ? (const uint8_t*)k_dev
+                             : p->host_dev + (size_t)(layer % p->host_layers) * p->R * p->region_bytes;
+  int b1 = block_end;
+  if (b1 <= block_begin) b1 = block_begin + 1;  // still record the counts
+  PI_CUDA_TRY(pi_launch_summaries(p, layer, src, k_dev == nullptr, block_begin, b1, st, stage));
+  for (int r = 0; r < p->R; r++) p->ntok_h[(size_t)r * p->L + layer] = ntok_host[r];
+  return PI_OK;
+}
+
+extern "C" pi_status pi_append_kv(pi_pool* p, int layer, const void* k_new, const void* v_new, pi_stream s) {
+  if (!p || layer < 0 || layer >= p->L || !k_new || !v_new) return PI_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15) return PI_ERR_INVALID;
+  for (int r = 0; r < p->R; r++)
+    if ((long long)p->ntok_h[(size_t)r * p->L + layer] + 1 > (long long)p->max_blocks * p->B) return PI_ERR_INVALID;
+  PI_CUDA_TRY(pi_launch_append(p, layer, k_new, v_new, reinterpret_cast<cudaStream_t>(s)));
+  for (int r = 0; r < p->R; r++) p->ntok_h[(size_t)r * p->L + layer] += 1;
+  return PI_OK;
+}
+
+extern "C" pi_status pi_select_topk(pi_pool* p, int layer, const void* q, const int* k_per_req, int mode, int* sel,
+                                    int* nsel, pi_stream s) {
+  if (!p || layer < 0 || layer >= p->L || !q || !k_per_req || !sel || !nsel) return PI_ERR_INVALID;
+  if (mode != p->mode) return PI_ERR_STATE;
+  if (reinterpret_cast<uintptr_t>(q) & 3) return PI_ERR_INVALID;
+  PI_CUDA_TRY(pi_launch_select(p, layer, q, k_per_req, sel, nsel, reinterpret_cast<cudaStream_t>(s)));
+  return PI_OK;
+}

@@ -1,0 +1,190 @@
+// Layer-wise two-stream decode step.
+//
+// "PulseInfer Guide: I/O-Centric Sparse KV Cache Offloading", section
+// "Interruptible Layer-Wise Scheduling", and the PulseInfer abstract: recall of
+// one layer's blocks runs while the GPU computes another layer, so variable
+// recall latency hides behind compute. Here the compute stream runs append,
+// selection and attention, the copy stream runs the recall (plan + gather), and
+// events order them: recall(l) waits for select(l); attention(l) waits for
+// recall(l). select(l+1) is issued before attention(l), so recall(l+1) overlaps
+// attention(l). With the UVA gather arm no step needs the host.
+#include <cstring>
+#include <vector>
+
+#include "pi_internal.cuh"
+
+pi_status pi_recall_impl(pi_pool* p, int layer, const int* sel, const int* nsel, int method, int* table,
+                         pi_recall_stats* stats, cudaStream_t st);
+
+// event pair of (layer, kind) for the step being recorded, or nullptr
+static cudaEvent_t* tev_of(pi_pool* p, int l, int kind) {
+  if (p->timing_used >= p->timing_steps) return nullptr;
+  return &p->tev[(((size_t)p->timing_used * p->L + l) * PI_K_KINDS + kind) * 2];
+}
+
+#define PI_TIMED(l, kind, stream, launch_expr)                     \
+  do {                                                             \
+    cudaEvent_t* _ev = tev_of(p, (l), (kind));                     \
+    if (_ev) PI_CUDA_TRY(cudaEventRecord(_ev[0], (stream)));       \
+    PI_CUDA_TRY(launch_expr);                                      \
+    if (_ev) PI_CUDA_TRY(cudaEventRecord(_ev[1], (stream)));       \
+  } while (0)
+
+cudaError_t pi_launch_plan(pi_pool* p, int layer, const int* sel, const int* nsel, int* table, cudaStream_t s);
+
+static pi_status step_impl(pi_pool* p, const uint8_t* q_all, const uint8_t* k_new_all, const uint8_t* v_new_all,
+                           const int* k_budget, int method, uint8_t* out_all, float* lse_all, cudaStream_t cs,
+                           cudaStream_t ys, pi_step_stats* stats) {
+  const size_t q_bytes = (size_t)p->R * p->Hq * p->D * 2;
+  const size_t kv_bytes = (size_t)p->R * p->Hkv * p->D * 2;
+  const size_t RU = (size_t)p->R * p->U;
+  const bool append = (k_new_all != nullptr);
+  if (append)
+    for (int l = 0; l < p->L; l++)
+      for (int r = 0; r < p->R; r++)
+        if ((long long)p->ntok_h[(size_t)r * p->L + l] + 1 > (long long)p->max_blocks * p->B) return PI_ERR_INVALID;
+  if (stats) {
+    memset(stats, 0, sizeof(*stats));
+    PI_CUDA_TRY(cudaMemsetAsync(p->recall_counts, 0, sizeof(long long) * 4 * p->L, ys));
+  }
+  // the copy stream must not run ahead of work the caller queued on the compute stream
+  PI_CUDA_TRY(cudaEventRecord(p->ev_start, cs));
+  PI_CUDA_TRY(cudaStreamWaitEvent(ys, p->ev_start, 0));
+
+  auto sel_of = [&](int l) { return p->step_sel + (size_t)l * RU * p->cap; };
+  auto nsel_of = [&](int l) { return p->step_nsel + (size_t)l * RU; };
+  auto tab_of = [&](int l) { return p->step_table + (size_t)l * RU * p->cap; };
+  auto select = [&](int l) -> pi_status {
+    if (append) {
+      PI_TIMED(l, PI_K_APPEND, cs,
+               pi_launch_append(p, l, k_new_all + (size_t)l * kv_bytes, v_new_all + (size_t)l * kv_bytes, cs));
+      for (int r = 0; r < p->R; r++) p->ntok_h[(size_t)r * p->L + l] += 1;
+    }
+    PI_TIMED(l, PI_K_SELECT, cs,
+             pi_launch_select(p, l, q_all + (size_t)l * q_bytes, k_budget + (size_t)l * p->R, sel_of(l), nsel_of(l), cs));
+    PI_CUDA_TRY(cudaEventRecord(p->ev_sel[l], cs));
+    return PI_OK;
+  };
+
+  pi_status st = select(0);
+  if (st != PI_OK) return st;
+  for (int l = 0; l < p->L; l++) {
+    PI_CUDA_TRY(cudaStreamWaitEvent(ys, p->ev_sel[l], 0));
+    if (method == PI_RECALL_UVA) {
+      // the UVA arm inlined so each kernel can be timed on its own
+      p->recall_calls++;
+      if (p->fault_recall_at > 0 && p->recall_calls == p->fault_recall_at) return PI_ERR_FAULT_INJECTED;
+      PI_TIMED(l, PI_K_PLAN, ys, pi_launch_plan(p, l, sel_of(l), nsel_of(l), tab_of(l), ys));
+      PI_TIMED(l, PI_K_GATHER, ys, pi_launch_gather(p, l, nullptr, true, true, ys));
+    } else {
+      st = pi_recall_impl(p, l, sel_of(l), nsel_of(l), method, tab_of(l), nullptr, ys);
+      if (st != PI_OK) return st;
+    }
+    PI_CUDA_TRY(cudaEventRecord(p->ev_rec[l], ys));
+    if (l + 1 < p->L) {
+      st = select(l + 1);
+      if (st != PI_OK) return st;
+    }
+    PI_CUDA_TRY(cudaStreamWaitEvent(cs, p->ev_rec[l], 0));
+    PI_TIMED(l, PI_K_ATTENTION, cs,
+             pi_launch_attention(p, l, q_all + (size_t)l * q_bytes, sel_of(l), tab_of(l), nsel_of(l),
+                                 out_all + (size_t)l * q_bytes, lse_all ? lse_all + (size_t)l * p->R * p->Hq : nullptr,
+                                 nullptr, cs));
+  }
+  if (p->timing_used < p->timing_steps) p->timing_used++;
+  if (stats) {
+    std::vector<long long> c((size_t)4 * p->L);
+    PI_CUDA_TRY(cudaStreamSynchronize(cs));
+    PI_CUDA_TRY(cudaStreamSynchronize(ys));
+    PI_CUDA_TRY(cudaMemcpy(c.data(), p->recall_counts, sizeof(long long) * 4 * p->L, cudaMemcpyDeviceToHost));
+    std::vector<int> ns((size_t)p->L * RU);
+    PI_CUDA_TRY(cudaMemcpy(ns.data(), p->step_nsel, sizeof(int) * ns.size(), cudaMemcpyDeviceToHost));
+    for (int l = 0; l < p->L; l++) {
+      stats->recall.fragments += c[(size_t)l * 4 + 0];
+      stats->recall.hits += c[(size_t)l * 4 + 1];
+    }
+    for (int v : ns) stats->selected += v;
+    stats->recall.bytes = stats->recall.fragments * (long long)p->copy_bytes;
+    stats->recall.runs = stats->recall.fragments;
+  }
+  return PI_OK;
+}
+
+extern "C" pi_status pi_decode_step(pi_pool* p, const void* q_all, const void* k_new_all, const void* v_new_all,
+                                    const int* k_budget, int method, void* out_all, float* lse_all, pi_stream compute,
+                                    pi_stream copy, pi_step_stats* stats) {
+  if (!p || !q_all || !k_budget || !out_all) return PI_ERR_INVALID;
+  if ((k_new_all == nullptr) != (v_new_all == nullptr)) return PI_ERR_INVALID;
+  if (method != PI_RECALL_UVA && method != PI_RECALL_MEMCPY && method != PI_RECALL_STAGED) return PI_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(q_all) & 3) return PI_ERR_INVALID;
+  if (k_new_all && ((reinterpret_cast<uintptr_t>(k_new_all) | reinterpret_cast<uintptr_t>(v_new_all)) & 15))
+    return PI_ERR_INVALID;
+  return step_impl(p, (const uint8_t*)q_all, (const uint8_t*)k_new_all, (const uint8_t*)v_new_all, k_budget, method,
+                   (uint8_t*)out_all, lse_all, reinterpret_cast<cudaStream_t>(compute),
+                   reinterpret_cast<cudaStream_t>(copy), stats);
+}
+
+extern "C" pi_status pi_decode_step_host(pi_pool* p, const void* q_all, const void* k_new_all, const void* v_new_all,
+                                         const int* k_budget, int method, void* out_all, float* lse_all,
+                                         pi_stream compute, pi_stream copy) {
+  if (!p || !q_all || !k_budget || !out_all) return PI_ERR_INVALID;
+  if ((k_new_all == nullptr) != (v_new_all == nullptr)) return PI_ERR_INVALID;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(compute);
+  const size_t q_total = (size_t)p->L * p->R * p->Hq * p->D * 2;
+  const size_t kv_total = (size_t)p->L * p->R * p->Hkv * p->D * 2;
+  const size_t b_total = (size_t)p->L * p->R * sizeof(int);
+  uint8_t* dq = p->step_in;
+  uint8_t* dk = dq + q_total;
+  uint8_t* dv = dk + kv_total;
+  int* db = reinterpret_cast<int*>(dv + kv_total);
+  uint8_t* dout = p->step_out;
+  float* dlse = reinterpret_cast<float*>(dout + q_total);
+  PI_CUDA_TRY(cudaMemcpyAsync(dq, q_all, q_total, cudaMemcpyHostToDevice, cs));
+  if (k_new_all) {
+    PI_CUDA_TRY(cudaMemcpyAsync(dk, k_new_all, kv_total, cudaMemcpyHostToDevice, cs));
+    PI_CUDA_TRY(cudaMemcpyAsync(dv, v_new_all, kv_total, cudaMemcpyHostToDevice, cs));
+  }
+  PI_CUDA_TRY(cudaMemcpyAsync(db, k_budget, b_total, cudaMemcpyHostToDevice, cs));
+  pi_status st = step_impl(p, dq, k_new_all ? dk : nullptr, k_new_all ? dv : nullptr, db, method, dout,
+                           lse_all ? dlse : nullptr, cs, reinterpret_cast<cudaStream_t>(copy), nullptr);
+  if (st != PI_OK) return st;
+  PI_CUDA_TRY(cudaMemcpyAsync(out_all, dout, q_total, cudaMemcpyDeviceToHost, cs));
+  if (lse_all)
+    PI_CUDA_TRY(cudaMemcpyAsync(lse_all, dlse, (size_t)p->L * p->R * p->Hq * sizeof(float), cudaMemcpyDeviceToHost, cs));
+  PI_CUDA_TRY(cudaStreamSynchronize(cs));
+  return PI_OK;
+}
+
+extern "C" pi_status pi_pool_set_timing(pi_pool* p, int max_steps) {
+  if (!p || max_steps < 0) return PI_ERR_INVALID;
+  PI_CUDA_TRY(cudaDeviceSynchronize());
+  for (auto e : p->tev) cudaEventDestroy(e);
+  p->tev.clear();
+  p->timing_steps = 0;
+  p->timing_used = 0;
+  if (max_steps == 0) return PI_OK;
+  const size_t n = (size_t)max_steps * p->L * PI_K_KINDS * 2;
+  p->tev.resize(n, nullptr);
+  for (size_t i = 0; i < n; i++) PI_CUDA_TRY(cudaEventCreate(&p->tev[i]));
+  p->timing_steps = max_steps;
+  return PI_OK;
+}
+
+extern "C" pi_status pi_pool_get_timing(pi_pool* p, pi_kernel_timing* out) {
+  if (!p || !out) return PI_ERR_INVALID;
+  PI_CUDA_TRY(cudaDeviceSynchronize());
+  for (int k = 0; k < PI_K_KINDS; k++) out[k] = pi_kernel_timing{0, 0.0};
+  for (int s = 0; s < p->timing_used; s++)
+    for (int l = 0; l < p->L; l++)
+      for (int k = 0; k < PI_K_KINDS; k++) {
+        cudaEvent_t* ev = &p->tev[(((size_t)s * p->L + l) * PI_K_KINDS + k) * 2];
+        float ms = 0.0f;
+        // a kind that did not run in this step leaves its pair unrecorded
+        if (cudaEventQuery(ev[1]) != cudaSuccess) { cudaGetLastError(); continue; }
+        if (cudaEventElapsedTime(&ms, ev[0], ev[1]) != cudaSuccess) { cudaGetLastError(); continue; }
+        out[k].launches++;
+        out[k].total_ms += ms;
+      }
+  p->timing_used = 0;
+  return PI_OK;
+}
