@@ -45,6 +45,11 @@ CONFIGS = {
                         "top-32 + 2 recent, pool 25% of blocks, AR(1) rho 0.9 queries, 5% heavy-hitter blocks",
                layers=32, batch=8, hq=32, hkv=8, head_dim=128, block_tokens=64, ntok=32768, k=32, window=2,
                pool_slots=128, rho=0.9, heavy=0.05),
+    "c3": dict(workload="variable-recall stress: llama3-8b shape, 32 layers, batch 32, 65536 tokens, blocks of 64, "
+                        "top-k drawn per (layer, step) from 16..128 + 2 recent, per-request resident fraction "
+                        "10..60% (pool = max(fraction x blocks, 130)), AR(1) rho 0.8 queries",
+               layers=32, batch=32, hq=32, hkv=8, head_dim=128, block_tokens=64, ntok=65536, k=128, window=2,
+               pool_slots=0, rho=0.8, heavy=0.05, k_range=(16, 128), frac_range=(0.10, 0.60)),
     "c4": dict(workload="llama3-70b-slice: 8 of 80 layers, batch 16, 64 q / 8 KV heads, d 128, 131072 tokens, "
                         "blocks of 64, top-64 + 4 recent, pool 10% of blocks",
                layers=8, batch=16, hq=64, hkv=8, head_dim=128, block_tokens=64, ntok=131072, k=64, window=4,
@@ -146,6 +151,27 @@ def measure_h2d_peak(torch, dev) -> float:
     return best
 
 
+def reduce_max(value: float, world: int, device=None) -> float:
+    """Max of a per-rank float over all ranks (identity at world 1)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_seed(seed: int, rank: int) -> int:
+    """Each rank serves its own requests (data parallel over requests)."""
+    return seed + 1000 * rank
+
+
+def weak_scaling_tokens_per_s(world: int, batch: int, steps: int, elapsed_max_s: float) -> float:
+    """Whole-job throughput: every rank decodes `batch` tokens per step; time is the slowest rank's."""
+    return world * batch * steps / elapsed_max_s
+
+
 # ------------------------------------------------------------------ CPU oracle leg
 def oracle_unit_step(orc, region, kmean, ntok, q, k, W, sob, bos, pool_copy, k_new, v_new, hkv, B):
     """One (request, layer) of one decode step on the CPU oracle: append, select,
@@ -175,6 +201,7 @@ class OracleSample:
         self.units = units
         self.B, self.hkv = cfg["block_tokens"], cfg["hkv"]
         self.state = {}
+        P_unit = cfg["pool_slots"] or (cfg["k"] + cfg["window"])
         for (r, l) in units:
             if region_source is not None:
                 reg = np.array(region_source(l, r))
@@ -186,8 +213,8 @@ class OracleSample:
             km[:nb0] = orc.region_summaries(reg, cfg["ntok"])
             self.state[(r, l)] = dict(region=reg, kmean=km, ntok=cfg["ntok"],
                                       sob=np.full(max_blocks, -1, dtype=np.int32),
-                                      bos=np.full(cfg["pool_slots"], -1, dtype=np.int32),
-                                      pool=np.zeros((cfg["pool_slots"],) + reg.shape[1:], dtype=np.uint16))
+                                      bos=np.full(P_unit, -1, dtype=np.int32),
+                                      pool=np.zeros((P_unit,) + reg.shape[1:], dtype=np.uint16))
 
     def step(self, qs_step, step_idx, budget_s=None):
         """Run every unit (or until budget_s elapses). Returns (units done, seconds)."""
@@ -237,7 +264,7 @@ def run_ours(args, cfg, rank, world, local_rank):
     total_steps = Wm + 3 * K + 1
     ntok0 = cfg["ntok"]
     max_blocks = -(-(ntok0 + total_steps) // B) + 1
-    seed = args.seed + 1000 * rank
+    seed = rank_seed(args.seed, rank)
     method = {"uva": pi.PI_RECALL_UVA, "memcpy": pi.PI_RECALL_MEMCPY, "staged": pi.PI_RECALL_STAGED}[args.method]
 
     h2d_peak = measure_h2d_peak(torch, dev)
@@ -250,14 +277,27 @@ def run_ours(args, cfg, rank, world, local_rank):
     if full_host > budget:
         host_layers = max(1, int(budget // (region_bytes * R)))
         log(f"rank {rank}: host store for {host_layers} of {L} layers (aliased) to fit host memory")
-    pool = pi.Pool(L, R, Hq, Hkv, D, B, max_blocks, cfg["pool_slots"], cfg["k"], cfg["window"],
-                   host_layers=(host_layers if host_layers < L else 0), gather_ctas=args.gather_ctas)
+    nb0 = -(-ntok0 // B)
+    fracs = None
+    slots_per_req = None
+    if "frac_range" in cfg:
+        lo, hi = cfg["frac_range"]
+        fracs = [synth.uniform_real(seed, synth.KIND_FRAC, r, 0, 0, lo, hi) for r in range(R)]
+        slots_per_req = [max(int(math.ceil(f * nb0)), cfg["k"] + cfg["window"]) for f in fracs]
+    pool = pi.Pool(L, R, Hq, Hkv, D, B, max_blocks, cfg["pool_slots"] or cfg["k"] + cfg["window"], cfg["k"],
+                   cfg["window"], host_layers=(host_layers if host_layers < L else 0), gather_ctas=args.gather_ctas,
+                   pool_slots_per_req=slots_per_req)
     t0 = time.time()
     for hl in range(host_layers):
         for r in range(R):
             synth.fill_kv(pool.host_kv_ptr(hl, r), seed, hl, r, ntok0, max_blocks, Hkv, B, D, cfg["heavy"], 2.0)
     for l in range(L):
         pool.update_summaries(l, [ntok0] * R)
+    if fracs is not None:
+        for l in range(L):
+            for r in range(R):
+                n_res = int(round(fracs[r] * nb0))
+                pool.preload(l, r, synth.sample_sorted(seed, synth.KIND_RESIDENT, l, r, nb0, n_res))
     torch.cuda.synchronize()
     log(f"rank {rank}: host store {host_layers * R * region_bytes / 2**30:.1f} GiB filled + summarised in "
         f"{time.time() - t0:.1f} s")
@@ -269,11 +309,17 @@ def run_ours(args, cfg, rank, world, local_rank):
         for l in range(L):
             for r in range(R):
                 kn[s, l, r], vn[s, l, r] = synth.token_kv(seed, l % host_layers, r, ntok0 + s, Hkv, D)
-    kb = np.full((L, R), cfg["k"], dtype=np.int32)
+    if "k_range" in cfg:
+        lo, hi = cfg["k_range"]
+        kbs = np.array([[[synth.uniform_int(seed, synth.KIND_BUDGET, s_, l, 0, lo, hi)] * R for l in range(L)]
+                        for s_ in range(total_steps)], dtype=np.int32)
+    else:
+        kbs = np.full((total_steps, L, R), cfg["k"], dtype=np.int32)
+    kb = kbs[0]
     q_d = torch.from_numpy(qs.view(np.int16)).to(dev)
     kn_d = torch.from_numpy(kn.view(np.int16)).to(dev)
     vn_d = torch.from_numpy(vn.view(np.int16)).to(dev)
-    kb_d = torch.from_numpy(kb).to(dev)
+    kb_d = torch.from_numpy(kbs).to(dev)
     out = torch.empty((L, R, Hq, D), dtype=torch.int16, device=dev)
     lse = torch.empty((L, R, Hq), dtype=torch.float32, device=dev)
     compute, copy = torch.cuda.Stream(), torch.cuda.Stream()
@@ -281,8 +327,8 @@ def run_ours(args, cfg, rank, world, local_rank):
 
     def run_step(stats=False):
         nonlocal step
-        r_ = pool.decode_step(q_d[step], kn_d[step], vn_d[step], kb_d, out, lse, method=method, compute=compute,
-                              copy=copy, stats=stats)
+        r_ = pool.decode_step(q_d[step], kn_d[step], vn_d[step], kb_d[step], out, lse, method=method,
+                              compute=compute, copy=copy, stats=stats)
         step += 1
         return r_
 
@@ -309,11 +355,8 @@ def run_ours(args, cfg, rank, world, local_rank):
         torch.cuda.synchronize()
     barrier()
     elapsed = e0.elapsed_time(e1) / 1e3
-    t = torch.tensor([elapsed], device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    elapsed_max = float(t.item())
-    tok_s = world * R * K / elapsed_max
+    elapsed_max = reduce_max(elapsed, world, dev)
+    tok_s = weak_scaling_tokens_per_s(world, R, K, elapsed_max)
 
     # ---- pass B: per-kernel CUDA-event durations inside the same pipelined step
     pool.set_timing(K)
@@ -375,23 +418,20 @@ def run_ours(args, cfg, rank, world, local_rank):
         qh = torch.from_numpy(qs.view(np.int16)).pin_memory()
         knh = torch.from_numpy(kn.view(np.int16)).pin_memory()
         vnh = torch.from_numpy(vn.view(np.int16)).pin_memory()
-        kbh = torch.from_numpy(kb).pin_memory()
+        kbh = torch.from_numpy(kbs).pin_memory()
         outh = torch.empty((L, R, Hq, D), dtype=torch.int16).pin_memory()
         lseh = torch.empty((L, R, Hq), dtype=torch.float32).pin_memory()
         barrier()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         for _ in range(K):
-            pool.decode_step_host(qh[step], knh[step], vnh[step], kbh, outh, lseh, method=method, compute=compute,
-                                  copy=copy)
+            pool.decode_step_host(qh[step], knh[step], vnh[step], kbh[step], outh, lseh, method=method,
+                                  compute=compute, copy=copy)
             step += 1
-        t_e2e = time.perf_counter() - t0
-        tt = torch.tensor([t_e2e], device=dev)
-        if world > 1:
-            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        t_e2e = reduce_max(time.perf_counter() - t0, world, dev)
         h2d_b = L * R * Hq * D * 2 + 2 * L * R * Hkv * D * 2 + L * R * 4
         d2h_b = L * R * Hq * D * 2 + L * R * Hq * 4
-        e2e = {"value": world * R * K / float(tt.item()), "unit": "tok/s", "h2d_bytes_per_step": h2d_b,
+        e2e = {"value": weak_scaling_tokens_per_s(world, R, K, t_e2e), "unit": "tok/s", "h2d_bytes_per_step": h2d_b,
                "d2h_bytes_per_step": d2h_b, "api": "pi_decode_step_host (pinned host buffers)"}
     assert pool.device_status() == pi.PI_OK
 
@@ -410,7 +450,9 @@ def run_ours(args, cfg, rank, world, local_rank):
         "dtype": "bf16", "data": "synthetic (seeded; shapes of the pages' Llama-3 long-context workloads)",
         "config": {"workload": cfg["workload"], "layers": L, "batch": R, "hq": Hq, "hkv": Hkv, "head_dim": D,
                    "block_tokens": B, "context": ntok0, "top_k": cfg["k"], "window": cfg["window"],
-                   "pool_slots": cfg["pool_slots"], "recall": args.method, "host_layers": host_layers,
+                   "pool_slots": cfg["pool_slots"] or (f"per request {min(slots_per_req)}..{max(slots_per_req)}"
+                                                       if slots_per_req else None),
+                   "recall": args.method, "host_layers": host_layers,
                    "parallelism": f"replicas{world}" if world > 1 else "single",
                    "l2": "inputs larger than L2 (host store and pool far exceed 129 MB)"},
         "recall": {"gbs": recall_gbs, "h2d_peak_gbs": h2d_peak,
@@ -429,6 +471,97 @@ def run_ours(args, cfg, rank, world, local_rank):
     }
     pool.close()
     return line
+
+
+def run_fragmentation_sweep(args):
+    """Block size 16/32/64/128 at an equal 2048-token budget per (request, layer):
+    shared top-k vs per-KV-head top-k, 0 % resident (pool flushed every step), each
+    recall arm; recall GB/s and transfer counts per step. Emits one JSON line per
+    (block size, selection, arm) and a final summary line."""
+    import torch
+
+    import synth
+    import sparse_kv_cache_block_gb300 as pi
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    pi.build()
+    pi.load()
+    L, R, Hq, Hkv, D, N = 32, 64, 32, 8, 128, 32768
+    if args.layers:
+        L = args.layers
+    if args.batch:
+        R = args.batch
+    budget_tokens = 2048
+    host_layers = max(1, min(L, args.sweep_host_layers))
+    h2d_peak = measure_h2d_peak(torch, dev)
+    methods = {"uva": pi.PI_RECALL_UVA, "memcpy": pi.PI_RECALL_MEMCPY, "staged": pi.PI_RECALL_STAGED}
+    arms = [m for m in args.sweep_methods.split(",") if m]
+    rows = []
+    s_ = torch.cuda.Stream()
+    for B in (int(b) for b in args.sweep_blocks.split(",")):
+        k = budget_tokens // B
+        max_blocks = N // B + 1
+        qs = synth.q_ar1(args.seed, L, R, Hq, D, 2, 0.9)
+        for mode_name, mode in (("shared", pi.PI_SHARED), ("headwise", pi.PI_HEADWISE)):
+            pool = pi.Pool(L, R, Hq, Hkv, D, B, max_blocks, k, k, 0, select_mode=mode,
+                           host_layers=(host_layers if host_layers < L else 0), gather_ctas=args.gather_ctas)
+            t0 = time.time()
+            for hl in range(host_layers):
+                for r in range(R):
+                    synth.fill_kv(pool.host_kv_ptr(hl, r), args.seed, hl, r, N, max_blocks, Hkv, B, D, 0.0, 0.0)
+            for l in range(L):
+                pool.update_summaries(l, [N] * R)
+            torch.cuda.synchronize()
+            log(f"B={B} {mode_name}: host store {host_layers * R * pool.region_bytes / 2**30:.1f} GiB ready in "
+                f"{time.time() - t0:.1f} s")
+            U = Hkv if mode == pi.PI_HEADWISE else 1
+            sel = torch.empty((L, R * U, k), dtype=torch.int32, device=dev)
+            nsel = torch.empty((L, R * U), dtype=torch.int32, device=dev)
+            table = torch.empty_like(sel)
+            kb = torch.full((R,), k, dtype=torch.int32, device=dev)
+            q_d = torch.from_numpy(qs.view(np.int16)).to(dev)
+            with torch.cuda.stream(s_):
+                for l in range(L):
+                    pool.select_topk(l, q_d[0, l], kb, sel[l], nsel[l], stream=s_)
+            torch.cuda.synchronize()
+            for arm in arms:
+                res = None
+                for rep in range(2):  # rep 0 warms up
+                    pool.flush(-1, stream=s_)
+                    torch.cuda.synchronize()
+                    tot = {"bytes": 0, "fragments": 0, "runs": 0, "api_calls": 0, "host_wait_ms": 0.0,
+                           "cpu_gather_ms": 0.0}
+                    ms = 0.0
+                    for l in range(L):
+                        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                        h0 = time.perf_counter()
+                        e0.record(s_)
+                        st = pool.recall(l, sel[l], nsel[l], table[l], method=methods[arm], stats=True, stream=s_)
+                        e1.record(s_)
+                        e1.synchronize()
+                        wall = time.perf_counter() - h0
+                        # the memcpy and staged arms block on the host for part of the call:
+                        # count the whole call (host wall clock) for them, device time for UVA
+                        ms += e0.elapsed_time(e1) if arm == "uva" else 1e3 * wall
+                        for kk in tot:
+                            tot[kk] += st[kk]
+                    res = (ms, tot)
+                ms, tot = res
+                assert pool.device_status() == pi.PI_OK
+                row = {"sweep": "fragmentation", "block_tokens": B, "k": k, "selection": mode_name, "recall": arm,
+                       "layers": L, "batch": R, "bytes_per_step": tot["bytes"], "fragments_per_step": tot["fragments"],
+                       "runs_per_step": tot["runs"], "api_calls_per_step": tot["api_calls"],
+                       "recall_ms_per_step": ms, "recall_gbs": tot["bytes"] / (ms / 1e3) / 1e9,
+                       "h2d_peak_gbs": h2d_peak, "frac_of_h2d_peak": tot["bytes"] / (ms / 1e3) / 1e9 / h2d_peak,
+                       "host_wait_ms": tot["host_wait_ms"], "cpu_gather_ms": tot["cpu_gather_ms"],
+                       "host_layers": host_layers}
+                rows.append(row)
+                print(json.dumps(row), flush=True)
+            pool.close()
+            del sel, nsel, table
+            torch.cuda.empty_cache()
+    return rows
 
 
 def run_reference(args, cfg):
@@ -477,14 +610,31 @@ def main():
     ap.add_argument("--ref-units", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--layers", type=int, default=0, help="override the layer count (small profiling cases)")
+    ap.add_argument("--batch", type=int, default=0, help="override the batch (small profiling cases)")
+    ap.add_argument("--sweep", default="", choices=["", "fragmentation"],
+                    help="fragmentation: block-size sweep of shared vs head-wise recall (not the headline line)")
+    ap.add_argument("--sweep-blocks", default="16,32,64,128")
+    ap.add_argument("--sweep-methods", default="uva,memcpy,staged")
+    ap.add_argument("--sweep-host-layers", type=int, default=2)
     args = ap.parse_args()
     if args.warmup < 3:
         log("warm-up raised to 3 steps (minimum)")
         args.warmup = 3
-    cfg = CONFIGS[args.config]
+    cfg = dict(CONFIGS[args.config])
+    if args.layers:
+        cfg["layers"] = args.layers
+        cfg["workload"] += f" [layers overridden to {args.layers}]"
+    if args.batch:
+        cfg["batch"] = args.batch
+        cfg["workload"] += f" [batch overridden to {args.batch}]"
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.sweep == "fragmentation":
+        rows = run_fragmentation_sweep(args)
+        print(json.dumps({"sweep": "fragmentation", "rows": len(rows)}), flush=True)
+        return
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args, cfg)), flush=True)

@@ -86,7 +86,12 @@ typedef struct pi_config {
                                 tokens for aliased layers). */
   int staging_blocks;        /* staged recall arm: staging capacity in copy units
                                 (0 = as many as fit in 256 MiB) */
-  int gather_ctas;           /* UVA gather kernel grid (0 = 2 per SM) */
+  int gather_ctas;           /* UVA gather kernel grid (0 = one per SM) */
+  int gather_depth;          /* 16-byte loads in flight per gather thread: 2, 4, 8 or 16
+                                (0 = 8) */
+  int host_alloc;            /* host store allocation: 0 = cudaHostAlloc (pinned,
+                                mapped); 1 = anonymous mmap advised for transparent huge
+                                pages, then cudaHostRegister (pinned, mapped) */
   const int* pool_slots_per_req; /* optional host [batch]: per-request P (each
                                 >= k_max + window); NULL = pool_slots for all */
 } pi_config;
@@ -275,6 +280,12 @@ pi_status pi_pool_get_timing(pi_pool* p, pi_kernel_timing* out);
  * (PI_ERR_DEVICE, PI_ERR_TIMEOUT, PI_ERR_POOL_FULL) recorded since the last clear. */
 pi_status pi_get_device_status(pi_pool* p);
 pi_status pi_clear_device_status(pi_pool* p);
+
+/* Self-test of the bounded device wait every kernel uses: one thread waits on an
+ * mbarrier phase that nothing completes, gives up after limit_cycles (clock64;
+ * 1..2e9), records PI_ERR_TIMEOUT in the status word and exits. The context
+ * stays usable. Synchronous; returns the status word's verdict. */
+pi_status pi_selftest_bounded_wait(pi_pool* p, long long limit_cycles);
 
 /* Host-side fault injection for tests: "recall_fail@N" or "" (off). The
  * environment variable PI_FAULT is read once at pool creation. */

@@ -60,10 +60,11 @@ class Pool:
 
     def __init__(self, layers: int, batch: int, hq: int, hkv: int, head_dim: int, block_tokens: int,
                  max_blocks: int, pool_slots: int, k_max: int, window: int, select_mode: int = PI_SHARED,
-                 host_layers: int = 0, staging_blocks: int = 0, gather_ctas: int = 0, pool_slots_per_req=None):
+                 host_layers: int = 0, staging_blocks: int = 0, gather_ctas: int = 0, pool_slots_per_req=None,
+                 gather_depth: int = 0, host_alloc: int = 0):
         self.lib = load()
         cfg = pi_config(layers, batch, hq, hkv, head_dim, block_tokens, max_blocks, pool_slots, k_max, window,
-                        select_mode, host_layers, staging_blocks, gather_ctas, None)
+                        select_mode, host_layers, staging_blocks, gather_ctas, gather_depth, host_alloc, None)
         self._slots_arr = None
         if pool_slots_per_req is not None:
             self._slots_arr = (ctypes.c_int * batch)(*[int(x) for x in pool_slots_per_req])
@@ -212,6 +213,9 @@ class Pool:
 
     def clear_device_status(self):
         check(self.lib.pi_clear_device_status(self.h), "pi_clear_device_status")
+
+    def selftest_bounded_wait(self, limit_cycles: int) -> int:
+        return self.lib.pi_selftest_bounded_wait(self.h, limit_cycles)
 
     def set_fault(self, spec: str):
         check(self.lib.pi_set_fault(self.h, spec.encode()), "pi_set_fault")

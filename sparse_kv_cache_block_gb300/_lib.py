@@ -25,7 +25,8 @@ class pi_config(ctypes.Structure):
     _fields_ = [("layers", c_int), ("batch", c_int), ("hq", c_int), ("hkv", c_int), ("head_dim", c_int),
                 ("block_tokens", c_int), ("max_blocks", c_int), ("pool_slots", c_int), ("k_max", c_int),
                 ("window", c_int), ("select_mode", c_int), ("host_layers", c_int), ("staging_blocks", c_int),
-                ("gather_ctas", c_int), ("pool_slots_per_req", ctypes.POINTER(c_int))]
+                ("gather_ctas", c_int), ("gather_depth", c_int), ("host_alloc", c_int),
+                ("pool_slots_per_req", ctypes.POINTER(c_int))]
 
 
 class pi_recall_stats(ctypes.Structure):
@@ -77,6 +78,7 @@ _SIGS = {
     "pi_get_device_status": (c_int, [_P]),
     "pi_clear_device_status": (c_int, [_P]),
     "pi_set_fault": (c_int, [_P, c_char_p]),
+    "pi_selftest_bounded_wait": (c_int, [_P, c_ll]),
 }
 
 _lib = None

@@ -51,7 +51,8 @@ struct AttnShape {
   static constexpr int kStage = 4 * B * D;  // K + V of one head of one block, bytes
   static constexpr int kNS = (98304 / kStage) < 2 ? 2 : ((98304 / kStage) > 8 ? 8 : (98304 / kStage));
   static constexpr int kSub = B * 128;      // one 64-column swizzled sub-tile
-  static constexpr int kSmem = kNS * kStage + 1024 + 2 * kNS * 8 + 64;
+  static constexpr int kSelCap = 512;        // selected blocks one CTA may take
+  static constexpr int kSmem = kNS * kStage + 1024 + 2 * kNS * 8 + 64 + 2 * kSelCap * 4;
 };
 
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
@@ -68,6 +69,8 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + NS * S::kStage);
   uint64_t* empty = full + NS;
   int* flags = reinterpret_cast<int*>(empty + NS);
+  int* s_blk = flags + 16;            // this CTA's selected block ids
+  int* s_slot = s_blk + S::kSelCap;   // and their pool slots
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int u = blockIdx.y;
@@ -82,7 +85,11 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
   }
   const int split = blockIdx.x;
   const int i0 = split * p.bps;
-  const int nblk = max(0, min(n, i0 + p.bps) - i0);
+  const int nblk = min(S::kSelCap, max(0, min(n, i0 + p.bps) - i0));
+  for (int i = threadIdx.x; i < nblk; i += kThreads) {
+    s_blk[i] = selu[i0 + i];
+    s_slot[i] = tabu[i0 + i];
+  }
   const int nt = p.ntok[(size_t)r * p.L + p.layer];
   const int Pr = p.P[r];
   const long long gbase = p.slot_base[r] + (long long)p.layer * Pr;
@@ -104,7 +111,7 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
       for (int it = 0; it < nblk; it++) {
         const int s = it % NS;
         if (it >= NS && !pi_mbar_wait_bounded(&empty[s], ((it / NS) - 1) & 1, p.status)) break;
-        int slot = tabu[i0 + it];
+        int slot = s_slot[it];
         if (slot < 0 || slot >= Pr) {
           pi_flag(p.status, PI_DEV_BAD_INDEX);
           slot = 0;  // keep the barrier accounting whole; the unit's output is flagged
@@ -145,7 +152,7 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
     for (int it = 0; it < nblk; it++) {
       const int s = it % NS;
       if (!pi_mbar_wait_bounded(&full[s], (it / NS) & 1, p.status)) break;
-      const int b = selu[i0 + it];
+      const int b = s_blk[it];
       int nv = nt - b * B;
       nv = nv > B ? B : nv;
       if (b < 0) nv = 0;
@@ -316,6 +323,25 @@ cudaError_t launch_attn(pi_pool* p, const AttnParams& ap, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+int attn_smem_bytes(int D, int B) {
+  if (D == 128) {
+    switch (B) {
+      case 16: return AttnShape<128, 16>::kSmem;
+      case 32: return AttnShape<128, 32>::kSmem;
+      case 64: return AttnShape<128, 64>::kSmem;
+      case 128: return AttnShape<128, 128>::kSmem;
+    }
+  } else {
+    switch (B) {
+      case 16: return AttnShape<64, 16>::kSmem;
+      case 32: return AttnShape<64, 32>::kSmem;
+      case 64: return AttnShape<64, 64>::kSmem;
+      case 128: return AttnShape<64, 128>::kSmem;
+    }
+  }
+  return 227 * 1024;
+}
+
 }  // namespace
 
 cudaError_t pi_launch_attention(pi_pool* p, int layer, const void* q, const int* sel, const int* table,
@@ -344,8 +370,12 @@ cudaError_t pi_launch_attention(pi_pool* p, int layer, const void* q, const int*
   ap.U = p->U;
   ap.cap = p->cap;
   ap.splits_max = p->attn_max_splits;
-  // split the selection so that about two CTAs per SM have work
-  int splits = (int)((2LL * p->num_sms + (long long)units - 1) / (long long)units);
+  // split the selection so the grid fills the GPU in one wave at the kernel's
+  // occupancy, with at most 512 selected blocks per CTA
+  const int smem = attn_smem_bytes(p->D, p->B);
+  const int per_sm = max(1, (228 * 1024) / (smem + 1024));
+  int splits = (int)(((long long)per_sm * p->num_sms) / (long long)units);
+  splits = max(splits, (p->cap + 511) / 512);
   splits = max(1, min(splits, p->attn_max_splits));
   int bps = (p->cap + splits - 1) / splits;
   splits = (p->cap + bps - 1) / bps;

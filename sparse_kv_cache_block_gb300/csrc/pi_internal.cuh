@@ -46,6 +46,7 @@ struct pi_pool {
   uint8_t* host = nullptr;       // host address
   uint8_t* host_dev = nullptr;   // device address of the same memory
   size_t host_bytes = 0;
+  bool host_mmapped = false;     // mmap + cudaHostRegister instead of cudaHostAlloc
 
   // device state
   uint8_t* pool = nullptr;       // all slots
@@ -112,12 +113,14 @@ static inline long long pi_global_slot(const pi_pool* p, int r, int l, int s) {
 // kernel launchers (return cudaGetLastError of the launch)
 cudaError_t pi_launch_summaries(pi_pool* p, int layer, const uint8_t* src, bool src_is_host, int b0, int b1,
                                 cudaStream_t s, const int* ntok_new);
-cudaError_t pi_launch_append(pi_pool* p, int layer, const void* k_new, const void* v_new, cudaStream_t s);
+cudaError_t pi_launch_append(pi_pool* p, int layer, const void* k_new, const void* v_new, cudaStream_t s,
+                             bool write_host = true);
+// fused_table != nullptr: the last CTA of each unit also writes the recall plan and the table
 cudaError_t pi_launch_select(pi_pool* p, int layer, const void* q, const int* k_per_req, int* sel, int* nsel,
-                             cudaStream_t s);
+                             cudaStream_t s, int* fused_table = nullptr);
 cudaError_t pi_launch_plan(pi_pool* p, int layer, const int* sel, const int* nsel, int* table, cudaStream_t s);
 cudaError_t pi_launch_gather(pi_pool* p, int layer, const uint8_t* stage_src, bool copy, bool commit,
-                             cudaStream_t s);
+                             cudaStream_t s, const void* k_new = nullptr, const void* v_new = nullptr);
 cudaError_t pi_launch_attention(pi_pool* p, int layer, const void* q, const int* sel, const int* table,
                                 const int* nsel, void* out, float* lse, float* logits, cudaStream_t s);
 bool pi_make_tmap(pi_pool* p);

@@ -6,6 +6,7 @@
 // address space so kernels can read it directly), and a paged KV block pool in
 // HBM that recalled blocks are written into.
 #include <cudaTypedefs.h>
+#include <sys/mman.h>
 
 #include <cstdio>
 #include <cstdlib>
@@ -51,7 +52,14 @@ static void pool_free(pi_pool* p) {
                       p->ntok_stage};
   for (void* d : dev_ptrs)
     if (d) cudaFree(d);
-  if (p->host) cudaFreeHost(p->host);
+  if (p->host) {
+    if (p->host_mmapped) {
+      cudaHostUnregister(p->host);
+      munmap(p->host, p->host_bytes);
+    } else {
+      cudaFreeHost(p->host);
+    }
+  }
   if (p->stage_host) cudaFreeHost(p->stage_host);
   delete p;
 }
@@ -80,6 +88,11 @@ static bool valid_config(const pi_config& c) {
   if (c.select_mode != PI_SHARED && c.select_mode != PI_HEADWISE) return false;
   if (c.host_layers < 0 || c.host_layers > c.layers) return false;
   if (c.hkv * c.head_dim > 1024) return false;  // selection keeps one block's summary per warp pass
+  if (c.gather_depth != 0 && c.gather_depth != 2 && c.gather_depth != 4 && c.gather_depth != 8 &&
+      c.gather_depth != 16)
+    return false;
+  if (c.host_alloc != 0 && c.host_alloc != 1) return false;
+  if (c.gather_ctas < 0) return false;
   int cap = c.k_max + c.window;
   if (c.pool_slots_per_req) {
     for (int r = 0; r < c.batch; r++)
@@ -152,14 +165,32 @@ extern "C" pi_status pi_pool_create(const pi_config* cfg, pi_pool** out) {
   // host store: pinned and mapped
   p->host_bytes = p->region_bytes * (size_t)p->host_layers * (size_t)p->R;
   if (fault && strcmp(fault, "pinned_alloc_fail") == 0) { pool_free(p); return PI_ERR_HOST_ALLOC; }
-  if (cudaHostAlloc(reinterpret_cast<void**>(&p->host), p->host_bytes, cudaHostAllocMapped | cudaHostAllocPortable) !=
-      cudaSuccess) {
-    cudaGetLastError();
-    p->host = nullptr;
-    pool_free(p);
-    return PI_ERR_HOST_ALLOC;
+  if (cfg->host_alloc == 1) {
+    void* m = mmap(nullptr, p->host_bytes, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS, -1, 0);
+    if (m == MAP_FAILED) {
+      pool_free(p);
+      return PI_ERR_HOST_ALLOC;
+    }
+    madvise(m, p->host_bytes, MADV_HUGEPAGE);  // advice only: the kernel may decline
+    memset(m, 0, p->host_bytes);               // fault the pages in before pinning
+    if (cudaHostRegister(m, p->host_bytes, cudaHostRegisterMapped | cudaHostRegisterPortable) != cudaSuccess) {
+      cudaGetLastError();
+      munmap(m, p->host_bytes);
+      pool_free(p);
+      return PI_ERR_HOST_ALLOC;
+    }
+    p->host = static_cast<uint8_t*>(m);
+    p->host_mmapped = true;
+  } else {
+    if (cudaHostAlloc(reinterpret_cast<void**>(&p->host), p->host_bytes,
+                      cudaHostAllocMapped | cudaHostAllocPortable) != cudaSuccess) {
+      cudaGetLastError();
+      p->host = nullptr;
+      pool_free(p);
+      return PI_ERR_HOST_ALLOC;
+    }
+    memset(p->host, 0, p->host_bytes);
   }
-  memset(p->host, 0, p->host_bytes);
   if (cudaHostGetDevicePointer(reinterpret_cast<void**>(&p->host_dev), p->host, 0) != cudaSuccess) {
     pool_free(p);
     return PI_ERR_CUDA;
@@ -196,6 +227,7 @@ extern "C" pi_status pi_pool_create(const pi_config* cfg, pi_pool** out) {
     int s = (4 * p->num_sms + units - 1) / units;
     if (s < 1) s = 1;
     if (s > p->cap) s = p->cap;
+    if (s < (p->cap + 511) / 512) s = (p->cap + 511) / 512;
     p->attn_max_splits = s;
   }
   TRY_ALLOC(dalloc(&p->attn_o, (size_t)p->L * p->R * p->Hkv * p->attn_max_splits * p->G * p->D, false));
@@ -371,4 +403,22 @@ bool pi_make_tmap(pi_pool* p) {
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   p->tmap_ok = (r == CUDA_SUCCESS);
   return p->tmap_ok;
+}
+
+// One thread waits on a phase of an mbarrier that never completes (its expected
+// arrival count is 2 and nothing arrives); the bounded wait gives up and flags.
+static __global__ void bounded_wait_selftest_kernel(unsigned* status, long long limit) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    pi_mbar_init(&bar, 2);
+    pi_fence_barrier_init();
+    pi_mbar_wait_bounded(&bar, 0, status, limit);
+  }
+}
+
+extern "C" pi_status pi_selftest_bounded_wait(pi_pool* p, long long limit_cycles) {
+  if (!p || limit_cycles < 1 || limit_cycles > 2000000000LL) return PI_ERR_INVALID;
+  bounded_wait_selftest_kernel<<<1, 32>>>(p->dev_status, limit_cycles);
+  PI_CUDA_TRY(cudaGetLastError());
+  return pi_get_device_status(p);
 }

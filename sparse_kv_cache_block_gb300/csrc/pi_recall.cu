@@ -16,39 +16,13 @@
 #include <cstring>
 
 #include "pi_internal.cuh"
+#include "pi_plan.cuh"
 
 namespace {
 
 constexpr int kPlanThreads = 256;
 constexpr int kGatherThreads = 256;
-constexpr int kChunkBytes = kGatherThreads * 16 * 4;  // 16 KiB per CTA iteration
 
-__device__ __forceinline__ int cta_excl_scan(int v, int* warp_sums, int& total) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  constexpr int NW = kPlanThreads / 32;
-  int x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) warp_sums[w] = x;
-  __syncthreads();
-  if (w == 0) {
-    int s = (lane < NW) ? warp_sums[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      int y = __shfl_up_sync(0xffffffffu, s, o);
-      if (lane >= o) s += y;
-    }
-    if (lane < NW) warp_sums[lane] = s;
-  }
-  __syncthreads();
-  const int before = (w == 0) ? 0 : warp_sums[w - 1];
-  total = warp_sums[NW - 1];
-  __syncthreads();
-  return before + x - v;
-}
 
 struct PlanParams {
   const int* sel;
@@ -68,101 +42,29 @@ struct PlanParams {
 // plan; the maps are committed later by the copy kernel.
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
   extern __shared__ int sm[];
-  const int words = (p.max_blocks + 31) / 32;
-  unsigned* bits = reinterpret_cast<unsigned*>(sm);
-  int* miss_pos = sm + words;
-  int* free_list = miss_pos + p.cap;
   __shared__ int warp_sums[kPlanThreads / 32];
-
+  const int words = (p.max_blocks + 31) / 32;
   const int u = blockIdx.x;
   const int r = u / p.U, gu = u % p.U;
   const size_t rlu = ((size_t)r * p.L + p.layer) * p.U + gu;
-  const int* sob = p.slot_of + rlu * p.max_blocks;
-  const int* bos = p.block_of + rlu * p.p_max;
-  const int Pr = p.P[r];
-  const int* su = p.sel + (size_t)u * p.cap;
-  int* tab = p.table + (size_t)u * p.cap;
   int n = p.nsel[u];
   if (n < 0 || n > p.cap) {
     if (threadIdx.x == 0) pi_flag(p.status, PI_DEV_BAD_INDEX);
     n = 0;
   }
-  for (int w = threadIdx.x; w < words; w += kPlanThreads) bits[w] = 0u;
-  __syncthreads();
-  for (int i = threadIdx.x; i < n; i += kPlanThreads) {
-    const int b = su[i];
-    if (b >= 0 && b < p.max_blocks) atomicOr(&bits[b >> 5], 1u << (b & 31));
-  }
-  __syncthreads();
-
-  // missing = selected without a slot, in selection (ascending) order
-  int nm = 0;
-  for (int base = 0; base < n; base += kPlanThreads) {
-    const int i = base + threadIdx.x;
-    int miss = 0;
-    if (i < n) {
-      const int b = su[i];
-      if (b < 0 || b >= p.max_blocks) {
-        pi_flag(p.status, PI_DEV_BAD_INDEX);
-        tab[i] = -1;
-      } else {
-        const int s = sob[b];
-        if (s < 0) {
-          miss = 1;
-        } else if (s >= Pr) {
-          pi_flag(p.status, PI_DEV_BAD_INDEX);
-          tab[i] = -1;
-        } else {
-          tab[i] = s;
-        }
-      }
-    }
-    int tot;
-    const int pos = cta_excl_scan(miss, warp_sums, tot);
-    if (miss) miss_pos[nm + pos] = i;
-    nm += tot;
-  }
-
-  // free = slots empty or holding an unselected block, ascending; first nm only
-  int nf = 0;
-  for (int base = 0; base < Pr && nf < nm; base += kPlanThreads) {
-    const int s = base + threadIdx.x;
-    int fr = 0;
-    if (s < Pr) {
-      const int bb = bos[s];
-      if (bb < 0) {
-        fr = 1;
-      } else if (bb >= p.max_blocks) {
-        pi_flag(p.status, PI_DEV_BAD_INDEX);
-      } else {
-        fr = ((bits[bb >> 5] >> (bb & 31)) & 1u) ? 0 : 1;
-      }
-    }
-    int tot;
-    const int pos = cta_excl_scan(fr, warp_sums, tot);
-    if (fr && nf + pos < nm) free_list[nf + pos] = s;
-    nf += tot;
-  }
-  if (nf < nm) {
-    if (threadIdx.x == 0) {
-      pi_flag(p.status, PI_DEV_POOL_FULL);
-      p.plan_n[u] = 0;
-    }
-    for (int j = threadIdx.x; j < nm; j += kPlanThreads) tab[miss_pos[j]] = -1;
-    return;
-  }
-  int4* pl = p.plan + (size_t)u * p.cap;
-  for (int j = threadIdx.x; j < nm; j += kPlanThreads) {
-    const int i = miss_pos[j];
-    const int s = free_list[j];
-    pl[j] = make_int4(su[i], s, bos[s], 0);
-    tab[i] = s;
-  }
-  if (threadIdx.x == 0) {
-    p.plan_n[u] = nm;
-    atomicAdd(reinterpret_cast<unsigned long long*>(p.counts + 0), (unsigned long long)nm);
-    atomicAdd(reinterpret_cast<unsigned long long*>(p.counts + 1), (unsigned long long)(n - nm));
-  }
+  pi_plan::UnitArgs a;
+  a.sel = p.sel + (size_t)u * p.cap;
+  a.n = n;
+  a.sob = p.slot_of + rlu * p.max_blocks;
+  a.bos = p.block_of + rlu * p.p_max;
+  a.P = p.P[r];
+  a.max_blocks = p.max_blocks;
+  a.table = p.table + (size_t)u * p.cap;
+  a.plan = p.plan + (size_t)u * p.cap;
+  a.plan_n = p.plan_n + u;
+  a.counts = p.counts;
+  a.status = p.status;
+  pi_plan::plan_unit<kPlanThreads>(a, reinterpret_cast<unsigned*>(sm), sm + words, sm + words + p.cap, warp_sums);
 }
 
 struct GatherParams {
@@ -171,14 +73,18 @@ struct GatherParams {
   int* slot_of;
   int* block_of;
   const uint8_t* host_src;   // device address of this layer's host store (request 0)
+  uint8_t* host_dst;         // same memory, writable (write-through of new tokens)
   const uint8_t* stage_src;  // staged arm: device staging buffer (entries e_begin..)
   uint8_t* pool;
   const long long* slot_base;
   const int* P;
+  const int* ntok;           // [R][L] (after this step's append)
+  const uint8_t* k_new;      // optional [R][Hkv][D]: this step's token of this layer
+  const uint8_t* v_new;
   unsigned* status;
   long long region_bytes;
   long long e_begin, e_end;  // entry range to process (global plan order)
-  int layer, L, U, max_blocks, p_max, cap, units, copy_bytes, block_bytes, do_copy, do_commit;
+  int layer, L, R, U, Hkv, B, D, max_blocks, p_max, cap, units, copy_bytes, block_bytes, do_copy, do_commit;
 };
 
 __device__ __forceinline__ uint4 ld_stream(const uint4* ptr) {
@@ -189,17 +95,39 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* ptr) {
   return v;
 }
 
-// Grid-stride over (plan entry, 16 KiB chunk). Each thread keeps four 16-byte
-// loads in flight, so a CTA has 16 KiB outstanding on the host link.
+// Grid-stride over (plan entry, chunk of 256 x 16 x DEPTH bytes). Each thread
+// keeps DEPTH 16-byte loads in flight (DEPTH = 8: 32 KiB outstanding per CTA).
+// With k_new set (decode-step pipeline), CTA 0 also writes this step's token of
+// every request through to the host store, and a CTA that copies a chunk of the
+// block holding that token overwrites the token's rows from k_new/v_new, so the
+// pool never depends on when the host write lands.
+template <int kGatherDepth>
 __global__ void __launch_bounds__(kGatherThreads) gather_kernel(GatherParams g) {
+  constexpr int kChunkBytes = kGatherThreads * 16 * kGatherDepth;
   extern __shared__ long long prefix[];  // [units + 1]
   __shared__ int warp_sums[kGatherThreads / 32];
+  const int row_bytes = g.D * 2;
+  const int row_words = row_bytes / 16;
+  // write-through of the new tokens (host store), one request per pass
+  if (g.k_new && blockIdx.x == 0) {
+    const int per_req = g.Hkv * 2 * row_words;  // 16-byte words of K and V rows
+    for (int w = threadIdx.x; w < g.R * per_req; w += kGatherThreads) {
+      const int r = w / per_req, rem = w % per_req;
+      const int g_ = rem / (2 * row_words), kv = (rem / row_words) & 1, x = rem % row_words;
+      const int t = g.ntok[(size_t)r * g.L + g.layer] - 1;
+      if (t < 0 || t / g.B >= g.max_blocks) continue;
+      const int b = t / g.B, tp = t % g.B;
+      const uint8_t* src = (kv ? g.v_new : g.k_new) + (((size_t)r * g.Hkv + g_) * g.D) * 2 + (size_t)x * 16;
+      uint8_t* dst = g.host_dst + (size_t)r * g.region_bytes + (size_t)b * g.block_bytes +
+                     (((size_t)g_ * 2 + kv) * g.B + tp) * row_bytes + (size_t)x * 16;
+      *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+    }
+  }
   // prefix sums of the per-unit plan counts (every CTA computes its own copy)
   long long run = 0;
   for (int base = 0; base < g.units; base += kGatherThreads) {
     const int u = base + threadIdx.x;
     const int v = (u < g.units) ? g.plan_n[u] : 0;
-    // reuse the plan kernel's scan shape
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     int x = v;
 #pragma unroll
@@ -229,7 +157,6 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(GatherParams g) 
   for (long long it = blockIdx.x; it < items; it += gridDim.x) {
     const long long e = e0 + it / cpe;
     const int c = (int)(it % cpe);
-    // unit owning entry e: last u with prefix[u] <= e
     int lo = 0, hi = g.units - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -252,18 +179,38 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(GatherParams g) 
       const uint8_t* src = g.stage_src ? g.stage_src + (size_t)(e - e0) * g.copy_bytes + off
                                        : g.host_src + (size_t)r * g.region_bytes +
                                              (size_t)pe.x * g.block_bytes + head_off + off;
-      uint8_t* dst = g.pool + (size_t)(g.slot_base[r] + (long long)g.layer * Pr + pe.y) * g.block_bytes + head_off + off;
+      uint8_t* blk = g.pool + (size_t)(g.slot_base[r] + (long long)g.layer * Pr + pe.y) * g.block_bytes;
+      uint8_t* dst = blk + head_off + off;
       const uint4* s4 = reinterpret_cast<const uint4*>(src);
       uint4* d4 = reinterpret_cast<uint4*>(dst);
       const int words = len >> 4;
-      for (int w = threadIdx.x; w < words; w += kGatherThreads * 4) {
-        uint4 v[4];
+      for (int w = threadIdx.x; w < words; w += kGatherThreads * kGatherDepth) {
+        uint4 v[kGatherDepth];
 #pragma unroll
-        for (int k = 0; k < 4; k++)
+        for (int k = 0; k < kGatherDepth; k++)
           if (w + k * kGatherThreads < words) v[k] = ld_stream(s4 + w + k * kGatherThreads);
 #pragma unroll
-        for (int k = 0; k < 4; k++)
+        for (int k = 0; k < kGatherDepth; k++)
           if (w + k * kGatherThreads < words) d4[w + k * kGatherThreads] = v[k];
+      }
+      if (g.k_new) {
+        const int t = g.ntok[(size_t)r * g.L + g.layer] - 1;
+        if (t >= 0 && t / g.B == pe.x) {
+          // this block holds the new token: rewrite its rows that fall in this chunk
+          __syncthreads();
+          const int tp = t % g.B;
+          const int heads = (g.U > 1) ? 1 : g.Hkv;
+          for (int w = threadIdx.x; w < heads * 2 * row_words; w += kGatherThreads) {
+            const int hh = w / (2 * row_words), kv = (w / row_words) & 1, x = w % row_words;
+            const int g_ = (g.U > 1) ? gu : hh;
+            const size_t rel = (((size_t)g_ * 2 + kv) * g.B + tp) * row_bytes + (size_t)x * 16;  // in the block
+            const size_t lo_b = head_off + off, hi_b = head_off + off + len;
+            if (rel >= lo_b && rel < hi_b) {
+              const uint8_t* tsrc = (kv ? g.v_new : g.k_new) + (((size_t)r * g.Hkv + g_) * g.D) * 2 + (size_t)x * 16;
+              *reinterpret_cast<uint4*>(blk + rel) = *reinterpret_cast<const uint4*>(tsrc);
+            }
+          }
+        }
       }
     }
     if (g.do_commit && c == 0 && threadIdx.x == 0) {
@@ -298,7 +245,7 @@ cudaError_t pi_launch_plan(pi_pool* p, int layer, const int* sel, const int* nse
   pp.max_blocks = p->max_blocks;
   pp.p_max = p->p_max;
   pp.cap = p->cap;
-  const size_t smem = sizeof(int) * ((p->max_blocks + 31) / 32 + 2 * (size_t)p->cap);
+  const size_t smem = pi_plan::plan_smem_bytes(p->max_blocks, p->cap);
   if (smem > 48 * 1024) cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   plan_kernel<<<(unsigned)RU, kPlanThreads, smem, s>>>(pp);
   return cudaGetLastError();
@@ -312,7 +259,11 @@ static GatherParams gather_params(pi_pool* p, int layer) {
   g.slot_of = p->slot_of;
   g.block_of = p->block_of;
   g.host_src = p->host_dev + (size_t)(layer % p->host_layers) * p->R * p->region_bytes;
+  g.host_dst = p->host_dev + (size_t)(layer % p->host_layers) * p->R * p->region_bytes;
   g.stage_src = nullptr;
+  g.ntok = p->ntok;
+  g.k_new = nullptr;
+  g.v_new = nullptr;
   g.pool = p->pool;
   g.slot_base = p->slot_base;
   g.P = p->P;
@@ -322,7 +273,11 @@ static GatherParams gather_params(pi_pool* p, int layer) {
   g.e_end = 1LL << 62;
   g.layer = layer;
   g.L = p->L;
+  g.R = p->R;
   g.U = p->U;
+  g.Hkv = p->Hkv;
+  g.B = p->B;
+  g.D = p->D;
   g.max_blocks = p->max_blocks;
   g.p_max = p->p_max;
   g.cap = p->cap;
@@ -334,18 +289,33 @@ static GatherParams gather_params(pi_pool* p, int layer) {
   return g;
 }
 
-static cudaError_t launch_gather(pi_pool* p, const GatherParams& g, cudaStream_t s) {
-  const size_t smem = sizeof(long long) * ((size_t)g.units + 1);
-  if (smem > 48 * 1024) cudaFuncSetAttribute(gather_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  int ctas = p->cfg.gather_ctas > 0 ? p->cfg.gather_ctas : 2 * p->num_sms;
-  gather_kernel<<<ctas, kGatherThreads, smem, s>>>(g);
+template <int DEPTH>
+static cudaError_t launch_gather_t(int ctas, size_t smem, const GatherParams& g, cudaStream_t s) {
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(gather_kernel<DEPTH>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  gather_kernel<DEPTH><<<ctas, kGatherThreads, smem, s>>>(g);
   return cudaGetLastError();
 }
 
+static cudaError_t launch_gather(pi_pool* p, const GatherParams& g, cudaStream_t s) {
+  const size_t smem = sizeof(long long) * ((size_t)g.units + 1);
+  const int ctas = p->cfg.gather_ctas > 0 ? p->cfg.gather_ctas : p->num_sms;
+  switch (p->cfg.gather_depth) {
+    case 2: return launch_gather_t<2>(ctas, smem, g, s);
+    case 4: return launch_gather_t<4>(ctas, smem, g, s);
+    case 16: return launch_gather_t<16>(ctas, smem, g, s);
+    default: return launch_gather_t<8>(ctas, smem, g, s);
+  }
+}
+
 cudaError_t pi_launch_gather(pi_pool* p, int layer, const uint8_t* stage_src, bool copy, bool commit,
-                             cudaStream_t s) {
+                             cudaStream_t s, const void* k_new, const void* v_new) {
   GatherParams g = gather_params(p, layer);
   g.stage_src = stage_src;
+  g.k_new = (const uint8_t*)k_new;
+  g.v_new = (const uint8_t*)v_new;
   g.do_copy = copy ? 1 : 0;
   g.do_commit = commit ? 1 : 0;
   return launch_gather(p, g, s);

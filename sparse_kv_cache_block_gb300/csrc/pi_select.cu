@@ -13,6 +13,7 @@
 // fixed fp32 order (per-lane fused multiply-add over elements 128c+4*lane+j,
 // then a xor butterfly); ties go to the lower block index.
 #include "pi_internal.cuh"
+#include "pi_plan.cuh"
 
 namespace {
 
@@ -76,6 +77,7 @@ struct AppendParams {
   float* tail_sum;
   unsigned* status;
   int layer, L, R, Hkv, B, D, U, max_blocks, host_layer;
+  int write_host;         // 0: the decode-step gather writes the host copy instead
 };
 
 // grid R; one thread per 8 consecutive elements of one head
@@ -99,8 +101,10 @@ __global__ void append_kernel(AppendParams a) {
     const size_t in_block_v = (((size_t)g * 2 + 1) * a.B + tp) * a.D * 2 + (size_t)d * 2;
     uint8_t* host_blk =
         a.host_dev + (((size_t)a.host_layer * a.R + r) * a.max_blocks + b) * block_bytes;
-    *reinterpret_cast<uint4*>(host_blk + in_block_k) = kv;
-    *reinterpret_cast<uint4*>(host_blk + in_block_v) = vv;
+    if (a.write_host) {
+      *reinterpret_cast<uint4*>(host_blk + in_block_k) = kv;
+      *reinterpret_cast<uint4*>(host_blk + in_block_v) = vv;
+    }
     const int u = (a.U == 1) ? 0 : g;
     const int slot = a.slot_of[(rl * a.U + u) * a.max_blocks + b];
     if (slot >= 0) {
@@ -146,6 +150,16 @@ struct SelParams {
   unsigned* counter;   // [R*U] for this layer
   unsigned* status;
   int layer, L, Hq, Hkv, G, D, B, max_blocks, W, k_max, cap, U, bpc;
+  int keys_smem;       // candidate keys cached in shared memory (0: read from global)
+  // fused recall plan (decode-step pipeline); table == nullptr disables it
+  int* table;
+  const int* slot_of;
+  const int* block_of;
+  const int* P;
+  int* plan_n;
+  int4* plan;
+  long long* counts;
+  int p_max;
 };
 
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -154,38 +168,12 @@ __device__ __forceinline__ uint32_t order_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// exclusive scan over the CTA (kSelThreads threads); returns the prefix, sets total
-__device__ __forceinline__ int cta_excl_scan(int v, int* warp_sums, int& total) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  int x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) warp_sums[w] = x;
-  __syncthreads();
-  if (w == 0) {
-    int s = (lane < kSelThreads / 32) ? warp_sums[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      int y = __shfl_up_sync(0xffffffffu, s, o);
-      if (lane >= o) s += y;
-    }
-    if (lane < kSelThreads / 32) warp_sums[lane] = s;  // inclusive warp prefix
-  }
-  __syncthreads();
-  const int before = (w == 0) ? 0 : warp_sums[w - 1];
-  total = warp_sums[kSelThreads / 32 - 1];
-  __syncthreads();
-  return before + x - v;
-}
-
 __global__ void __launch_bounds__(kSelThreads) select_kernel(SelParams p) {
   __shared__ __align__(16) float qs[1024];
   __shared__ int hist[256];
   __shared__ int warp_sums[kSelThreads / 32];
   __shared__ int bcast[4];
+  extern __shared__ __align__(16) uint32_t dyn[];  // [keys_smem] + plan scratch
   const int u = blockIdx.y;
   const int r = u / p.U;
   const int g = (p.U == 1) ? 0 : u % p.U;
@@ -208,20 +196,28 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelParams p) {
   }
   __syncthreads();
 
-  // scores of this CTA's candidates: one warp per block, canonical lane order
+  // scores of this CTA's candidates: one warp per block, canonical lane order,
+  // two blocks per pass so sixteen 16-byte loads per lane are in flight
   const int b_begin = blockIdx.x * p.bpc;
   const int b_end = min(ncand, b_begin + p.bpc);
   float* sc = p.scores + (size_t)u * p.max_blocks;
   const int chunks = (E + 127) / 128;
-  for (int b = b_begin + warp; b < b_end; b += kSelThreads / 32) {
+  constexpr int NW = kSelThreads / 32;
+  for (int b = b_begin + warp; b < b_end; b += 2 * NW) {
+    const int b2 = b + NW;
+    const bool two = b2 < b_end;
     const float* km = p.kmean + ((rl * p.max_blocks + b) * p.Hkv) * p.D + goff;
-    float4 kv[8];
+    const float* km2 = p.kmean + ((rl * p.max_blocks + (two ? b2 : b)) * p.Hkv) * p.D + goff;
+    float4 kv[8], kv2[8];
 #pragma unroll
     for (int c = 0; c < 8; c++) {
       const int e = 128 * c + 4 * lane;
-      if (c < chunks && e < E) kv[c] = __ldg(reinterpret_cast<const float4*>(km + e));
+      if (c < chunks && e < E) {
+        kv[c] = __ldg(reinterpret_cast<const float4*>(km + e));
+        if (two) kv2[c] = __ldg(reinterpret_cast<const float4*>(km2 + e));
+      }
     }
-    float acc = 0.0f;
+    float acc = 0.0f, acc2 = 0.0f;
 #pragma unroll
     for (int c = 0; c < 8; c++) {
       const int e = 128 * c + 4 * lane;
@@ -231,11 +227,23 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelParams p) {
         acc = __fmaf_rn(qv.y, kv[c].y, acc);
         acc = __fmaf_rn(qv.z, kv[c].z, acc);
         acc = __fmaf_rn(qv.w, kv[c].w, acc);
+        if (two) {
+          acc2 = __fmaf_rn(qv.x, kv2[c].x, acc2);
+          acc2 = __fmaf_rn(qv.y, kv2[c].y, acc2);
+          acc2 = __fmaf_rn(qv.z, kv2[c].z, acc2);
+          acc2 = __fmaf_rn(qv.w, kv2[c].w, acc2);
+        }
       }
     }
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, off));
-    if (lane == 0) sc[b] = acc;
+    for (int off = 16; off >= 1; off >>= 1) {
+      acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, off));
+      acc2 = __fadd_rn(acc2, __shfl_xor_sync(0xffffffffu, acc2, off));
+    }
+    if (lane == 0) {
+      sc[b] = acc;
+      if (two) sc[b2] = acc2;
+    }
   }
 
   // the last CTA of this unit to finish runs the top-k
@@ -254,6 +262,12 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelParams p) {
   kreq = max(0, min(kreq, p.k_max));
   const int kk = min(kreq, ncand);
   int* out = p.sel + (size_t)u * p.cap;
+  uint32_t* keys = dyn;
+  const bool cached = ncand <= p.keys_smem;
+  if (cached)
+    for (int b = threadIdx.x; b < ncand; b += kSelThreads) keys[b] = order_key(__ldcg(sc + b));
+  __syncthreads();
+  auto key_at = [&](int b) -> uint32_t { return cached ? keys[b] : order_key(__ldcg(sc + b)); };
 
   uint32_t T = 0;      // key of the kk-th largest candidate
   int need_eq = 0;     // how many candidates equal to T to take (lowest indices)
@@ -265,7 +279,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelParams p) {
       hist[threadIdx.x] = 0;  // kSelThreads == 256 bins
       __syncthreads();
       for (int b = threadIdx.x; b < ncand; b += kSelThreads) {
-        const uint32_t key = order_key(__ldcg(sc + b));
+        const uint32_t key = key_at(b);
         if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255], 1);
       }
       __syncthreads();
@@ -320,16 +334,16 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelParams p) {
         if (take_all) {
           gt = 1;
         } else {
-          const uint32_t key = order_key(__ldcg(sc + b));
+          const uint32_t key = key_at(b);
           gt = key > T;
           eq = key == T;
         }
       }
       int eq_total;
-      const int eq_before = cta_excl_scan(eq, warp_sums, eq_total);
+      const int eq_before = pi_plan::cta_excl_scan<kSelThreads>(eq, warp_sums, eq_total);
       const int take = gt || (eq && (eq_seen + eq_before) < need_eq);
       int take_total;
-      const int pos = cta_excl_scan(take, warp_sums, take_total);
+      const int pos = pi_plan::cta_excl_scan<kSelThreads>(take, warp_sums, take_total);
       if (take && out_n + pos < kk) out[out_n + pos] = b;
       out_n += take_total;
       eq_seen += eq_total;
@@ -342,6 +356,28 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelParams p) {
     if (out_n != kk) pi_flag(p.status, PI_DEV_BAD_INDEX);
     p.nsel[u] = kk + nrecent;
   }
+  if (p.table == nullptr) return;
+
+  // fused recall plan of this unit (the selection is in global memory, written
+  // by this CTA; the barrier makes it visible to every thread of the CTA)
+  __syncthreads();
+  const int words = (p.max_blocks + 31) / 32;
+  uint32_t* pl = dyn + (p.keys_smem > 0 ? ((p.keys_smem + 3) & ~3) : 0);
+  pi_plan::UnitArgs a;
+  a.sel = out;
+  a.n = kk + nrecent;
+  const size_t rlu = rl * p.U + g;
+  a.sob = p.slot_of + rlu * p.max_blocks;
+  a.bos = p.block_of + rlu * p.p_max;
+  a.P = p.P[r];
+  a.max_blocks = p.max_blocks;
+  a.table = p.table + (size_t)u * p.cap;
+  a.plan = p.plan + (size_t)u * p.cap;
+  a.plan_n = p.plan_n + u;
+  a.counts = p.counts;
+  a.status = p.status;
+  pi_plan::plan_unit<kSelThreads>(a, pl, reinterpret_cast<int*>(pl) + words, reinterpret_cast<int*>(pl) + words + p.cap,
+                                  warp_sums);
 }
 
 }  // namespace
@@ -359,8 +395,10 @@ cudaError_t pi_launch_summaries(pi_pool* p, int layer, const uint8_t* src, bool 
   return cudaGetLastError();
 }
 
-cudaError_t pi_launch_append(pi_pool* p, int layer, const void* k_new, const void* v_new, cudaStream_t s) {
+cudaError_t pi_launch_append(pi_pool* p, int layer, const void* k_new, const void* v_new, cudaStream_t s,
+                             bool write_host) {
   AppendParams a;
+  a.write_host = write_host ? 1 : 0;
   a.k_new = (const uint8_t*)k_new;
   a.v_new = (const uint8_t*)v_new;
   a.host_dev = p->host_dev;
@@ -387,7 +425,7 @@ cudaError_t pi_launch_append(pi_pool* p, int layer, const void* k_new, const voi
 }
 
 cudaError_t pi_launch_select(pi_pool* p, int layer, const void* q, const int* k_per_req, int* sel, int* nsel,
-                             cudaStream_t s) {
+                             cudaStream_t s, int* fused_table) {
   SelParams sp;
   sp.q = (const uint16_t*)q;
   sp.k_per_req = k_per_req;
@@ -425,8 +463,23 @@ cudaError_t pi_launch_select(pi_pool* p, int layer, const void* q, const int* k_
   bpc = ((max(bpc, 8) + 7) / 8) * 8;
   chunks = max(1, (ncand_max + bpc - 1) / bpc);
   sp.bpc = bpc;
+  sp.keys_smem = (ncand_max <= 4096) ? ncand_max : 0;
+  sp.table = fused_table;
+  sp.slot_of = p->slot_of;
+  sp.block_of = p->block_of;
+  sp.P = p->P;
+  sp.plan_n = p->plan_n + (size_t)layer * RU;
+  sp.plan = p->plan + (size_t)layer * RU * p->cap;
+  sp.counts = p->recall_counts + (size_t)layer * 4;
+  sp.p_max = p->p_max;
+  size_t smem = sizeof(uint32_t) * (size_t)((sp.keys_smem + 3) & ~3);
+  if (fused_table) smem += pi_plan::plan_smem_bytes(p->max_blocks, p->cap);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
   dim3 grid(chunks, (unsigned)RU);
-  select_kernel<<<grid, kSelThreads, 0, s>>>(sp);
+  select_kernel<<<grid, kSelThreads, smem, s>>>(sp);
   return cudaGetLastError();
 }
 
@@ -465,6 +518,6 @@ extern "C" pi_status pi_select_topk(pi_pool* p, int layer, const void* q, const 
   if (!p || layer < 0 || layer >= p->L || !q || !k_per_req || !sel || !nsel) return PI_ERR_INVALID;
   if (mode != p->mode) return PI_ERR_STATE;
   if (reinterpret_cast<uintptr_t>(q) & 3) return PI_ERR_INVALID;
-  PI_CUDA_TRY(pi_launch_select(p, layer, q, k_per_req, sel, nsel, reinterpret_cast<cudaStream_t>(s)));
+  PI_CUDA_TRY(pi_launch_select(p, layer, q, k_per_req, sel, nsel, reinterpret_cast<cudaStream_t>(s), nullptr));
   return PI_OK;
 }

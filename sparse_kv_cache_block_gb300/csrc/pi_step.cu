@@ -54,14 +54,19 @@ static pi_status step_impl(pi_pool* p, const uint8_t* q_all, const uint8_t* k_ne
   auto sel_of = [&](int l) { return p->step_sel + (size_t)l * RU * p->cap; };
   auto nsel_of = [&](int l) { return p->step_nsel + (size_t)l * RU; };
   auto tab_of = [&](int l) { return p->step_table + (size_t)l * RU * p->cap; };
+  // UVA arm: the plan runs in the selection kernel's last CTA and the gather
+  // writes the new tokens through to the host store, so the copy stream carries
+  // only the gather and the compute stream never waits on host-memory writes.
+  const bool uva = (method == PI_RECALL_UVA);
   auto select = [&](int l) -> pi_status {
     if (append) {
       PI_TIMED(l, PI_K_APPEND, cs,
-               pi_launch_append(p, l, k_new_all + (size_t)l * kv_bytes, v_new_all + (size_t)l * kv_bytes, cs));
+               pi_launch_append(p, l, k_new_all + (size_t)l * kv_bytes, v_new_all + (size_t)l * kv_bytes, cs, !uva));
       for (int r = 0; r < p->R; r++) p->ntok_h[(size_t)r * p->L + l] += 1;
     }
     PI_TIMED(l, PI_K_SELECT, cs,
-             pi_launch_select(p, l, q_all + (size_t)l * q_bytes, k_budget + (size_t)l * p->R, sel_of(l), nsel_of(l), cs));
+             pi_launch_select(p, l, q_all + (size_t)l * q_bytes, k_budget + (size_t)l * p->R, sel_of(l), nsel_of(l), cs,
+                              uva ? tab_of(l) : nullptr));
     PI_CUDA_TRY(cudaEventRecord(p->ev_sel[l], cs));
     return PI_OK;
   };
@@ -70,12 +75,12 @@ static pi_status step_impl(pi_pool* p, const uint8_t* q_all, const uint8_t* k_ne
   if (st != PI_OK) return st;
   for (int l = 0; l < p->L; l++) {
     PI_CUDA_TRY(cudaStreamWaitEvent(ys, p->ev_sel[l], 0));
-    if (method == PI_RECALL_UVA) {
-      // the UVA arm inlined so each kernel can be timed on its own
+    if (uva) {
       p->recall_calls++;
       if (p->fault_recall_at > 0 && p->recall_calls == p->fault_recall_at) return PI_ERR_FAULT_INJECTED;
-      PI_TIMED(l, PI_K_PLAN, ys, pi_launch_plan(p, l, sel_of(l), nsel_of(l), tab_of(l), ys));
-      PI_TIMED(l, PI_K_GATHER, ys, pi_launch_gather(p, l, nullptr, true, true, ys));
+      PI_TIMED(l, PI_K_GATHER, ys,
+               pi_launch_gather(p, l, nullptr, true, true, ys, append ? k_new_all + (size_t)l * kv_bytes : nullptr,
+                                append ? v_new_all + (size_t)l * kv_bytes : nullptr));
     } else {
       st = pi_recall_impl(p, l, sel_of(l), nsel_of(l), method, tab_of(l), nullptr, ys);
       if (st != PI_OK) return st;

@@ -375,3 +375,15 @@ def test_invalid_arguments_return_status():
                              torch.zeros(1, dtype=torch.int32, device="cuda"), torch.zeros(1, 36, dtype=torch.int32,
                                                                                            device="cuda"),
                              torch.zeros(1, dtype=torch.int32, device="cuda"), mode=pi.PI_HEADWISE)
+
+
+def test_bounded_wait_times_out_into_status_word():
+    """A wait on a barrier phase that nothing completes gives up after its limit,
+    records PI_ERR_TIMEOUT, and leaves the context usable (a normal call follows)."""
+    w = C1
+    with make_pool(w) as pool:
+        assert pool.selftest_bounded_wait(20_000_000) == pi.PI_ERR_TIMEOUT
+        pool.clear_device_status()
+        prefill(pool, w)
+        om = OracleModel(w)
+        run_layer(pool, om, w, 0, queries(w)[0][0], [w.k], pi.PI_RECALL_UVA)
