@@ -286,7 +286,7 @@ def run_ours(args, cfg, rank, world, local_rank):
         slots_per_req = [max(int(math.ceil(f * nb0)), cfg["k"] + cfg["window"]) for f in fracs]
     pool = pi.Pool(L, R, Hq, Hkv, D, B, max_blocks, cfg["pool_slots"] or cfg["k"] + cfg["window"], cfg["k"],
                    cfg["window"], host_layers=(host_layers if host_layers < L else 0), gather_ctas=args.gather_ctas,
-                   pool_slots_per_req=slots_per_req)
+                   pool_slots_per_req=slots_per_req, gather_depth=args.gather_depth, host_alloc=args.host_alloc)
     t0 = time.time()
     for hl in range(host_layers):
         for r in range(R):
@@ -452,7 +452,8 @@ def run_ours(args, cfg, rank, world, local_rank):
                    "block_tokens": B, "context": ntok0, "top_k": cfg["k"], "window": cfg["window"],
                    "pool_slots": cfg["pool_slots"] or (f"per request {min(slots_per_req)}..{max(slots_per_req)}"
                                                        if slots_per_req else None),
-                   "recall": args.method, "host_layers": host_layers,
+                   "recall": args.method, "host_layers": host_layers, "gather_ctas": args.gather_ctas or "one per SM",
+                   "gather_depth": args.gather_depth or 8, "host_alloc": ["cudaHostAlloc", "mmap+THP+register"][args.host_alloc],
                    "parallelism": f"replicas{world}" if world > 1 else "single",
                    "l2": "inputs larger than L2 (host store and pool far exceed 129 MB)"},
         "recall": {"gbs": recall_gbs, "h2d_peak_gbs": h2d_peak,
@@ -606,6 +607,9 @@ def main():
     ap.add_argument("--method", default="uva", choices=["uva", "memcpy", "staged"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--gather-ctas", type=int, default=0)
+    ap.add_argument("--gather-depth", type=int, default=0)
+    ap.add_argument("--host-alloc", type=int, default=0, choices=[0, 1],
+                    help="0 cudaHostAlloc, 1 mmap + transparent huge pages + cudaHostRegister")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ref-units", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")

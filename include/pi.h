@@ -220,6 +220,10 @@ pi_status pi_recall(pi_pool* p, int layer, const int* sel, const int* nsel, int 
  * Errors: PI_ERR_INVALID (n > P_r, unsorted, out of range, head-wise pool). */
 pi_status pi_pool_preload(pi_pool* p, int layer, int req, const int* blocks, int n, pi_stream s);
 
+/* Retune the UVA gather: grid size (CTAs, > 0) and 16-byte loads in flight per
+ * thread (2, 4, 8 or 16). Applies to calls issued afterwards. */
+pi_status pi_pool_set_gather(pi_pool* p, int ctas, int depth);
+
 /* Forget residency of `layer` (-1 = all layers): every slot empty. Bytes stay. */
 pi_status pi_pool_flush(pi_pool* p, int layer, pi_stream s);
 

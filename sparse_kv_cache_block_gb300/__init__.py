@@ -173,6 +173,9 @@ class Pool:
         check(self.lib.pi_pool_preload(self.h, layer, req, arr.ctypes.data if arr.size else None, int(arr.size),
                                        _stream(stream)), "pi_pool_preload")
 
+    def set_gather(self, ctas: int, depth: int):
+        check(self.lib.pi_pool_set_gather(self.h, ctas, depth), "pi_pool_set_gather")
+
     def flush(self, layer: int = -1, stream=None):
         check(self.lib.pi_pool_flush(self.h, layer, _stream(stream)), "pi_pool_flush")
 

@@ -70,6 +70,7 @@ _SIGS = {
     "pi_recall": (c_int, [_P, c_int, _P, _P, c_int, _P, ctypes.POINTER(pi_recall_stats), _P]),
     "pi_pool_preload": (c_int, [_P, c_int, c_int, _P, c_int, _P]),
     "pi_pool_flush": (c_int, [_P, c_int, _P]),
+    "pi_pool_set_gather": (c_int, [_P, c_int, c_int]),
     "pi_sparse_decode": (c_int, [_P, c_int, _P, _P, _P, _P, _P, _P, _P, _P]),
     "pi_decode_step": (c_int, [_P, _P, _P, _P, _P, c_int, _P, _P, _P, _P, ctypes.POINTER(pi_step_stats)]),
     "pi_decode_step_host": (c_int, [_P, _P, _P, _P, _P, c_int, _P, _P, _P, _P]),

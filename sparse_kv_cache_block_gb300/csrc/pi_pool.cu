@@ -422,3 +422,10 @@ extern "C" pi_status pi_selftest_bounded_wait(pi_pool* p, long long limit_cycles
   PI_CUDA_TRY(cudaGetLastError());
   return pi_get_device_status(p);
 }
+
+extern "C" pi_status pi_pool_set_gather(pi_pool* p, int ctas, int depth) {
+  if (!p || ctas <= 0 || (depth != 2 && depth != 4 && depth != 8 && depth != 16)) return PI_ERR_INVALID;
+  p->cfg.gather_ctas = ctas;
+  p->cfg.gather_depth = depth;
+  return PI_OK;
+}
