@@ -242,6 +242,31 @@ pi_status pi_pool_flush(pi_pool* p, int layer, pi_stream s);
 pi_status pi_sparse_decode(pi_pool* p, int layer, const void* q, const int* sel, const int* table,
                            const int* nsel, void* out, float* lse, float* logits, pi_stream s);
 
+/* Sparse decode attention that allocates nothing. The pages have no counterpart:
+ * this entry point exists for callers that cannot call cudaMalloc, such as
+ * serving engines that reserve all device memory in their own arena up front
+ * and forbid later allocations. It computes what pi_sparse_decode computes
+ * (shared selection only) over a caller-owned paged KV buffer, without a pool:
+ *   kv_slots   device, n_slots slots of [hkv][2 (K,V)][block_tokens][head_dim]
+ *              bf16 (16-byte aligned); slot_table [batch][cap] gives, for each
+ *              selected block, its slot index in kv_slots;
+ *   q [batch][hq][head_dim] bf16, sel [batch][cap] ascending block ids, nsel
+ *   [batch], ntok [batch] tokens held per request (all device);
+ *   out [batch][hq][head_dim] bf16, lse [batch][hq] fp32 (optional).
+ * Its scratch (split-K partials, merge counters, per-request slot bases; about
+ * 8.3 MiB) is one fixed array in device memory that every GPU loading the
+ * library holds until the process exits. Limits: batch*hkv <= 1024,
+ * cap <= 512, (hq/hkv)*head_dim <= 1024, hq/hkv <= 8; larger sizes return
+ * PI_ERR_INVALID. The first call on a device resolves the array's address on
+ * that device (make it before any stream capture). Every call shares the array:
+ * each call clears what must start at zero, and calls that overlap on the GPU
+ * (other streams, other threads) race. A table entry outside [0, n_slots) is
+ * read as slot 0 and not reported. */
+pi_status pi_sparse_decode_noalloc(const void* kv_slots, long long n_slots, int batch, int hq, int hkv,
+                                   int head_dim, int block_tokens, int cap, const void* q, const int* sel,
+                                   const int* slot_table, const int* nsel, const int* ntok, void* out, float* lse,
+                                   pi_stream s);
+
 /* ------------------------------------------------------------------ a-6 pipeline */
 /* One decode step over all layers with the recall of layer l+1 overlapped with
  * attention of layer l: compute stream runs append, select and attention; the

@@ -55,6 +55,16 @@ def device_view(ptr: int, shape, dtype: str):
     return torch.as_tensor(_DevView(ptr, shape, typestr), device="cuda")
 
 
+def sparse_decode_noalloc(kv_slots, n_slots: int, batch: int, hq: int, hkv: int, head_dim: int,
+                          block_tokens: int, cap: int, q, sel, slot_table, nsel, ntok, out, lse=None, stream=None):
+    """pi_sparse_decode_noalloc: attention over a caller-owned paged KV buffer
+    that allocates nothing (its scratch is a fixed array inside the library).
+    Returns the pi_status code (0 = ok) without raising."""
+    return load().pi_sparse_decode_noalloc(_ptr(kv_slots), int(n_slots), batch, hq, hkv, head_dim, block_tokens, cap,
+                                           _ptr(q), _ptr(sel), _ptr(slot_table), _ptr(nsel), _ptr(ntok), _ptr(out),
+                                           _ptr(lse), _stream(stream))
+
+
 class Pool:
     """One pi_pool: pinned host KV store + device block pool + summaries + maps."""
 

@@ -72,6 +72,8 @@ _SIGS = {
     "pi_pool_flush": (c_int, [_P, c_int, _P]),
     "pi_pool_set_gather": (c_int, [_P, c_int, c_int]),
     "pi_sparse_decode": (c_int, [_P, c_int, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "pi_sparse_decode_noalloc": (c_int, [_P, c_ll, c_int, c_int, c_int, c_int, c_int, c_int, _P, _P, _P, _P, _P,
+                                         _P, _P, _P]),
     "pi_decode_step": (c_int, [_P, _P, _P, _P, _P, c_int, _P, _P, _P, _P, ctypes.POINTER(pi_step_stats)]),
     "pi_decode_step_host": (c_int, [_P, _P, _P, _P, _P, c_int, _P, _P, _P, _P]),
     "pi_pool_set_timing": (c_int, [_P, c_int]),

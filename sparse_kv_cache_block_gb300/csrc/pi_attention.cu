@@ -18,7 +18,10 @@
 // accumulator fragment, so P never touches shared memory. Online softmax in the
 // log2 domain, fp32. Warps merge in shared memory; splits merge through a small
 // global partial buffer, finalised by the last CTA of the unit.
+#include <cudaTypedefs.h>
+
 #include <cstdio>
+#include <mutex>
 
 #include "pi_internal.cuh"
 
@@ -407,5 +410,187 @@ extern "C" pi_status pi_sparse_decode(pi_pool* p, int layer, const void* q, cons
   if (reinterpret_cast<uintptr_t>(q) & 3) return PI_ERR_INVALID;
   if (!p->tmap_ok) return PI_ERR_STATE;
   PI_CUDA_TRY(pi_launch_attention(p, layer, q, sel, table, nsel, out, lse, logits, reinterpret_cast<cudaStream_t>(s)));
+  return PI_OK;
+}
+
+// ----------------------------------------------------------------------------
+// Attention with no allocation (no pool, no cudaMalloc).
+//
+// For callers that cannot allocate device memory: engines that reserve all HBM
+// up front in their own arena and forbid further cudaMalloc calls, or code that
+// runs where a runtime allocation would stall or fail. They own the paged KV
+// buffer, tables and outputs; the split-K partials, merge counters and per-request
+// slot bases this kernel needs live in the fixed array below, which every GPU that
+// loads the library holds until the process exits.
+namespace {
+
+constexpr int kNoAllocMaxUnits = 1024;   // batch * KV heads
+constexpr int kNoAllocMaxParts = 2048;   // units * splits
+constexpr int kNoAllocMaxCap = 512;      // selected blocks per request
+constexpr int kNoAllocMaxGD = 8 * 128;   // query heads per group * head_dim
+
+struct NoAllocLayout {
+  static constexpr size_t o_bytes = (size_t)kNoAllocMaxParts * kNoAllocMaxGD * sizeof(float);
+  static constexpr size_t ml_bytes = (size_t)kNoAllocMaxParts * 8 * sizeof(float2);
+  static constexpr size_t ctr_bytes = (size_t)kNoAllocMaxUnits * sizeof(unsigned);
+  static constexpr size_t base_bytes = (size_t)kNoAllocMaxUnits * sizeof(long long);
+  static constexpr size_t p_bytes = (size_t)kNoAllocMaxUnits * sizeof(int);
+  static constexpr size_t o_off = 0;
+  static constexpr size_t ml_off = o_off + o_bytes;
+  static constexpr size_t ctr_off = ml_off + ml_bytes;
+  static constexpr size_t base_off = ctr_off + ctr_bytes;
+  static constexpr size_t p_off = base_off + base_bytes;
+  static constexpr size_t status_off = p_off + p_bytes;
+  static constexpr size_t total = status_off + 256;
+};
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[NoAllocLayout::total];
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+unsigned char* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+// Counters and the status word start at zero; every request's slots start at
+// global slot 0 of the caller's buffer and are bounded by its slot count.
+__global__ void noalloc_prepare_kernel(unsigned char* scratch, int batch, int units, int n_slots) {
+  unsigned* ctr = reinterpret_cast<unsigned*>(scratch + NoAllocLayout::ctr_off);
+  long long* base = reinterpret_cast<long long*>(scratch + NoAllocLayout::base_off);
+  int* P = reinterpret_cast<int*>(scratch + NoAllocLayout::p_off);
+  for (int i = threadIdx.x; i < units; i += blockDim.x) ctr[i] = 0u;
+  for (int r = threadIdx.x; r < batch; r += blockDim.x) {
+    base[r] = 0;
+    P[r] = n_slots;
+  }
+  if (threadIdx.x == 0) *reinterpret_cast<unsigned*>(scratch + NoAllocLayout::status_off) = 0u;
+}
+
+template <int D, int B>
+cudaError_t launch_attn_noalloc(const CUtensorMap& tmap, const AttnParams& ap, int units, cudaStream_t s) {
+  using S = AttnShape<D, B>;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(attn_kernel<D, B>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  dim3 grid(ap.splits, units);
+  attn_kernel<D, B><<<grid, kThreads, S::kSmem, s>>>(tmap, ap);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+extern "C" pi_status pi_sparse_decode_noalloc(const void* kv_slots, long long n_slots, int batch, int hq, int hkv,
+                                              int head_dim, int block_tokens, int cap, const void* q, const int* sel,
+                                              const int* slot_table, const int* nsel, const int* ntok, void* out,
+                                              float* lse, pi_stream stream) {
+  if (!kv_slots || !q || !sel || !slot_table || !nsel || !ntok || !out) return PI_ERR_INVALID;
+  if (batch <= 0 || hq <= 0 || hkv <= 0 || hq % hkv != 0 || hq / hkv > 8 || n_slots <= 0 || cap <= 0)
+    return PI_ERR_INVALID;
+  if (head_dim != 64 && head_dim != 128) return PI_ERR_INVALID;
+  if (block_tokens != 16 && block_tokens != 32 && block_tokens != 64 && block_tokens != 128) return PI_ERR_INVALID;
+  // the fixed scratch bounds every size this entry point accepts
+  const long long units = (long long)batch * hkv;
+  if (units > kNoAllocMaxUnits || cap > kNoAllocMaxCap) return PI_ERR_INVALID;
+  if ((long long)(hq / hkv) * head_dim > kNoAllocMaxGD) return PI_ERR_INVALID;
+  const unsigned long long rows = (unsigned long long)n_slots * hkv * 2 * block_tokens;
+  if (rows >= (1ULL << 31)) return PI_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(kv_slots) & 15) || (reinterpret_cast<uintptr_t>(q) & 3)) return PI_ERR_INVALID;
+
+  int dev = 0;
+  PI_CUDA_TRY(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return PI_ERR_INVALID;
+  unsigned char* scratch = nullptr;
+  {
+    // first call on this device: resolve the array's device address (this device is current)
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+      void* ptr = nullptr;
+      cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+      if (e != cudaSuccess || !ptr) {
+        pi_note_cuda_error(e, "cudaGetSymbolAddress(g_noalloc_scratch)", __FILE__, __LINE__);
+        return PI_ERR_CUDA;
+      }
+      g_noalloc_ptr[dev] = static_cast<unsigned char*>(ptr);
+    }
+    scratch = g_noalloc_ptr[dev];
+  }
+
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult qres;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &qres) != cudaSuccess ||
+      qres != cudaDriverEntryPointSuccess || !fn) {
+    cudaGetLastError();
+    return PI_ERR_CUDA;
+  }
+  CUtensorMap tmap;
+  cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)head_dim * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)block_tokens};
+  cuuint32_t estr[2] = {1, 1};
+  if (reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn)(
+          &tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(kv_slots), dims, strides, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return PI_ERR_INVALID;
+
+  int num_sms = 0;
+  PI_CUDA_TRY(cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev));
+  const int G = hq / hkv;
+  const int smem = attn_smem_bytes(head_dim, block_tokens);
+  const int per_sm = max(1, (228 * 1024) / (smem + 1024));
+  int splits = (int)(((long long)per_sm * max(num_sms, 1)) / units);
+  splits = max(1, min(splits, min(cap, (int)(kNoAllocMaxParts / units))));
+  int bps = (cap + splits - 1) / splits;
+  splits = (cap + bps - 1) / bps;
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  noalloc_prepare_kernel<<<1, 256, 0, s>>>(scratch, batch, (int)units, (int)min(n_slots, (long long)INT_MAX));
+  PI_CUDA_TRY(cudaGetLastError());
+
+  AttnParams ap;
+  ap.q = (const uint16_t*)q;
+  ap.sel = sel;
+  ap.table = slot_table;
+  ap.nsel = nsel;
+  ap.ntok = ntok;
+  ap.slot_base = reinterpret_cast<const long long*>(scratch + NoAllocLayout::base_off);
+  ap.P = reinterpret_cast<const int*>(scratch + NoAllocLayout::p_off);
+  ap.part_o = reinterpret_cast<float*>(scratch + NoAllocLayout::o_off);
+  ap.part_ml = reinterpret_cast<float2*>(scratch + NoAllocLayout::ml_off);
+  ap.counter = reinterpret_cast<unsigned*>(scratch + NoAllocLayout::ctr_off);
+  ap.out = (uint16_t*)out;
+  ap.lse = lse;
+  ap.logits = nullptr;
+  ap.status = reinterpret_cast<unsigned*>(scratch + NoAllocLayout::status_off);
+  ap.layer = 0;
+  ap.L = 1;
+  ap.Hq = hq;
+  ap.Hkv = hkv;
+  ap.G = G;
+  ap.U = 1;
+  ap.cap = cap;
+  ap.splits = splits;
+  ap.splits_max = splits;
+  ap.bps = bps;
+  ap.scale = 1.0f / sqrtf((float)head_dim);
+  ap.scale_log2 = ap.scale * 1.4426950408889634f;
+  cudaError_t e = cudaErrorInvalidValue;
+  if (head_dim == 128) {
+    switch (block_tokens) {
+      case 16: e = launch_attn_noalloc<128, 16>(tmap, ap, (int)units, s); break;
+      case 32: e = launch_attn_noalloc<128, 32>(tmap, ap, (int)units, s); break;
+      case 64: e = launch_attn_noalloc<128, 64>(tmap, ap, (int)units, s); break;
+      case 128: e = launch_attn_noalloc<128, 128>(tmap, ap, (int)units, s); break;
+    }
+  } else {
+    switch (block_tokens) {
+      case 16: e = launch_attn_noalloc<64, 16>(tmap, ap, (int)units, s); break;
+      case 32: e = launch_attn_noalloc<64, 32>(tmap, ap, (int)units, s); break;
+      case 64: e = launch_attn_noalloc<64, 64>(tmap, ap, (int)units, s); break;
+      case 128: e = launch_attn_noalloc<64, 128>(tmap, ap, (int)units, s); break;
+    }
+  }
+  PI_CUDA_TRY(e);
   return PI_OK;
 }
