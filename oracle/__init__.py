@@ -76,6 +76,8 @@ def lib():
         L.or_select_headwise.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp]
         L.or_recall_plan.restype = i32
         L.or_recall_plan.argtypes = [vp, i32, vp, vp, i32, vp, vp, vp, vp]
+        L.or_recall_plan_lru.restype = i32
+        L.or_recall_plan_lru.argtypes = [vp, i32, vp, vp, vp, i32, i32, vp, vp, vp, vp]
         L.or_attention.restype = None
         L.or_attention.argtypes = [vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, vp, vp, vp, i32]
         _lib = L
@@ -188,6 +190,27 @@ def recall_plan(sel: np.ndarray, slot_of_block: np.ndarray, block_of_slot: np.nd
     ms = np.empty(max(n, 1), dtype=np.int32)
     ev = np.empty(max(n, 1), dtype=np.int32)
     nm = lib().or_recall_plan(_p(sel), n, _p(slot_of_block), _p(block_of_slot), P, _p(table), _p(mb), _p(ms), _p(ev))
+    if nm < 0:
+        return None
+    return table[:n].copy(), mb[:nm].copy(), ms[:nm].copy(), ev[:nm].copy()
+
+
+def recall_plan_lru(sel: np.ndarray, slot_of_block: np.ndarray, block_of_slot: np.ndarray, stamp: np.ndarray,
+                    epoch: int):
+    """Least-recently-selected variant: free slots taken by (stamp, slot)
+    ascending; selected slots stamped with `epoch`. Updates maps and stamps in
+    place; returns (table, miss_blocks, miss_slots, evicted) or None."""
+    sel = _c(sel, np.int32)
+    for a in (slot_of_block, block_of_slot, stamp):
+        assert a.dtype == np.int32 and a.flags["C_CONTIGUOUS"]
+    n = sel.size
+    P = block_of_slot.size
+    table = np.empty(max(n, 1), dtype=np.int32)
+    mb = np.empty(max(n, 1), dtype=np.int32)
+    ms = np.empty(max(n, 1), dtype=np.int32)
+    ev = np.empty(max(n, 1), dtype=np.int32)
+    nm = lib().or_recall_plan_lru(_p(sel), n, _p(slot_of_block), _p(block_of_slot), _p(stamp), P, int(epoch),
+                                  _p(table), _p(mb), _p(ms), _p(ev))
     if nm < 0:
         return None
     return table[:n].copy(), mb[:nm].copy(), ms[:nm].copy(), ev[:nm].copy()

@@ -228,6 +228,62 @@ int or_recall_plan(const int* sel, int nsel, int* slot_of_block, int* block_of_s
   return nmiss;
 }
 
+/* Least-recently-selected variant of the plan (a pool policy option; the pages
+ * leave eviction open). stamp[s] is the epoch at which slot s's block was last
+ * selected (-1: never, or the slot is empty). This call is epoch `epoch`: the
+ * free slots (empty or holding an unselected block) are taken in order of
+ * (stamp ascending, slot ascending), so empty slots go first and among occupied
+ * ones the block selected longest ago is evicted first. Every selected block's
+ * slot is stamped with `epoch` afterwards. Otherwise as or_recall_plan. */
+typedef struct { int stamp, slot; } or_free_cand;
+
+static int or_free_cmp(const void* pa, const void* pb) {
+  const or_free_cand* a = (const or_free_cand*)pa;
+  const or_free_cand* b = (const or_free_cand*)pb;
+  if (a->stamp != b->stamp) return (a->stamp < b->stamp) ? -1 : 1;
+  return (a->slot > b->slot) - (a->slot < b->slot);
+}
+
+int or_recall_plan_lru(const int* sel, int nsel, int* slot_of_block, int* block_of_slot, int* stamp, int P,
+                       int epoch, int* table, int* miss_block, int* miss_slot, int* evicted) {
+  int nmiss = 0, nfree = 0;
+  int* missing = (int*)malloc(sizeof(int) * (size_t)(nsel > 0 ? nsel : 1));
+  or_free_cand* freel = (or_free_cand*)malloc(sizeof(or_free_cand) * (size_t)(P > 0 ? P : 1));
+  for (int i = 0; i < nsel; i++)
+    if (slot_of_block[sel[i]] < 0) missing[nmiss++] = sel[i];
+  for (int s = 0; s < P; s++) {
+    int b = block_of_slot[s];
+    int keep = 0;
+    if (b >= 0)
+      for (int i = 0; i < nsel; i++)
+        if (sel[i] == b) { keep = 1; break; }
+    if (!keep) {
+      freel[nfree].stamp = (b >= 0) ? stamp[s] : -1;
+      freel[nfree].slot = s;
+      nfree++;
+    }
+  }
+  if (nmiss > nfree) { free(missing); free(freel); return -1; }
+  qsort(freel, (size_t)nfree, sizeof(or_free_cand), or_free_cmp);
+  for (int i = 0; i < nmiss; i++) {
+    int s = freel[i].slot;
+    int old = block_of_slot[s];
+    if (old >= 0) slot_of_block[old] = -1;
+    slot_of_block[missing[i]] = s;
+    block_of_slot[s] = missing[i];
+    if (miss_block) miss_block[i] = missing[i];
+    if (miss_slot) miss_slot[i] = s;
+    if (evicted) evicted[i] = old;
+  }
+  for (int i = 0; i < nsel; i++) {
+    table[i] = slot_of_block[sel[i]];
+    stamp[table[i]] = epoch;
+  }
+  free(missing);
+  free(freel);
+  return nmiss;
+}
+
 /* ------------------------------------------------------------------ a-5 attention */
 /* Sparse GQA decode attention of one (request, layer) in fp64. For query head h
  * (KV head g = h / G) the tokens are those of the selected blocks, ascending block

@@ -308,6 +308,48 @@ def test_plan_invariants_random_sequence():
         assert (sob >= 0).sum() == (bos >= 0).sum()
 
 
+def test_plan_lru_hand_worked_example():
+    # 4 slots hold 5 (last selected at epoch 3), 7 (epoch 1), 9 (epoch 2); slot 3 empty.
+    sob = np.full(16, -1, dtype=np.int32)
+    bos = np.array([5, 7, 9, -1], dtype=np.int32)
+    stamp = np.array([3, 1, 2, -1], dtype=np.int32)
+    for s, b in enumerate(bos):
+        if b >= 0:
+            sob[b] = s
+    # epoch 4 selects [1, 8, 9]: 9 hits; 1 and 8 miss. Free: slot 3 (empty, first),
+    # then slot 1 (block 7, epoch 1) before slot 0 (block 5, epoch 3).
+    table, mb, ms, ev = oracle.recall_plan_lru(np.array([1, 8, 9]), sob, bos, stamp, 4)
+    assert list(mb) == [1, 8] and list(ms) == [3, 1] and list(ev) == [-1, 7]
+    assert list(table) == [3, 1, 2]
+    assert list(bos) == [5, 8, 9, 1] and list(stamp) == [3, 4, 4, 4]
+
+
+def test_plan_lru_evicts_least_recently_selected_invariant():
+    r = np.random.default_rng(11)
+    nb, P = 120, 24
+    sob = np.full(nb, -1, dtype=np.int32)
+    bos = np.full(P, -1, dtype=np.int32)
+    stamp = np.full(P, -1, dtype=np.int32)
+    for epoch in range(1, 80):
+        sel = np.sort(r.choice(nb, size=int(r.integers(1, P + 1)), replace=False)).astype(np.int32)
+        before_bos, before_stamp = bos.copy(), stamp.copy()
+        out = oracle.recall_plan_lru(sel, sob, bos, stamp, epoch)
+        assert out is not None
+        table, mb, ms, ev = out
+        S = set(sel.tolist())
+        # every evicted slot is no more recent than any unselected resident that was kept
+        kept_unsel = [before_stamp[s] for s in range(P) if before_bos[s] >= 0 and before_bos[s] not in S
+                      and s not in set(ms.tolist())]
+        for s in ms:
+            if before_bos[s] >= 0:
+                assert not any(k < before_stamp[s] for k in kept_unsel)
+        assert all(stamp[t] == epoch for t in table)
+        assert list(table) == [sob[b] for b in sel]
+        for s in range(P):
+            if bos[s] >= 0:
+                assert sob[bos[s]] == s
+
+
 # ------------------------------------------------------------------ a-5 attention
 def _dense_inputs(reg, ntok, hkv, sel):
     B = reg.shape[3]
