@@ -261,7 +261,7 @@ def run_ours(args, cfg, rank, world, local_rank):
     pi.load()
     L, R, Hq, Hkv, D, B = (cfg[k] for k in ("layers", "batch", "hq", "hkv", "head_dim", "block_tokens"))
     K, Wm = args.steps, args.warmup
-    total_steps = Wm + 3 * K + 1
+    total_steps = 2 * Wm + 4 * K + 4
     ntok0 = cfg["ntok"]
     max_blocks = -(-(ntok0 + total_steps) // B) + 1
     seed = rank_seed(args.seed, rank)
@@ -286,7 +286,10 @@ def run_ours(args, cfg, rank, world, local_rank):
         slots_per_req = [max(int(math.ceil(f * nb0)), cfg["k"] + cfg["window"]) for f in fracs]
     pool = pi.Pool(L, R, Hq, Hkv, D, B, max_blocks, cfg["pool_slots"] or cfg["k"] + cfg["window"], cfg["k"],
                    cfg["window"], host_layers=(host_layers if host_layers < L else 0), gather_ctas=args.gather_ctas,
-                   pool_slots_per_req=slots_per_req, gather_depth=args.gather_depth, host_alloc=args.host_alloc)
+                   pool_slots_per_req=slots_per_req, gather_depth=args.gather_depth, host_alloc=args.host_alloc,
+                   evict_policy=(pi.PI_EVICT_LRU if args.evict == "lru" else pi.PI_EVICT_ASCENDING))
+    if args.select_ahead >= 0:
+        pool.set_pipeline(args.select_ahead)
     t0 = time.time()
     for hl in range(host_layers):
         for r in range(R):
@@ -435,6 +438,31 @@ def run_ours(args, cfg, rank, world, local_rank):
                "d2h_bytes_per_step": d2h_b, "api": "pi_decode_step_host (pinned host buffers)"}
     assert pool.device_status() == pi.PI_OK
 
+    # ---- the other eviction policy on the same pool: flush, warm up, time K steps
+    variant = None
+    if not args.no_variant and fracs is None:
+        other = "lru" if args.evict == "ascending" else "ascending"
+        pool.flush()
+        pool.set_evict(pi.PI_EVICT_LRU if other == "lru" else pi.PI_EVICT_ASCENDING)
+        for _ in range(Wm):
+            run_step()
+        vstats = []
+        torch.cuda.synchronize()
+        e4, e5 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e4.record(compute)
+        for _ in range(K):
+            run_step()
+        e5.record(compute)
+        torch.cuda.synchronize()
+        v_s = reduce_max(e4.elapsed_time(e5) / 1e3, world, dev)
+        for _ in range(2):
+            vstats.append(run_step(stats=True))
+        assert pool.device_status() == pi.PI_OK
+        variant = {"evict": other, "value": weak_scaling_tokens_per_s(world, R, K, v_s), "unit": "tok/s",
+                   "ms_per_step": 1e3 * v_s / K,
+                   "recall_blocks_per_step": sum(v["fragments"] for v in vstats) / len(vstats),
+                   "note": "same pool and inputs after a flush and warm-up; not the headline"}
+
     # ---- CPU oracle baseline on a bounded sample (rank 0, N = 1)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -452,7 +480,9 @@ def run_ours(args, cfg, rank, world, local_rank):
                    "block_tokens": B, "context": ntok0, "top_k": cfg["k"], "window": cfg["window"],
                    "pool_slots": cfg["pool_slots"] or (f"per request {min(slots_per_req)}..{max(slots_per_req)}"
                                                        if slots_per_req else None),
-                   "recall": args.method, "host_layers": host_layers, "gather_ctas": args.gather_ctas or "one per SM",
+                   "recall": args.method, "evict": args.evict, "host_layers": host_layers,
+                   "select_ahead": ("library default" if args.select_ahead < 0 else (args.select_ahead or "all")),
+                   "gather_ctas": args.gather_ctas or "one per SM",
                    "gather_depth": args.gather_depth or 8, "host_alloc": ["cudaHostAlloc", "mmap+THP+register"][args.host_alloc],
                    "parallelism": f"replicas{world}" if world > 1 else "single",
                    "l2": "inputs larger than L2 (host store and pool far exceed 129 MB)"},
@@ -462,6 +492,7 @@ def run_ours(args, cfg, rank, world, local_rank):
                    "selected_per_step": selected / K,
                    "pipelined_link_gbs": recalled * BB / pass_b_s / 1e9},
         "roofline": roofline,
+        "evict_variant": variant,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": K * L * 5,
@@ -608,6 +639,11 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--gather-ctas", type=int, default=0)
     ap.add_argument("--gather-depth", type=int, default=0)
+    ap.add_argument("--evict", default="ascending", choices=["ascending", "lru"],
+                    help="pool eviction policy of the headline passes")
+    ap.add_argument("--no-variant", action="store_true", help="skip the extra pass under the other eviction policy")
+    ap.add_argument("--select-ahead", type=int, default=-1,
+                    help="layers selected ahead of attention in the step (0 = all; -1 = library default)")
     ap.add_argument("--host-alloc", type=int, default=0, choices=[0, 1],
                     help="0 cudaHostAlloc, 1 mmap + transparent huge pages + cudaHostRegister")
     ap.add_argument("--cpu-budget", type=float, default=15.0)

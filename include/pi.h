@@ -71,6 +71,7 @@ typedef enum {
 
 enum { PI_SHARED = 0, PI_HEADWISE = 1 };
 enum { PI_RECALL_UVA = 0, PI_RECALL_MEMCPY = 1, PI_RECALL_STAGED = 2 };
+enum { PI_EVICT_ASCENDING = 0, PI_EVICT_LRU = 1 };
 
 typedef struct pi_config {
   int layers, batch, hq, hkv, head_dim, block_tokens;
@@ -89,6 +90,9 @@ typedef struct pi_config {
   int gather_ctas;           /* UVA gather kernel grid (0 = one per SM) */
   int gather_depth;          /* 16-byte loads in flight per gather thread: 2, 4, 8 or 16
                                 (0 = 8) */
+  int evict_policy;          /* which free slots a recall takes first: PI_EVICT_ASCENDING
+                                (lowest slot index) or PI_EVICT_LRU (empty slots, then
+                                the block selected longest ago); placed before host_alloc */
   int host_alloc;            /* host store allocation: 0 = cudaHostAlloc (pinned,
                                 mapped); 1 = anonymous mmap advised for transparent huge
                                 pages, then cudaHostRegister (pinned, mapped) */
@@ -128,6 +132,8 @@ typedef struct pi_pool_views {
   int* step_nsel;            /* device [L][R][U] */
   int* step_table;           /* device [L][R][U][cap] */
   size_t block_bytes, frag_bytes, host_region_bytes;
+  int* slot_stamp;           /* device [R][L][U][P_max]: epoch a slot's block was last
+                                selected (-1 never); maintained under PI_EVICT_LRU */
 } pi_pool_views;
 
 /* ------------------------------------------------------------------ lifetime */
@@ -220,6 +226,11 @@ pi_status pi_recall(pi_pool* p, int layer, const int* sel, const int* nsel, int 
  * Errors: PI_ERR_INVALID (n > P_r, unsorted, out of range, head-wise pool). */
 pi_status pi_pool_preload(pi_pool* p, int layer, int req, const int* blocks, int n, pi_stream s);
 
+/* Switch the eviction policy for recalls issued afterwards (PI_EVICT_ASCENDING
+ * or PI_EVICT_LRU; head-wise pools included). Least-recently-selected is this
+ * library's variant: the pages leave eviction open. */
+pi_status pi_pool_set_evict(pi_pool* p, int policy);
+
 /* Retune the UVA gather: grid size (CTAs, > 0) and 16-byte loads in flight per
  * thread (2, 4, 8 or 16). Applies to calls issued afterwards. */
 pi_status pi_pool_set_gather(pi_pool* p, int ctas, int depth);
@@ -279,6 +290,12 @@ pi_status pi_sparse_decode_noalloc(const void* kv_slots, long long n_slots, int 
 pi_status pi_decode_step(pi_pool* p, const void* q_all, const void* k_new_all, const void* v_new_all,
                          const int* k_budget, int method, void* out_all, float* lse_all, pi_stream compute,
                          pi_stream copy, pi_step_stats* stats);
+
+/* How far selection (append + select + plan) runs ahead of attention inside
+ * pi_decode_step: select_ahead layers (1 = the next layer only), or 0 = every
+ * layer's selection first. Results are identical for every depth; depth only
+ * changes how well the copy stream stays busy. */
+pi_status pi_pool_set_pipeline(pi_pool* p, int select_ahead);
 
 /* pi_decode_step with HOST inputs and outputs (pinned or pageable): copies
  * q_all, k_new_all, v_new_all, k_budget host->device into pool-owned buffers,

@@ -12,7 +12,7 @@ import ctypes
 import numpy as np
 
 from . import _lib
-from ._lib import (PI_ERR_CUDA, PI_ERR_DEVICE, PI_ERR_FAULT_INJECTED, PI_ERR_HOST_ALLOC, PI_ERR_INVALID, PI_ERR_OOM,
+from ._lib import (PI_EVICT_ASCENDING, PI_EVICT_LRU, PI_ERR_CUDA, PI_ERR_DEVICE, PI_ERR_FAULT_INJECTED, PI_ERR_HOST_ALLOC, PI_ERR_INVALID, PI_ERR_OOM,
                    PI_ERR_POOL_FULL, PI_ERR_STATE, PI_ERR_TIMEOUT, PI_HEADWISE, PI_OK, PI_RECALL_MEMCPY,
                    PI_RECALL_STAGED, PI_RECALL_UVA, PI_SHARED, PiError, check, declared_functions, load, pi_config,
                    pi_pool_views, pi_recall_stats, pi_step_stats)
@@ -71,10 +71,11 @@ class Pool:
     def __init__(self, layers: int, batch: int, hq: int, hkv: int, head_dim: int, block_tokens: int,
                  max_blocks: int, pool_slots: int, k_max: int, window: int, select_mode: int = PI_SHARED,
                  host_layers: int = 0, staging_blocks: int = 0, gather_ctas: int = 0, pool_slots_per_req=None,
-                 gather_depth: int = 0, host_alloc: int = 0):
+                 gather_depth: int = 0, host_alloc: int = 0, evict_policy: int = 0):
         self.lib = load()
         cfg = pi_config(layers, batch, hq, hkv, head_dim, block_tokens, max_blocks, pool_slots, k_max, window,
-                        select_mode, host_layers, staging_blocks, gather_ctas, gather_depth, host_alloc, None)
+                        select_mode, host_layers, staging_blocks, gather_ctas, gather_depth, evict_policy, host_alloc,
+                        None)
         self._slots_arr = None
         if pool_slots_per_req is not None:
             self._slots_arr = (ctypes.c_int * batch)(*[int(x) for x in pool_slots_per_req])
@@ -182,6 +183,15 @@ class Pool:
         arr = np.ascontiguousarray(blocks, dtype=np.int32)
         check(self.lib.pi_pool_preload(self.h, layer, req, arr.ctypes.data if arr.size else None, int(arr.size),
                                        _stream(stream)), "pi_pool_preload")
+
+    def set_pipeline(self, select_ahead: int):
+        check(self.lib.pi_pool_set_pipeline(self.h, select_ahead), "pi_pool_set_pipeline")
+
+    def set_evict(self, policy: int):
+        check(self.lib.pi_pool_set_evict(self.h, policy), "pi_pool_set_evict")
+
+    def view_slot_stamp(self):
+        return device_view(self._views.slot_stamp, (self.R, self.L, self.U, self.p_max), "int32")
 
     def set_gather(self, ctas: int, depth: int):
         check(self.lib.pi_pool_set_gather(self.h, ctas, depth), "pi_pool_set_gather")

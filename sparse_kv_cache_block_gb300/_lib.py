@@ -19,13 +19,14 @@ PI_OK, PI_ERR_INVALID, PI_ERR_CUDA, PI_ERR_OOM, PI_ERR_HOST_ALLOC = 0, 1, 2, 3, 
 PI_ERR_POOL_FULL, PI_ERR_TIMEOUT, PI_ERR_DEVICE, PI_ERR_STATE, PI_ERR_FAULT_INJECTED = 5, 6, 7, 8, 9
 PI_SHARED, PI_HEADWISE = 0, 1
 PI_RECALL_UVA, PI_RECALL_MEMCPY, PI_RECALL_STAGED = 0, 1, 2
+PI_EVICT_ASCENDING, PI_EVICT_LRU = 0, 1
 
 
 class pi_config(ctypes.Structure):
     _fields_ = [("layers", c_int), ("batch", c_int), ("hq", c_int), ("hkv", c_int), ("head_dim", c_int),
                 ("block_tokens", c_int), ("max_blocks", c_int), ("pool_slots", c_int), ("k_max", c_int),
                 ("window", c_int), ("select_mode", c_int), ("host_layers", c_int), ("staging_blocks", c_int),
-                ("gather_ctas", c_int), ("gather_depth", c_int), ("host_alloc", c_int),
+                ("gather_ctas", c_int), ("gather_depth", c_int), ("evict_policy", c_int), ("host_alloc", c_int),
                 ("pool_slots_per_req", ctypes.POINTER(c_int))]
 
 
@@ -45,7 +46,8 @@ class pi_pool_views(ctypes.Structure):
     _fields_ = [("pool", c_void_p), ("slot_base", ctypes.POINTER(c_ll)), ("slots_per_req", ctypes.POINTER(c_int)),
                 ("kmean", c_void_p), ("ntok", c_void_p), ("slot_of_block", c_void_p), ("block_of_slot", c_void_p),
                 ("p_max", c_int), ("step_sel", c_void_p), ("step_nsel", c_void_p), ("step_table", c_void_p),
-                ("block_bytes", c_size_t), ("frag_bytes", c_size_t), ("host_region_bytes", c_size_t)]
+                ("block_bytes", c_size_t), ("frag_bytes", c_size_t), ("host_region_bytes", c_size_t),
+                ("slot_stamp", c_void_p)]
 
 
 class pi_kernel_timing(ctypes.Structure):
@@ -71,6 +73,8 @@ _SIGS = {
     "pi_pool_preload": (c_int, [_P, c_int, c_int, _P, c_int, _P]),
     "pi_pool_flush": (c_int, [_P, c_int, _P]),
     "pi_pool_set_gather": (c_int, [_P, c_int, c_int]),
+    "pi_pool_set_pipeline": (c_int, [_P, c_int]),
+    "pi_pool_set_evict": (c_int, [_P, c_int]),
     "pi_sparse_decode": (c_int, [_P, c_int, _P, _P, _P, _P, _P, _P, _P, _P]),
     "pi_sparse_decode_noalloc": (c_int, [_P, c_ll, c_int, c_int, c_int, c_int, c_int, c_int, _P, _P, _P, _P, _P,
                                          _P, _P, _P]),

@@ -47,6 +47,8 @@ struct pi_pool {
   uint8_t* host_dev = nullptr;   // device address of the same memory
   size_t host_bytes = 0;
   bool host_mmapped = false;     // mmap + cudaHostRegister instead of cudaHostAlloc
+  void* host_map = nullptr;      // the whole mapping (the store starts at an aligned offset in it)
+  size_t host_map_bytes = 0;
 
   // device state
   uint8_t* pool = nullptr;       // all slots
@@ -61,6 +63,9 @@ struct pi_pool {
   std::vector<int> ntok_h;        // host mirror [R][L]
   int* slot_of = nullptr;         // [R][L][U][max_blocks]
   int* block_of = nullptr;        // [R][L][U][p_max]
+  int* slot_stamp = nullptr;      // [R][L][U][p_max] last selection epoch (least-recently-selected policy)
+  int* epoch = nullptr;           // [R][L][U]
+  int lru_p2 = 0;                 // power of two >= p_max (sort width of the policy)
   unsigned* dev_status = nullptr;
 
   // per-layer scratch
@@ -99,6 +104,9 @@ struct pi_pool {
   // per-kernel timing inside pi_decode_step: events [step][layer][kind][2]
   std::vector<cudaEvent_t> tev;
   int timing_steps = 0, timing_used = 0;
+
+  // decode-step pipeline: layers selected ahead of attention (0 = all)
+  int select_ahead = 1;
 
   // fault injection
   long long fault_recall_at = 0;

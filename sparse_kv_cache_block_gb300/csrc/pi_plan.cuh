@@ -47,6 +47,8 @@ __device__ __forceinline__ int cta_excl_scan(int v, int* warp_sums, int& total) 
 struct UnitArgs {
   const int* sel;        // this unit's selection [n], ascending
   int n;
+  int* stamp;            // least-recently-selected policy: this unit's slot stamps [P], else nullptr
+  int* epoch;            // and its epoch counter
   const int* sob;        // this unit's slot_of_block [max_blocks]
   const int* bos;        // this unit's block_of_slot [P]
   int P, max_blocks;
@@ -57,9 +59,11 @@ struct UnitArgs {
   unsigned* status;
 };
 
-// Shared memory: bits [ceil(max_blocks/32)] + miss_pos [cap] + free_list [cap].
+// Shared memory: bits [ceil(max_blocks/32)] + miss_pos [cap] + free_list [cap];
+// with the least-recently-selected policy also keys [lru_p2] (8-byte aligned).
 template <int NT>
-__device__ void plan_unit(const UnitArgs& a, unsigned* bits, int* miss_pos, int* free_list, int* warp_sums) {
+__device__ void plan_unit(const UnitArgs& a, unsigned* bits, int* miss_pos, int* free_list, int* warp_sums,
+                          unsigned long long* keys = nullptr, int lru_p2 = 0) {
   const int words = (a.max_blocks + 31) / 32;
   const int n = a.n;
   for (int w = threadIdx.x; w < words; w += NT) bits[w] = 0u;
@@ -98,7 +102,63 @@ __device__ void plan_unit(const UnitArgs& a, unsigned* bits, int* miss_pos, int*
   }
 
   int nf = 0;
-  for (int base = 0; base < a.P && nf < nm; base += NT) {
+  if (a.stamp) {
+    // least recently selected first: every free slot keyed by (stamp + 1, slot),
+    // sorted ascending; empty slots carry stamp -1 and come first
+    const int e_new = *a.epoch + 1;
+    for (int base = 0; base < a.P; base += NT) {
+      const int s = base + threadIdx.x;
+      int fr = 0;
+      if (s < a.P) {
+        const int bb = a.bos[s];
+        if (bb < 0) fr = 1;
+        else if (bb >= a.max_blocks) pi_flag(a.status, PI_DEV_BAD_INDEX);
+        else fr = ((bits[bb >> 5] >> (bb & 31)) & 1u) ? 0 : 1;
+      }
+      int tot;
+      const int pos = cta_excl_scan<NT>(fr, warp_sums, tot);
+      if (fr) {
+        const int st = (a.bos[s] < 0) ? -1 : a.stamp[s];
+        keys[nf + pos] = ((unsigned long long)(unsigned)(st + 1) << 32) | (unsigned)s;
+      }
+      nf += tot;
+    }
+    int n2 = 1;
+    while (n2 < nf) n2 <<= 1;
+    if (n2 > lru_p2) {
+      if (threadIdx.x == 0) pi_flag(a.status, PI_DEV_BAD_INDEX);
+      n2 = 0;
+      nf = 0;
+    }
+    for (int i = nf + threadIdx.x; i < n2; i += NT) keys[i] = ~0ull;
+    __syncthreads();
+    for (int k = 2; k <= n2; k <<= 1)
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        for (int i = threadIdx.x; i < n2; i += NT) {
+          const int ix = i ^ j;
+          if (ix > i) {
+            const unsigned long long x = keys[i], y = keys[ix];
+            const bool up = (i & k) == 0;
+            if ((x > y) == up) {
+              keys[i] = y;
+              keys[ix] = x;
+            }
+          }
+        }
+        __syncthreads();
+      }
+    for (int j = threadIdx.x; j < nm && j < nf; j += NT) free_list[j] = (int)(keys[j] & 0xffffffffu);
+    // stamp the slots of the hits now; new entries are stamped at commit
+    for (int i = threadIdx.x; i < n; i += NT) {
+      const int b = a.sel[i];
+      if (b >= 0 && b < a.max_blocks) {
+        const int s = a.sob[b];
+        if (s >= 0 && s < a.P) a.stamp[s] = e_new;
+      }
+    }
+    __syncthreads();
+  }
+  for (int base = 0; base < a.P && nf < nm && !a.stamp; base += NT) {
     const int s = base + threadIdx.x;
     int fr = 0;
     if (s < a.P) {
@@ -124,22 +184,34 @@ __device__ void plan_unit(const UnitArgs& a, unsigned* bits, int* miss_pos, int*
     for (int j = threadIdx.x; j < nm; j += NT) a.table[miss_pos[j]] = -1;
     return;
   }
+  const int stamp_new = a.stamp ? *a.epoch + 1 : 0;
   for (int j = threadIdx.x; j < nm; j += NT) {
     const int i = miss_pos[j];
     const int s = free_list[j];
-    a.plan[j] = make_int4(a.sel[i], s, a.bos[s], 0);
+    a.plan[j] = make_int4(a.sel[i], s, a.bos[s], stamp_new);
     a.table[i] = s;
   }
+  __syncthreads();
   if (threadIdx.x == 0) {
+    if (a.stamp) *a.epoch = stamp_new;
     *a.plan_n = nm;
     atomicAdd(reinterpret_cast<unsigned long long*>(a.counts + 0), (unsigned long long)nm);
     atomicAdd(reinterpret_cast<unsigned long long*>(a.counts + 1), (unsigned long long)(n - nm));
   }
 }
 
-// bytes of dynamic shared memory plan_unit needs
-__host__ __device__ inline size_t plan_smem_bytes(int max_blocks, int cap) {
-  return sizeof(int) * ((size_t)(max_blocks + 31) / 32 + 2 * (size_t)cap);
+// smallest power of two >= n (n >= 1)
+__host__ __device__ inline int pow2_at_least(int n) {
+  int p = 1;
+  while (p < n) p <<= 1;
+  return p;
+}
+
+// bytes of dynamic shared memory plan_unit needs; layout: [keys u64 x lru_p2]
+// [bits][miss_pos][free_list]
+__host__ __device__ inline size_t plan_smem_bytes(int max_blocks, int cap, int lru_p2 = 0) {
+  return sizeof(unsigned long long) * (size_t)lru_p2 +
+         sizeof(int) * ((size_t)(max_blocks + 31) / 32 + 2 * (size_t)cap);
 }
 
 }  // namespace pi_plan

@@ -49,13 +49,13 @@ static void pool_free(pi_pool* p) {
                       p->slot_of,    p->block_of,   p->dev_status, p->sel_scores,  p->sel_counter, p->plan_n,
                       p->plan,       p->recall_counts, p->attn_o,  p->attn_ml,     p->attn_counter, p->step_sel,
                       p->step_nsel,  p->step_table, p->step_in,    p->step_out,    p->stage_dev,
-                      p->ntok_stage};
+                      p->ntok_stage, p->slot_stamp, p->epoch};
   for (void* d : dev_ptrs)
     if (d) cudaFree(d);
   if (p->host) {
     if (p->host_mmapped) {
       cudaHostUnregister(p->host);
-      munmap(p->host, p->host_bytes);
+      munmap(p->host_map, p->host_map_bytes);
     } else {
       cudaFreeHost(p->host);
     }
@@ -92,6 +92,7 @@ static bool valid_config(const pi_config& c) {
       c.gather_depth != 16)
     return false;
   if (c.host_alloc != 0 && c.host_alloc != 1) return false;
+  if (c.evict_policy != PI_EVICT_ASCENDING && c.evict_policy != PI_EVICT_LRU) return false;
   if (c.gather_ctas < 0) return false;
   int cap = c.k_max + c.window;
   if (c.pool_slots_per_req) {
@@ -161,21 +162,33 @@ extern "C" pi_status pi_pool_create(const pi_config* cfg, pi_pool** out) {
     acc += (long long)p->L * p->P_h[r];
   }
   p->total_slots = acc;
+  p->lru_p2 = 1;
+  while (p->lru_p2 < p->p_max) p->lru_p2 <<= 1;
+  if (p->lru_p2 > 8192) {  // the least-recently-selected sort keeps all free slots in shared memory
+    if (cfg->evict_policy == PI_EVICT_LRU) { pool_free(p); return PI_ERR_INVALID; }
+  }
 
   // host store: pinned and mapped
   p->host_bytes = p->region_bytes * (size_t)p->host_layers * (size_t)p->R;
   if (fault && strcmp(fault, "pinned_alloc_fail") == 0) { pool_free(p); return PI_ERR_HOST_ALLOC; }
   if (cfg->host_alloc == 1) {
-    void* m = mmap(nullptr, p->host_bytes, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS, -1, 0);
-    if (m == MAP_FAILED) {
+    // reserve extra so the store can start on a huge-page boundary (512 MiB covers
+    // the largest transparent huge page of 4 KiB / 16 KiB / 64 KiB base-page kernels)
+    const size_t align = (size_t)512 << 20;
+    p->host_map_bytes = p->host_bytes + align;
+    void* raw = mmap(nullptr, p->host_map_bytes, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS, -1, 0);
+    if (raw == MAP_FAILED) {
       pool_free(p);
       return PI_ERR_HOST_ALLOC;
     }
+    p->host_map = raw;
+    void* m = reinterpret_cast<void*>((reinterpret_cast<uintptr_t>(raw) + align - 1) & ~(uintptr_t)(align - 1));
     madvise(m, p->host_bytes, MADV_HUGEPAGE);  // advice only: the kernel may decline
     memset(m, 0, p->host_bytes);               // fault the pages in before pinning
     if (cudaHostRegister(m, p->host_bytes, cudaHostRegisterMapped | cudaHostRegisterPortable) != cudaSuccess) {
       cudaGetLastError();
-      munmap(m, p->host_bytes);
+      munmap(raw, p->host_map_bytes);
+      p->host_map = nullptr;
       pool_free(p);
       return PI_ERR_HOST_ALLOC;
     }
@@ -215,6 +228,8 @@ extern "C" pi_status pi_pool_create(const pi_config* cfg, pi_pool** out) {
   TRY_ALLOC(dalloc(&p->ntok_stage, RL));
   TRY_ALLOC(dalloc(&p->slot_of, RL * p->U * p->max_blocks, true, 0xFF));
   TRY_ALLOC(dalloc(&p->block_of, RL * p->U * p->p_max, true, 0xFF));
+  TRY_ALLOC(dalloc(&p->slot_stamp, RL * p->U * p->p_max, true, 0xFF));
+  TRY_ALLOC(dalloc(&p->epoch, RL * p->U));
   TRY_ALLOC(dalloc(&p->dev_status, 1));
   TRY_ALLOC(dalloc(&p->sel_scores, (size_t)p->L * RU * p->max_blocks));
   TRY_ALLOC(dalloc(&p->sel_counter, (size_t)p->L * RU));
@@ -303,6 +318,7 @@ extern "C" pi_status pi_pool_get_views(pi_pool* p, pi_pool_views* v) {
   v->block_bytes = p->block_bytes;
   v->frag_bytes = p->frag_bytes;
   v->host_region_bytes = p->region_bytes;
+  v->slot_stamp = p->slot_stamp;
   return PI_OK;
 }
 
@@ -345,6 +361,8 @@ extern "C" pi_status pi_pool_flush(pi_pool* p, int layer, pi_stream s) {
       PI_CUDA_TRY(cudaMemsetAsync(p->slot_of + rl * p->U * p->max_blocks, 0xFF,
                                   sizeof(int) * p->U * p->max_blocks, st));
       PI_CUDA_TRY(cudaMemsetAsync(p->block_of + rl * p->U * p->p_max, 0xFF, sizeof(int) * p->U * p->p_max, st));
+      PI_CUDA_TRY(cudaMemsetAsync(p->slot_stamp + rl * p->U * p->p_max, 0xFF, sizeof(int) * p->U * p->p_max, st));
+      PI_CUDA_TRY(cudaMemsetAsync(p->epoch + rl * p->U, 0, sizeof(int) * p->U, st));
     }
   return PI_OK;
 }
@@ -369,6 +387,10 @@ extern "C" pi_status pi_pool_preload(pi_pool* p, int layer, int req, const int* 
   PI_CUDA_TRY(cudaMemcpy(p->slot_of + rl * p->max_blocks, sob.data(), sizeof(int) * p->max_blocks,
                          cudaMemcpyHostToDevice));
   PI_CUDA_TRY(cudaMemcpy(p->block_of + rl * p->p_max, bos.data(), sizeof(int) * p->p_max, cudaMemcpyHostToDevice));
+  std::vector<int> stamps(p->p_max, -1);
+  for (int i = 0; i < n; i++) stamps[i] = 0;  // preloaded blocks count as selected at epoch 0
+  PI_CUDA_TRY(cudaMemcpy(p->slot_stamp + rl * p->p_max, stamps.data(), sizeof(int) * p->p_max, cudaMemcpyHostToDevice));
+  PI_CUDA_TRY(cudaMemset(p->epoch + rl, 0, sizeof(int)));
   const uint8_t* src = (const uint8_t*)pi_host_kv(p, layer, req);
   for (int i = 0; i < n; i++) {
     uint8_t* dst = p->pool + (size_t)pi_global_slot(p, req, layer, i) * p->block_bytes;
@@ -427,5 +449,12 @@ extern "C" pi_status pi_pool_set_gather(pi_pool* p, int ctas, int depth) {
   if (!p || ctas <= 0 || (depth != 2 && depth != 4 && depth != 8 && depth != 16)) return PI_ERR_INVALID;
   p->cfg.gather_ctas = ctas;
   p->cfg.gather_depth = depth;
+  return PI_OK;
+}
+
+extern "C" pi_status pi_pool_set_evict(pi_pool* p, int policy) {
+  if (!p || (policy != PI_EVICT_ASCENDING && policy != PI_EVICT_LRU)) return PI_ERR_INVALID;
+  if (policy == PI_EVICT_LRU && p->lru_p2 > 8192) return PI_ERR_INVALID;
+  p->cfg.evict_policy = policy;
   return PI_OK;
 }

@@ -35,15 +35,19 @@ struct PlanParams {
   const int* P;
   long long* counts;  // [0] misses, [1] hits
   unsigned* status;
-  int layer, L, U, max_blocks, p_max, cap;
+  int* slot_stamp;    // nullptr unless the least-recently-selected policy is on
+  int* epoch;
+  int layer, L, U, max_blocks, p_max, cap, lru_p2;
 };
 
 // One CTA per unit (request, or request x KV head). Writes the table and the
 // plan; the maps are committed later by the copy kernel.
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
-  extern __shared__ int sm[];
+  extern __shared__ __align__(16) unsigned char smraw[];
   __shared__ int warp_sums[kPlanThreads / 32];
   const int words = (p.max_blocks + 31) / 32;
+  unsigned long long* keys = reinterpret_cast<unsigned long long*>(smraw);
+  int* sm = reinterpret_cast<int*>(smraw + sizeof(unsigned long long) * (p.slot_stamp ? p.lru_p2 : 0));
   const int u = blockIdx.x;
   const int r = u / p.U, gu = u % p.U;
   const size_t rlu = ((size_t)r * p.L + p.layer) * p.U + gu;
@@ -64,7 +68,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
   a.plan_n = p.plan_n + u;
   a.counts = p.counts;
   a.status = p.status;
-  pi_plan::plan_unit<kPlanThreads>(a, reinterpret_cast<unsigned*>(sm), sm + words, sm + words + p.cap, warp_sums);
+  a.stamp = p.slot_stamp ? p.slot_stamp + rlu * p.p_max : nullptr;
+  a.epoch = p.slot_stamp ? p.epoch + rlu : nullptr;
+  pi_plan::plan_unit<kPlanThreads>(a, reinterpret_cast<unsigned*>(sm), sm + words, sm + words + p.cap, warp_sums,
+                                   keys, p.lru_p2);
 }
 
 struct GatherParams {
@@ -72,6 +79,7 @@ struct GatherParams {
   const int4* plan;
   int* slot_of;
   int* block_of;
+  int* slot_stamp;           // stamped at commit under the least-recently-selected policy
   const uint8_t* host_src;   // device address of this layer's host store (request 0)
   uint8_t* host_dst;         // same memory, writable (write-through of new tokens)
   const uint8_t* stage_src;  // staged arm: device staging buffer (entries e_begin..)
@@ -220,6 +228,7 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(GatherParams g) 
       if (pe.z >= 0) sob[pe.z] = -1;
       sob[pe.x] = pe.y;
       bos[pe.y] = pe.x;
+      if (g.slot_stamp) g.slot_stamp[rlu * g.p_max + pe.y] = pe.w;
     }
   }
 }
@@ -245,7 +254,11 @@ cudaError_t pi_launch_plan(pi_pool* p, int layer, const int* sel, const int* nse
   pp.max_blocks = p->max_blocks;
   pp.p_max = p->p_max;
   pp.cap = p->cap;
-  const size_t smem = pi_plan::plan_smem_bytes(p->max_blocks, p->cap);
+  const bool lru = p->cfg.evict_policy == PI_EVICT_LRU;
+  pp.slot_stamp = lru ? p->slot_stamp : nullptr;
+  pp.epoch = lru ? p->epoch : nullptr;
+  pp.lru_p2 = lru ? p->lru_p2 : 0;
+  const size_t smem = pi_plan::plan_smem_bytes(p->max_blocks, p->cap, pp.lru_p2);
   if (smem > 48 * 1024) cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   plan_kernel<<<(unsigned)RU, kPlanThreads, smem, s>>>(pp);
   return cudaGetLastError();
@@ -258,6 +271,7 @@ static GatherParams gather_params(pi_pool* p, int layer) {
   g.plan = p->plan + (size_t)layer * RU * p->cap;
   g.slot_of = p->slot_of;
   g.block_of = p->block_of;
+  g.slot_stamp = (p->cfg.evict_policy == PI_EVICT_LRU) ? p->slot_stamp : nullptr;
   g.host_src = p->host_dev + (size_t)(layer % p->host_layers) * p->R * p->region_bytes;
   g.host_dst = p->host_dev + (size_t)(layer % p->host_layers) * p->R * p->region_bytes;
   g.stage_src = nullptr;

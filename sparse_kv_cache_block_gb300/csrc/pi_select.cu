@@ -160,6 +160,9 @@ struct SelParams {
   int4* plan;
   long long* counts;
   int p_max;
+  int* slot_stamp;     // least-recently-selected policy, else nullptr
+  int* epoch;
+  int lru_p2;
 };
 
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -362,7 +365,9 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelParams p) {
   // by this CTA; the barrier makes it visible to every thread of the CTA)
   __syncthreads();
   const int words = (p.max_blocks + 31) / 32;
-  uint32_t* pl = dyn + (p.keys_smem > 0 ? ((p.keys_smem + 3) & ~3) : 0);
+  unsigned char* plb = reinterpret_cast<unsigned char*>(dyn + (p.keys_smem > 0 ? ((p.keys_smem + 3) & ~3) : 0));
+  unsigned long long* lkeys = reinterpret_cast<unsigned long long*>(plb);
+  uint32_t* pl = reinterpret_cast<uint32_t*>(plb + sizeof(unsigned long long) * (p.slot_stamp ? p.lru_p2 : 0));
   pi_plan::UnitArgs a;
   a.sel = out;
   a.n = kk + nrecent;
@@ -376,8 +381,10 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelParams p) {
   a.plan_n = p.plan_n + u;
   a.counts = p.counts;
   a.status = p.status;
+  a.stamp = p.slot_stamp ? p.slot_stamp + rlu * p.p_max : nullptr;
+  a.epoch = p.slot_stamp ? p.epoch + rlu : nullptr;
   pi_plan::plan_unit<kSelThreads>(a, pl, reinterpret_cast<int*>(pl) + words, reinterpret_cast<int*>(pl) + words + p.cap,
-                                  warp_sums);
+                                  warp_sums, lkeys, p.lru_p2);
 }
 
 }  // namespace
@@ -472,8 +479,12 @@ cudaError_t pi_launch_select(pi_pool* p, int layer, const void* q, const int* k_
   sp.plan = p->plan + (size_t)layer * RU * p->cap;
   sp.counts = p->recall_counts + (size_t)layer * 4;
   sp.p_max = p->p_max;
+  const bool lru = p->cfg.evict_policy == PI_EVICT_LRU;
+  sp.slot_stamp = lru ? p->slot_stamp : nullptr;
+  sp.epoch = lru ? p->epoch : nullptr;
+  sp.lru_p2 = lru ? p->lru_p2 : 0;
   size_t smem = sizeof(uint32_t) * (size_t)((sp.keys_smem + 3) & ~3);
-  if (fused_table) smem += pi_plan::plan_smem_bytes(p->max_blocks, p->cap);
+  if (fused_table) smem += pi_plan::plan_smem_bytes(p->max_blocks, p->cap, sp.lru_p2);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;

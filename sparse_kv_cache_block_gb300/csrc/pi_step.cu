@@ -6,8 +6,9 @@
 // recall latency hides behind compute. Here the compute stream runs append,
 // selection and attention, the copy stream runs the recall (plan + gather), and
 // events order them: recall(l) waits for select(l); attention(l) waits for
-// recall(l). select(l+1) is issued before attention(l), so recall(l+1) overlaps
-// attention(l). With the UVA gather arm no step needs the host.
+// recall(l). Selections are issued ahead of attention (one layer, or all layers
+// first), so recall(l+1) overlaps attention(l). With the UVA gather arm no step
+// needs the host.
 #include <cstring>
 #include <vector>
 
@@ -71,7 +72,21 @@ static pi_status step_impl(pi_pool* p, const uint8_t* q_all, const uint8_t* k_ne
     return PI_OK;
   };
 
-  pi_status st = select(0);
+  // selections run `ahead` layers in front of attention (0: every layer first).
+  // Any depth gives the same results: a layer's plan reads only maps committed by
+  // the previous step's gather of that layer, which the compute stream has
+  // already waited for; deeper lookahead only keeps the copy stream fed.
+  const int ahead = (p->select_ahead <= 0 || p->select_ahead > p->L) ? p->L : p->select_ahead;
+  int next_sel = 0;
+  pi_status st = PI_OK;
+  auto select_upto = [&](int upto) -> pi_status {
+    for (; next_sel <= upto && next_sel < p->L; next_sel++) {
+      pi_status s2 = select(next_sel);
+      if (s2 != PI_OK) return s2;
+    }
+    return PI_OK;
+  };
+  st = select_upto(ahead - 1);
   if (st != PI_OK) return st;
   for (int l = 0; l < p->L; l++) {
     PI_CUDA_TRY(cudaStreamWaitEvent(ys, p->ev_sel[l], 0));
@@ -86,10 +101,8 @@ static pi_status step_impl(pi_pool* p, const uint8_t* q_all, const uint8_t* k_ne
       if (st != PI_OK) return st;
     }
     PI_CUDA_TRY(cudaEventRecord(p->ev_rec[l], ys));
-    if (l + 1 < p->L) {
-      st = select(l + 1);
-      if (st != PI_OK) return st;
-    }
+    st = select_upto(l + ahead);
+    if (st != PI_OK) return st;
     PI_CUDA_TRY(cudaStreamWaitEvent(cs, p->ev_rec[l], 0));
     PI_TIMED(l, PI_K_ATTENTION, cs,
              pi_launch_attention(p, l, q_all + (size_t)l * q_bytes, sel_of(l), tab_of(l), nsel_of(l),
@@ -191,5 +204,11 @@ extern "C" pi_status pi_pool_get_timing(pi_pool* p, pi_kernel_timing* out) {
         out[k].total_ms += ms;
       }
   p->timing_used = 0;
+  return PI_OK;
+}
+
+extern "C" pi_status pi_pool_set_pipeline(pi_pool* p, int select_ahead) {
+  if (!p || select_ahead < 0) return PI_ERR_INVALID;
+  p->select_ahead = select_ahead;
   return PI_OK;
 }

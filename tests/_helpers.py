@@ -33,6 +33,7 @@ class Workload:
     select_mode: int = 0       # 0 shared, 1 head-wise
     max_blocks: int = 0        # 0: enough for the prefill plus `steps` appended tokens
     slots_per_req: list | None = None
+    evict_policy: int = 0      # 0 lowest free slot first, 1 least recently selected first
 
     def __post_init__(self):
         if self.max_blocks == 0:
@@ -102,12 +103,29 @@ class OracleModel:
                     for r in range(w.batch) for l in range(w.layers) for u in range(U)}
         self.bos = {(r, l, u): np.full(P[r], -1, dtype=np.int32)
                     for r in range(w.batch) for l in range(w.layers) for u in range(U)}
-        self.recalled = {}  # (r, l) -> list of (unit, block, slot) moved by the last recall
+        self.stamp = {(r, l, u): np.full(P[r], -1, dtype=np.int32)
+                      for r in range(w.batch) for l in range(w.layers) for u in range(U)}
+        self.epoch = {(r, l, u): 0 for r in range(w.batch) for l in range(w.layers) for u in range(U)}
 
     def preload(self, l, r, blocks):
         for s, b in enumerate(blocks):
             self.sob[(r, l, 0)][b] = s
             self.bos[(r, l, 0)][s] = b
+            self.stamp[(r, l, 0)][s] = 0
+
+    def flush(self):
+        for key in self.sob:
+            self.sob[key][:] = -1
+            self.bos[key][:] = -1
+            self.stamp[key][:] = -1
+            self.epoch[key] = 0
+
+    def _plan(self, sel, r, l, u):
+        key = (r, l, u)
+        if self.w.evict_policy == 1:
+            self.epoch[key] += 1
+            return oracle.recall_plan_lru(sel, self.sob[key], self.bos[key], self.stamp[key], self.epoch[key])
+        return oracle.recall_plan(sel, self.sob[key], self.bos[key])
 
     def append(self, l, k_new, v_new):
         w = self.w
@@ -142,13 +160,13 @@ class OracleModel:
         tables = []
         for r, s in enumerate(sels):
             if self.U == 1:
-                res = oracle.recall_plan(s, self.sob[(r, l, 0)], self.bos[(r, l, 0)])
+                res = self._plan(s, r, l, 0)
                 assert res is not None
                 tables.append(res[0])
             else:
                 tt = []
                 for g in range(self.U):
-                    res = oracle.recall_plan(s[g], self.sob[(r, l, g)], self.bos[(r, l, g)])
+                    res = self._plan(s[g], r, l, g)
                     assert res is not None
                     tt.append(res[0])
                 tables.append(tt)

@@ -30,7 +30,7 @@ def _built():
 def make_pool(w: Workload, **kw):
     return pi.Pool(w.layers, w.batch, w.hq, w.hkv, w.head_dim, w.block_tokens, w.max_blocks, w.pool_slots, w.k,
                    w.window, select_mode=w.select_mode, host_layers=(w.host_layers if w.host_layers != w.layers else 0),
-                   pool_slots_per_req=w.slots_per_req, **kw)
+                   pool_slots_per_req=w.slots_per_req, evict_policy=w.evict_policy, **kw)
 
 
 def prefill(pool, w: Workload):
@@ -80,6 +80,9 @@ def check_tables_maps_bytes(pool, om, w, l, sels, tables, table_dev):
             assert np.array_equal(got, want_t), (r, u, got, want_t)
             assert np.array_equal(sob[r, l, u], om.sob[(r, l, u)]), (r, l, u)
             assert np.array_equal(bos[r, l, u, : om.P[r]], om.bos[(r, l, u)]), (r, l, u)
+            if w.evict_policy == 1:
+                st = pool.view_slot_stamp().cpu().numpy()
+                assert np.array_equal(st[r, l, u, : om.P[r]], om.stamp[(r, l, u)]), (r, l, u)
             s_list = sels[r] if U == 1 else sels[r][u]
             reg = om.reg[(w.host_layer(l), r)]
             for i, b in enumerate(s_list):
@@ -165,15 +168,19 @@ def test_small_config_layer_calls(method):
         assert st2["fragments"] == 0 and st2["hits"] == 36
 
 
-@pytest.mark.parametrize("method", METHODS)
-def test_multistep_pipeline_8b_shape(method):
+@pytest.mark.parametrize("method,evict,ahead", [(m, 0, 1) for m in METHODS] +
+                         [(pi.PI_RECALL_UVA, 1, 1), (pi.PI_RECALL_MEMCPY, 1, 1), (pi.PI_RECALL_UVA, 0, 0),
+                          (pi.PI_RECALL_UVA, 1, 0)])
+def test_multistep_pipeline_8b_shape(method, evict, ahead):
     """Llama-3-8B-shaped heads (32 q / 8 KV, d 128, blocks of 64), 2 layers, 2
     requests with ragged tails, heavy-hitter blocks, AR(1) queries, 4 pipelined
-    decode steps with token append; all per-layer results checked each step."""
+    decode steps with token append; all per-layer results checked each step,
+    under both eviction policies."""
     w = Workload(layers=2, batch=2, hq=32, hkv=8, head_dim=128, block_tokens=64, ntok=[4000, 2500], k=8, window=2,
-                 pool_slots=14, steps=4, rho=0.9, heavy_frac=0.05, heavy_shift=2.0, seed=3)
+                 pool_slots=14, steps=4, rho=0.9, heavy_frac=0.05, heavy_shift=2.0, seed=3, evict_policy=evict)
     L, R = w.layers, w.batch
     with make_pool(w) as pool:
+        pool.set_pipeline(ahead)
         prefill(pool, w)
         om = OracleModel(w)
         qs = queries(w)
@@ -204,11 +211,12 @@ def test_multistep_pipeline_8b_shape(method):
             assert st["selected"] == sum(int(nsel_v[l].sum()) for l in range(L))
 
 
-def test_headwise_arm():
+@pytest.mark.parametrize("evict", [0, 1])
+def test_headwise_arm(evict):
     """Per-KV-head selection (the fragmenting comparison arm): own top-k per head,
     fragment-granular recall into per-head sub-slots, attention per head."""
     w = Workload(layers=1, batch=2, hq=16, hkv=4, head_dim=128, block_tokens=32, ntok=[2000, 1500], k=6, window=0,
-                 pool_slots=6, steps=1, seed=5, select_mode=1)
+                 pool_slots=6, steps=1, seed=5, select_mode=1, evict_policy=evict)
     with make_pool(w) as pool:
         prefill(pool, w)
         om = OracleModel(w)
@@ -219,9 +227,7 @@ def test_headwise_arm():
                 assert stats["bytes"] == stats["fragments"] * pool.frag_bytes
             pool.flush()
             torch.cuda.synchronize()
-            for key in om.sob:
-                om.sob[key][:] = -1
-                om.bos[key][:] = -1
+            om.flush()
 
 
 def test_select_all_equals_dense_attention():
@@ -271,11 +277,12 @@ def test_edge_cases_tiny_and_degenerate():
                 run_layer(pool, om, w, 0, q, kreq, method)
 
 
-def test_preload_then_recall_counts_hits():
+@pytest.mark.parametrize("evict", [0, 1])
+def test_preload_then_recall_counts_hits(evict):
     """Initial residency (a seeded sample) placed in slots 0.. ; later recalls only
-    move what is missing, evicting unselected blocks."""
+    move what is missing, evicting unselected blocks; three queries in a row."""
     w = Workload(layers=1, batch=2, hq=32, hkv=8, head_dim=128, block_tokens=64, ntok=[6000, 6000], k=12, window=2,
-                 pool_slots=40, steps=1, seed=9, heavy_frac=0.05)
+                 pool_slots=40, steps=3, seed=9, heavy_frac=0.05, evict_policy=evict)
     with make_pool(w) as pool:
         prefill(pool, w)
         om = OracleModel(w)
@@ -284,9 +291,10 @@ def test_preload_then_recall_counts_hits():
             blocks = synth.sample_sorted(w.seed, synth.KIND_RESIDENT, 0, r, nb, 30)
             pool.preload(0, r, blocks)
             om.preload(0, r, blocks)
-        q = queries(w)[0][0]
-        stats, ref_sel = run_layer(pool, om, w, 0, q, [w.k] * w.batch, pi.PI_RECALL_UVA)
-        assert stats["hits"] + stats["fragments"] == sum(len(s) for s in ref_sel)
+        for step in range(w.steps):
+            q = queries(w)[step][0]
+            stats, ref_sel = run_layer(pool, om, w, 0, q, [w.k] * w.batch, pi.PI_RECALL_UVA)
+            assert stats["hits"] + stats["fragments"] == sum(len(s) for s in ref_sel)
 
 
 def test_decode_step_host_matches_device_inputs():
@@ -387,3 +395,18 @@ def test_bounded_wait_times_out_into_status_word():
         prefill(pool, w)
         om = OracleModel(w)
         run_layer(pool, om, w, 0, queries(w)[0][0], [w.k], pi.PI_RECALL_UVA)
+
+
+@pytest.mark.parametrize("hq,hkv", [(64, 8), (16, 8), (8, 8), (32, 4)], ids=["G8_70b", "G2", "G1", "G8_4kv"])
+def test_query_group_sizes(hq, hkv):
+    """Group sizes 1, 2 and 8 (the Llama-3-70B slice: 64 q / 8 KV heads fills every
+    column of the mma's N = 8), ragged tails, two layers."""
+    w = Workload(layers=2, batch=2, hq=hq, hkv=hkv, head_dim=128, block_tokens=64, ntok=[5000, 3001], k=16, window=4,
+                 pool_slots=24, steps=1, seed=31 + hq + hkv, heavy_frac=0.05)
+    with make_pool(w) as pool:
+        prefill(pool, w)
+        om = OracleModel(w)
+        check_kmean(pool, om, w)
+        q = queries(w)[0]
+        for l in range(w.layers):
+            run_layer(pool, om, w, l, q[l], [w.k, 7], pi.PI_RECALL_UVA)
