@@ -261,7 +261,8 @@ def run_ours(args, cfg, rank, world, local_rank):
     pi.load()
     L, R, Hq, Hkv, D, B = (cfg[k] for k in ("layers", "batch", "hq", "hkv", "head_dim", "block_tokens"))
     K, Wm = args.steps, args.warmup
-    total_steps = 2 * Wm + 4 * K + 4
+    prewarm_cap = 400  # warm-up runs at least W steps and at least args.warmup_s seconds, at most this many
+    total_steps = prewarm_cap + Wm + 4 * K + 4
     ntok0 = cfg["ntok"]
     max_blocks = -(-(ntok0 + total_steps) // B) + 1
     seed = rank_seed(args.seed, rank)
@@ -290,6 +291,8 @@ def run_ours(args, cfg, rank, world, local_rank):
                    evict_policy=(pi.PI_EVICT_LRU if args.evict == "lru" else pi.PI_EVICT_ASCENDING))
     if args.select_ahead >= 0:
         pool.set_pipeline(args.select_ahead)
+    if args.gather_exclusive:
+        pool.set_gather(args.gather_ctas, args.gather_depth or 8, True)
     t0 = time.time()
     for hl in range(host_layers):
         for r in range(R):
@@ -339,10 +342,20 @@ def run_ours(args, cfg, rank, world, local_rank):
         if world > 1:
             torch.distributed.barrier()
 
-    # warm-up (the pool starts empty: step 0 recalls every selected block)
+    # warm-up (the pool starts empty: step 0 recalls every selected block). The
+    # first ~0.3 s of pipelined steps after the host-side setup run slower than the
+    # steady state on this machine (measured), so warm-up lasts at least W steps and
+    # at least --warmup-s seconds; the JSON reports the steps actually run.
     warm_stats = []
-    for _ in range(Wm):
+    for _ in range(min(Wm, 3)):
         warm_stats.append(run_step(stats=True))
+    t_w = time.time()
+    warm_steps = len(warm_stats)
+    while warm_steps < Wm or (time.time() - t_w < args.warmup_s and warm_steps < prewarm_cap):
+        run_step()
+        warm_steps += 1
+        if warm_steps % 8 == 0:
+            torch.cuda.synchronize()
     torch.cuda.synchronize()
     assert pool.device_status() == pi.PI_OK
 
@@ -474,7 +487,7 @@ def run_ours(args, cfg, rank, world, local_rank):
     recall_gbs = kernels.get("gather", {}).get("achieved_gbs")
     line = {
         "metric": METRIC, "value": tok_s, "unit": "tok/s", "n_gpus": world, "steps": K, "warmup": Wm,
-        "ms_per_step": 1e3 * elapsed_max / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "ms_per_step": 1e3 * elapsed_max / K, "higher_is_better": True, "warmup_steps_run": warm_steps, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic (seeded; shapes of the pages' Llama-3 long-context workloads)",
         "config": {"workload": cfg["workload"], "layers": L, "batch": R, "hq": Hq, "hkv": Hkv, "head_dim": D,
                    "block_tokens": B, "context": ntok0, "top_k": cfg["k"], "window": cfg["window"],
@@ -483,7 +496,7 @@ def run_ours(args, cfg, rank, world, local_rank):
                    "recall": args.method, "evict": args.evict, "host_layers": host_layers,
                    "select_ahead": ("library default" if args.select_ahead < 0 else (args.select_ahead or "all")),
                    "gather_ctas": args.gather_ctas or "one per SM",
-                   "gather_depth": args.gather_depth or 8, "host_alloc": ["cudaHostAlloc", "mmap+THP+register"][args.host_alloc],
+                   "gather_depth": args.gather_depth or 8, "gather_exclusive": args.gather_exclusive, "host_alloc": ["cudaHostAlloc", "mmap+THP+register"][args.host_alloc],
                    "parallelism": f"replicas{world}" if world > 1 else "single",
                    "l2": "inputs larger than L2 (host store and pool far exceed 129 MB)"},
         "recall": {"gbs": recall_gbs, "h2d_peak_gbs": h2d_peak,
@@ -633,12 +646,16 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--warmup-s", type=float, default=1.5,
+                    help="warm-up also lasts at least this many seconds of pipelined steps")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="c2", choices=sorted(CONFIGS))
     ap.add_argument("--method", default="uva", choices=["uva", "memcpy", "staged"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--gather-ctas", type=int, default=0)
     ap.add_argument("--gather-depth", type=int, default=0)
+    ap.add_argument("--gather-exclusive", action="store_true",
+                    help="run the gather on a few SMs of its own (1024-thread CTAs)")
     ap.add_argument("--evict", default="ascending", choices=["ascending", "lru"],
                     help="pool eviction policy of the headline passes")
     ap.add_argument("--no-variant", action="store_true", help="skip the extra pass under the other eviction policy")

@@ -231,9 +231,13 @@ pi_status pi_pool_preload(pi_pool* p, int layer, int req, const int* blocks, int
  * library's variant: the pages leave eviction open. */
 pi_status pi_pool_set_evict(pi_pool* p, int policy);
 
-/* Retune the UVA gather: grid size (CTAs, > 0) and 16-byte loads in flight per
- * thread (2, 4, 8 or 16). Applies to calls issued afterwards. */
-pi_status pi_pool_set_gather(pi_pool* p, int ctas, int depth);
+/* Retune the UVA gather: grid size (CTAs; 0 = default), 16-byte loads in flight
+ * per thread (2, 4, 8 or 16) and placement: exclusive = 0 runs 256-thread CTAs,
+ * one per SM (default 152), beside other kernels; exclusive = 1 runs 1024-thread
+ * CTAs (default 24) that reserve enough shared memory to keep attention CTAs off
+ * their SMs, so host-link reads stay on a few SMs. Applies to calls issued
+ * afterwards. */
+pi_status pi_pool_set_gather(pi_pool* p, int ctas, int depth, int exclusive);
 
 /* Forget residency of `layer` (-1 = all layers): every slot empty. Bytes stay. */
 pi_status pi_pool_flush(pi_pool* p, int layer, pi_stream s);
@@ -296,6 +300,11 @@ pi_status pi_decode_step(pi_pool* p, const void* q_all, const void* k_new_all, c
  * layer's selection first. Results are identical for every depth; depth only
  * changes how well the copy stream stays busy. */
 pi_status pi_pool_set_pipeline(pi_pool* p, int select_ahead);
+
+/* Split count of the attention kernel (CTAs per request and KV head; 0 = the
+ * default: one wave at the kernel's occupancy). Clamped to what the pool's
+ * scratch holds. Results change only by floating-point summation order. */
+pi_status pi_pool_set_attention(pi_pool* p, int splits);
 
 /* pi_decode_step with HOST inputs and outputs (pinned or pageable): copies
  * q_all, k_new_all, v_new_all, k_budget host->device into pool-owned buffers,

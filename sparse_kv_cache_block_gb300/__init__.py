@@ -187,14 +187,17 @@ class Pool:
     def set_pipeline(self, select_ahead: int):
         check(self.lib.pi_pool_set_pipeline(self.h, select_ahead), "pi_pool_set_pipeline")
 
+    def set_attention(self, splits: int):
+        check(self.lib.pi_pool_set_attention(self.h, splits), "pi_pool_set_attention")
+
     def set_evict(self, policy: int):
         check(self.lib.pi_pool_set_evict(self.h, policy), "pi_pool_set_evict")
 
     def view_slot_stamp(self):
         return device_view(self._views.slot_stamp, (self.R, self.L, self.U, self.p_max), "int32")
 
-    def set_gather(self, ctas: int, depth: int):
-        check(self.lib.pi_pool_set_gather(self.h, ctas, depth), "pi_pool_set_gather")
+    def set_gather(self, ctas: int, depth: int, exclusive: bool = False):
+        check(self.lib.pi_pool_set_gather(self.h, ctas, depth, int(exclusive)), "pi_pool_set_gather")
 
     def flush(self, layer: int = -1, stream=None):
         check(self.lib.pi_pool_flush(self.h, layer, _stream(stream)), "pi_pool_flush")

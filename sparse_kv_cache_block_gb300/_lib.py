@@ -72,8 +72,9 @@ _SIGS = {
     "pi_recall": (c_int, [_P, c_int, _P, _P, c_int, _P, ctypes.POINTER(pi_recall_stats), _P]),
     "pi_pool_preload": (c_int, [_P, c_int, c_int, _P, c_int, _P]),
     "pi_pool_flush": (c_int, [_P, c_int, _P]),
-    "pi_pool_set_gather": (c_int, [_P, c_int, c_int]),
+    "pi_pool_set_gather": (c_int, [_P, c_int, c_int, c_int]),
     "pi_pool_set_pipeline": (c_int, [_P, c_int]),
+    "pi_pool_set_attention": (c_int, [_P, c_int]),
     "pi_pool_set_evict": (c_int, [_P, c_int]),
     "pi_sparse_decode": (c_int, [_P, c_int, _P, _P, _P, _P, _P, _P, _P, _P]),
     "pi_sparse_decode_noalloc": (c_int, [_P, c_ll, c_int, c_int, c_int, c_int, c_int, c_int, _P, _P, _P, _P, _P,

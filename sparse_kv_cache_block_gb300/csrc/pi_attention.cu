@@ -347,6 +347,8 @@ int attn_smem_bytes(int D, int B) {
 
 }  // namespace
 
+int pi_attention_smem(int D, int B) { return attn_smem_bytes(D, B); }
+
 cudaError_t pi_launch_attention(pi_pool* p, int layer, const void* q, const int* sel, const int* table,
                                 const int* nsel, void* out, float* lse, float* logits, cudaStream_t s) {
   AttnParams ap;
@@ -378,6 +380,7 @@ cudaError_t pi_launch_attention(pi_pool* p, int layer, const void* q, const int*
   const int smem = attn_smem_bytes(p->D, p->B);
   const int per_sm = max(1, (228 * 1024) / (smem + 1024));
   int splits = (int)(((long long)per_sm * p->num_sms) / (long long)units);
+  if (p->attn_splits > 0) splits = p->attn_splits;
   splits = max(splits, (p->cap + 511) / 512);
   splits = max(1, min(splits, p->attn_max_splits));
   int bps = (p->cap + splits - 1) / splits;

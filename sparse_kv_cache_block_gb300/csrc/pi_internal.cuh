@@ -107,6 +107,10 @@ struct pi_pool {
 
   // decode-step pipeline: layers selected ahead of attention (0 = all)
   int select_ahead = 1;
+  // gather on a few SMs of its own (1024-thread CTAs holding enough shared memory
+  // to keep attention CTAs away)
+  bool gather_exclusive = false;
+  int attn_splits = 0;            // attention split count override (0 = one wave at full occupancy)
 
   // fault injection
   long long fault_recall_at = 0;
@@ -132,6 +136,7 @@ cudaError_t pi_launch_gather(pi_pool* p, int layer, const uint8_t* stage_src, bo
 cudaError_t pi_launch_attention(pi_pool* p, int layer, const void* q, const int* sel, const int* table,
                                 const int* nsel, void* out, float* lse, float* logits, cudaStream_t s);
 bool pi_make_tmap(pi_pool* p);
+int pi_attention_smem(int D, int B);  // dynamic shared memory of one attention CTA
 
 // --------------------------------------------------------------- device helpers
 #ifdef __CUDACC__

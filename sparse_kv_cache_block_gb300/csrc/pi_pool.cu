@@ -239,7 +239,7 @@ extern "C" pi_status pi_pool_create(const pi_config* cfg, pi_pool** out) {
   // attention split-K partials: enough splits to give every SM work at any batch
   {
     int units = p->R * p->Hkv;
-    int s = (4 * p->num_sms + units - 1) / units;
+    int s = (8 * p->num_sms + units - 1) / units;
     if (s < 1) s = 1;
     if (s > p->cap) s = p->cap;
     if (s < (p->cap + 511) / 512) s = (p->cap + 511) / 512;
@@ -445,10 +445,11 @@ extern "C" pi_status pi_selftest_bounded_wait(pi_pool* p, long long limit_cycles
   return pi_get_device_status(p);
 }
 
-extern "C" pi_status pi_pool_set_gather(pi_pool* p, int ctas, int depth) {
-  if (!p || ctas <= 0 || (depth != 2 && depth != 4 && depth != 8 && depth != 16)) return PI_ERR_INVALID;
+extern "C" pi_status pi_pool_set_gather(pi_pool* p, int ctas, int depth, int exclusive) {
+  if (!p || ctas < 0 || (depth != 2 && depth != 4 && depth != 8 && depth != 16)) return PI_ERR_INVALID;
   p->cfg.gather_ctas = ctas;
   p->cfg.gather_depth = depth;
+  p->gather_exclusive = exclusive != 0;
   return PI_OK;
 }
 

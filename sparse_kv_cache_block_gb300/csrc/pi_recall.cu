@@ -21,7 +21,6 @@
 namespace {
 
 constexpr int kPlanThreads = 256;
-constexpr int kGatherThreads = 256;
 
 
 struct PlanParams {
@@ -109,7 +108,7 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* ptr) {
 // every request through to the host store, and a CTA that copies a chunk of the
 // block holding that token overwrites the token's rows from k_new/v_new, so the
 // pool never depends on when the host write lands.
-template <int kGatherDepth>
+template <int kGatherDepth, int kGatherThreads>
 __global__ void __launch_bounds__(kGatherThreads) gather_kernel(GatherParams g) {
   constexpr int kChunkBytes = kGatherThreads * 16 * kGatherDepth;
   extern __shared__ long long prefix[];  // [units + 1]
@@ -303,25 +302,47 @@ static GatherParams gather_params(pi_pool* p, int layer) {
   return g;
 }
 
-template <int DEPTH>
+template <int DEPTH, int THREADS>
 static cudaError_t launch_gather_t(int ctas, size_t smem, const GatherParams& g, cudaStream_t s) {
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(gather_kernel<DEPTH>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(gather_kernel<DEPTH, THREADS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  gather_kernel<DEPTH><<<ctas, kGatherThreads, smem, s>>>(g);
+  gather_kernel<DEPTH, THREADS><<<ctas, THREADS, smem, s>>>(g);
   return cudaGetLastError();
 }
 
-static cudaError_t launch_gather(pi_pool* p, const GatherParams& g, cudaStream_t s) {
-  const size_t smem = sizeof(long long) * ((size_t)g.units + 1);
-  const int ctas = p->cfg.gather_ctas > 0 ? p->cfg.gather_ctas : p->num_sms;
-  switch (p->cfg.gather_depth) {
-    case 2: return launch_gather_t<2>(ctas, smem, g, s);
-    case 4: return launch_gather_t<4>(ctas, smem, g, s);
-    case 16: return launch_gather_t<16>(ctas, smem, g, s);
-    default: return launch_gather_t<8>(ctas, smem, g, s);
+template <int THREADS>
+static cudaError_t launch_gather_d(int depth, int ctas, size_t smem, const GatherParams& g, cudaStream_t s) {
+  switch (depth) {
+    case 2: return launch_gather_t<2, THREADS>(ctas, smem, g, s);
+    case 4: return launch_gather_t<4, THREADS>(ctas, smem, g, s);
+    case 16:
+      // 1024-thread CTAs have 64 registers per thread: sixteen loads in flight would spill
+      if constexpr (THREADS <= 256) return launch_gather_t<16, THREADS>(ctas, smem, g, s);
+      return launch_gather_t<8, THREADS>(ctas, smem, g, s);
+    default: return launch_gather_t<8, THREADS>(ctas, smem, g, s);
   }
+}
+
+// Default: 256-thread CTAs, one per SM, sharing SMs with whatever else runs.
+// Exclusive: 1024-thread CTAs that reserve enough shared memory that no attention
+// CTA fits beside them, so the long-latency host-link reads stay on a few SMs and
+// the other SMs' memory requests never queue behind them.
+static cudaError_t launch_gather(pi_pool* p, const GatherParams& g, cudaStream_t s) {
+  size_t smem = sizeof(long long) * ((size_t)g.units + 1);
+  if (p->gather_exclusive) {
+    const int ctas = p->cfg.gather_ctas > 0 ? p->cfg.gather_ctas : 24;
+    const size_t attn = (size_t)pi_attention_smem(p->D, p->B);
+    const size_t sm_bytes = 228 * 1024, reserve = 1024;
+    size_t pad = (sm_bytes > attn + 2 * reserve) ? sm_bytes - attn - 2 * reserve + 1024 : 0;
+    if (pad > 220 * 1024) pad = 220 * 1024;
+    if (smem < pad) smem = pad;
+    return launch_gather_d<1024>(p->cfg.gather_depth, ctas, smem, g, s);
+  }
+  const int ctas = p->cfg.gather_ctas > 0 ? p->cfg.gather_ctas : p->num_sms;
+  return launch_gather_d<256>(p->cfg.gather_depth, ctas, smem, g, s);
 }
 
 cudaError_t pi_launch_gather(pi_pool* p, int layer, const uint8_t* stage_src, bool copy, bool commit,

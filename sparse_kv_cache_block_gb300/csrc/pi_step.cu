@@ -212,3 +212,9 @@ extern "C" pi_status pi_pool_set_pipeline(pi_pool* p, int select_ahead) {
   p->select_ahead = select_ahead;
   return PI_OK;
 }
+
+extern "C" pi_status pi_pool_set_attention(pi_pool* p, int splits) {
+  if (!p || splits < 0) return PI_ERR_INVALID;
+  p->attn_splits = splits;
+  return PI_OK;
+}

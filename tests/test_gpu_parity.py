@@ -168,10 +168,11 @@ def test_small_config_layer_calls(method):
         assert st2["fragments"] == 0 and st2["hits"] == 36
 
 
-@pytest.mark.parametrize("method,evict,ahead", [(m, 0, 1) for m in METHODS] +
-                         [(pi.PI_RECALL_UVA, 1, 1), (pi.PI_RECALL_MEMCPY, 1, 1), (pi.PI_RECALL_UVA, 0, 0),
-                          (pi.PI_RECALL_UVA, 1, 0)])
-def test_multistep_pipeline_8b_shape(method, evict, ahead):
+@pytest.mark.parametrize("method,evict,ahead,exclusive", [(m, 0, 1, False) for m in METHODS] +
+                         [(pi.PI_RECALL_UVA, 1, 1, False), (pi.PI_RECALL_MEMCPY, 1, 1, False),
+                          (pi.PI_RECALL_UVA, 0, 0, False), (pi.PI_RECALL_UVA, 1, 0, False),
+                          (pi.PI_RECALL_UVA, 0, 1, True), (pi.PI_RECALL_UVA, 1, 1, True)])
+def test_multistep_pipeline_8b_shape(method, evict, ahead, exclusive):
     """Llama-3-8B-shaped heads (32 q / 8 KV, d 128, blocks of 64), 2 layers, 2
     requests with ragged tails, heavy-hitter blocks, AR(1) queries, 4 pipelined
     decode steps with token append; all per-layer results checked each step,
@@ -181,6 +182,8 @@ def test_multistep_pipeline_8b_shape(method, evict, ahead):
     L, R = w.layers, w.batch
     with make_pool(w) as pool:
         pool.set_pipeline(ahead)
+        if exclusive:
+            pool.set_gather(5, 8, True)  # few CTAs: every CTA loops over many chunks
         prefill(pool, w)
         om = OracleModel(w)
         qs = queries(w)
