@@ -232,20 +232,27 @@ class OracleSample:
         return done, time.perf_counter() - t0
 
 
-def cpu_baseline(cfg, seed, qs, max_blocks, region_source, budget_s=15.0, n_units=24):
-    """Oracle on a bounded sample: n_units (request, layer) pairs for one decode step."""
+def cpu_baseline(cfg, seed, qs, max_blocks, region_source, budget_s=15.0, n_units=16):
+    """Oracle on a bounded sample: n_units (request, layer) pairs stepped through
+    consecutive decode steps until about budget_s seconds of oracle work."""
     L, R = cfg["layers"], cfg["batch"]
     rng = np.random.default_rng(seed + 17)
     all_units = [(r, l) for r in range(R) for l in range(L)]
     pick = [all_units[i] for i in sorted(rng.choice(len(all_units), size=min(n_units, len(all_units)),
                                                     replace=False))]
     samp = OracleSample(cfg, seed, pick, max_blocks, region_source)
-    done, secs = samp.step(qs[0], 0, budget_s)
+    done, secs, steps = 0, 0.0, 0
+    while secs < budget_s and steps < qs.shape[0]:
+        d, t = samp.step(qs[steps], steps)
+        done += d
+        secs += t
+        steps += 1
     per_unit = secs / max(done, 1)
     tok_s = 1.0 / (per_unit * L)   # one token of one request needs L units
     return {"value": tok_s, "unit": "tok/s", "cores": 1, "kind": "oracle",
-            "sample": f"{done} (request, layer) units of one decode step (append, select, plan, recall copy, "
-                      f"fp64 attention), {secs:.1f} s single-threaded; tokens/s = 1 / (s per unit x {L} layers)"}
+            "sample": f"{len(pick)} (request, layer) units x {steps} decode steps = {done} unit-steps (append, "
+                      f"select, plan, recall copy, fp64 attention), {secs:.1f} s single-threaded; "
+                      f"tokens/s = 1 / (s per unit-step x {L} layers)"}
 
 
 # ------------------------------------------------------------------ main arm
@@ -291,8 +298,8 @@ def run_ours(args, cfg, rank, world, local_rank):
                    evict_policy=(pi.PI_EVICT_LRU if args.evict == "lru" else pi.PI_EVICT_ASCENDING))
     if args.select_ahead >= 0:
         pool.set_pipeline(args.select_ahead)
-    if args.gather_exclusive:
-        pool.set_gather(args.gather_ctas, args.gather_depth or 8, True)
+    if args.gather_placement == "shared" or args.gather_ctas or args.gather_depth:
+        pool.set_gather(args.gather_ctas, args.gather_depth or 8, args.gather_placement == "exclusive")
     t0 = time.time()
     for hl in range(host_layers):
         for r in range(R):
@@ -495,8 +502,8 @@ def run_ours(args, cfg, rank, world, local_rank):
                                                        if slots_per_req else None),
                    "recall": args.method, "evict": args.evict, "host_layers": host_layers,
                    "select_ahead": ("library default" if args.select_ahead < 0 else (args.select_ahead or "all")),
-                   "gather_ctas": args.gather_ctas or "one per SM",
-                   "gather_depth": args.gather_depth or 8, "gather_exclusive": args.gather_exclusive, "host_alloc": ["cudaHostAlloc", "mmap+THP+register"][args.host_alloc],
+                   "gather_ctas": args.gather_ctas or "default",
+                   "gather_depth": args.gather_depth or 8, "gather_placement": args.gather_placement, "host_alloc": ["cudaHostAlloc", "mmap+THP+register"][args.host_alloc],
                    "parallelism": f"replicas{world}" if world > 1 else "single",
                    "l2": "inputs larger than L2 (host store and pool far exceed 129 MB)"},
         "recall": {"gbs": recall_gbs, "h2d_peak_gbs": h2d_peak,
@@ -654,8 +661,8 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--gather-ctas", type=int, default=0)
     ap.add_argument("--gather-depth", type=int, default=0)
-    ap.add_argument("--gather-exclusive", action="store_true",
-                    help="run the gather on a few SMs of its own (1024-thread CTAs)")
+    ap.add_argument("--gather-placement", default="exclusive", choices=["exclusive", "shared"],
+                    help="gather on a quarter of the SMs with 1024-thread CTAs (library default) or one CTA per SM")
     ap.add_argument("--evict", default="ascending", choices=["ascending", "lru"],
                     help="pool eviction policy of the headline passes")
     ap.add_argument("--no-variant", action="store_true", help="skip the extra pass under the other eviction policy")

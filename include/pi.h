@@ -87,7 +87,7 @@ typedef struct pi_config {
                                 tokens for aliased layers). */
   int staging_blocks;        /* staged recall arm: staging capacity in copy units
                                 (0 = as many as fit in 256 MiB) */
-  int gather_ctas;           /* UVA gather kernel grid (0 = one per SM) */
+  int gather_ctas;           /* UVA gather kernel grid (0 = default; see pi_pool_set_gather) */
   int gather_depth;          /* 16-byte loads in flight per gather thread: 2, 4, 8 or 16
                                 (0 = 8) */
   int evict_policy;          /* which free slots a recall takes first: PI_EVICT_ASCENDING
@@ -232,11 +232,11 @@ pi_status pi_pool_preload(pi_pool* p, int layer, int req, const int* blocks, int
 pi_status pi_pool_set_evict(pi_pool* p, int policy);
 
 /* Retune the UVA gather: grid size (CTAs; 0 = default), 16-byte loads in flight
- * per thread (2, 4, 8 or 16) and placement: exclusive = 0 runs 256-thread CTAs,
- * one per SM (default 152), beside other kernels; exclusive = 1 runs 1024-thread
- * CTAs (default 24) that reserve enough shared memory to keep attention CTAs off
- * their SMs, so host-link reads stay on a few SMs. Applies to calls issued
- * afterwards. */
+ * per thread (2, 4, 8 or 16) and placement: exclusive = 1 (the default) runs
+ * 1024-thread CTAs (default: a quarter of the SMs) that reserve enough shared
+ * memory to keep attention CTAs off their SMs, so host-link reads stay on a few
+ * SMs; exclusive = 0 runs 256-thread CTAs, one per SM, beside other kernels.
+ * Applies to calls issued afterwards. */
 pi_status pi_pool_set_gather(pi_pool* p, int ctas, int depth, int exclusive);
 
 /* Forget residency of `layer` (-1 = all layers): every slot empty. Bytes stay. */

@@ -109,7 +109,7 @@ struct pi_pool {
   int select_ahead = 1;
   // gather on a few SMs of its own (1024-thread CTAs holding enough shared memory
   // to keep attention CTAs away)
-  bool gather_exclusive = false;
+  bool gather_exclusive = true;
   int attn_splits = 0;            // attention split count override (0 = one wave at full occupancy)
 
   // fault injection

@@ -163,6 +163,8 @@ struct SelParams {
   int* slot_stamp;     // least-recently-selected policy, else nullptr
   int* epoch;
   int lru_p2;
+  int map_cache_blocks;  // fused plan: blocks of slot_of_block cached in shared memory (0: read global)
+  int map_cache_slots;   // and slots of block_of_slot
 };
 
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -266,6 +268,22 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelParams p) {
   const int kk = min(kreq, ncand);
   int* out = p.sel + (size_t)u * p.cap;
   uint32_t* keys = dyn;
+  // fused plan: start reading this unit's slot maps now, so their latency hides
+  // behind the radix passes and the plan runs from shared memory
+  const size_t rlu_m = rl * p.U + g;
+  const int P_r = p.P[r];
+  int* sob_c = nullptr;
+  int* bos_c = nullptr;
+  if (p.table && p.map_cache_blocks >= nb && p.map_cache_slots >= P_r) {
+    unsigned char* after = reinterpret_cast<unsigned char*>(dyn + ((p.keys_smem + 3) & ~3)) +
+                           pi_plan::plan_smem_bytes(p.max_blocks, p.cap, p.slot_stamp ? p.lru_p2 : 0);
+    sob_c = reinterpret_cast<int*>(after);
+    bos_c = sob_c + p.map_cache_blocks;
+    const int* sob_g = p.slot_of + rlu_m * p.max_blocks;
+    const int* bos_g = p.block_of + rlu_m * p.p_max;
+    for (int b = threadIdx.x; b < nb; b += kSelThreads) sob_c[b] = sob_g[b];
+    for (int s = threadIdx.x; s < P_r; s += kSelThreads) bos_c[s] = bos_g[s];
+  }
   const bool cached = ncand <= p.keys_smem;
   if (cached)
     for (int b = threadIdx.x; b < ncand; b += kSelThreads) keys[b] = order_key(__ldcg(sc + b));
@@ -372,8 +390,8 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelParams p) {
   a.sel = out;
   a.n = kk + nrecent;
   const size_t rlu = rl * p.U + g;
-  a.sob = p.slot_of + rlu * p.max_blocks;
-  a.bos = p.block_of + rlu * p.p_max;
+  a.sob = sob_c ? sob_c : p.slot_of + rlu * p.max_blocks;
+  a.bos = bos_c ? bos_c : p.block_of + rlu * p.p_max;
   a.P = p.P[r];
   a.max_blocks = p.max_blocks;
   a.table = p.table + (size_t)u * p.cap;
@@ -485,6 +503,15 @@ cudaError_t pi_launch_select(pi_pool* p, int layer, const void* q, const int* k_
   sp.lru_p2 = lru ? p->lru_p2 : 0;
   size_t smem = sizeof(uint32_t) * (size_t)((sp.keys_smem + 3) & ~3);
   if (fused_table) smem += pi_plan::plan_smem_bytes(p->max_blocks, p->cap, sp.lru_p2);
+  // slot maps cached for the fused plan when they are small (cached only up to
+  // the largest block count of this layer; nothing beyond it is ever looked up)
+  sp.map_cache_blocks = 0;
+  sp.map_cache_slots = 0;
+  if (fused_table && nb_max <= 4096 && p->p_max <= 4096) {
+    sp.map_cache_blocks = (nb_max + 3) & ~3;
+    sp.map_cache_slots = (p->p_max + 3) & ~3;
+    smem += sizeof(int) * (size_t)(sp.map_cache_blocks + sp.map_cache_slots);
+  }
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;

@@ -168,11 +168,12 @@ def test_small_config_layer_calls(method):
         assert st2["fragments"] == 0 and st2["hits"] == 36
 
 
-@pytest.mark.parametrize("method,evict,ahead,exclusive", [(m, 0, 1, False) for m in METHODS] +
-                         [(pi.PI_RECALL_UVA, 1, 1, False), (pi.PI_RECALL_MEMCPY, 1, 1, False),
-                          (pi.PI_RECALL_UVA, 0, 0, False), (pi.PI_RECALL_UVA, 1, 0, False),
-                          (pi.PI_RECALL_UVA, 0, 1, True), (pi.PI_RECALL_UVA, 1, 1, True)])
-def test_multistep_pipeline_8b_shape(method, evict, ahead, exclusive):
+@pytest.mark.parametrize("method,evict,ahead,placement", [(m, 0, 1, "default") for m in METHODS] +
+                         [(pi.PI_RECALL_UVA, 1, 1, "default"), (pi.PI_RECALL_MEMCPY, 1, 1, "default"),
+                          (pi.PI_RECALL_UVA, 0, 0, "default"), (pi.PI_RECALL_UVA, 1, 0, "default"),
+                          (pi.PI_RECALL_UVA, 0, 1, "few"), (pi.PI_RECALL_UVA, 1, 1, "shared"),
+                          (pi.PI_RECALL_UVA, 0, 1, "shared")])
+def test_multistep_pipeline_8b_shape(method, evict, ahead, placement):
     """Llama-3-8B-shaped heads (32 q / 8 KV, d 128, blocks of 64), 2 layers, 2
     requests with ragged tails, heavy-hitter blocks, AR(1) queries, 4 pipelined
     decode steps with token append; all per-layer results checked each step,
@@ -182,8 +183,10 @@ def test_multistep_pipeline_8b_shape(method, evict, ahead, exclusive):
     L, R = w.layers, w.batch
     with make_pool(w) as pool:
         pool.set_pipeline(ahead)
-        if exclusive:
-            pool.set_gather(5, 8, True)  # few CTAs: every CTA loops over many chunks
+        if placement == "few":
+            pool.set_gather(5, 8, True)  # few exclusive CTAs: every CTA loops over many chunks
+        elif placement == "shared":
+            pool.set_gather(0, 8, False)  # one 256-thread CTA per SM beside other kernels
         prefill(pool, w)
         om = OracleModel(w)
         qs = queries(w)
