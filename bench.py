@@ -296,8 +296,8 @@ def run_ours(args, cfg, rank, world, local_rank):
                    cfg["window"], host_layers=(host_layers if host_layers < L else 0), gather_ctas=args.gather_ctas,
                    pool_slots_per_req=slots_per_req, gather_depth=args.gather_depth, host_alloc=args.host_alloc,
                    evict_policy=(pi.PI_EVICT_LRU if args.evict == "lru" else pi.PI_EVICT_ASCENDING))
-    if args.select_ahead >= 0:
-        pool.set_pipeline(args.select_ahead)
+    if args.select_ahead >= 0 or args.two_streams:
+        pool.set_pipeline(max(args.select_ahead, 0) if args.select_ahead >= 0 else 1, not args.two_streams)
     if args.gather_placement == "shared" or args.gather_ctas or args.gather_depth:
         pool.set_gather(args.gather_ctas, args.gather_depth or 8, args.gather_placement == "exclusive")
     t0 = time.time()
@@ -502,6 +502,7 @@ def run_ours(args, cfg, rank, world, local_rank):
                                                        if slots_per_req else None),
                    "recall": args.method, "evict": args.evict, "host_layers": host_layers,
                    "select_ahead": ("library default" if args.select_ahead < 0 else (args.select_ahead or "all")),
+                   "streams": 2 if args.two_streams else 3,
                    "gather_ctas": args.gather_ctas or "default",
                    "gather_depth": args.gather_depth or 8, "gather_placement": args.gather_placement, "host_alloc": ["cudaHostAlloc", "mmap+THP+register"][args.host_alloc],
                    "parallelism": f"replicas{world}" if world > 1 else "single",
@@ -666,6 +667,9 @@ def main():
     ap.add_argument("--evict", default="ascending", choices=["ascending", "lru"],
                     help="pool eviction policy of the headline passes")
     ap.add_argument("--no-variant", action="store_true", help="skip the extra pass under the other eviction policy")
+    ap.add_argument("--two-streams", action="store_true",
+                    help="attention on the compute stream (default: on the pool's own stream, so selection runs "
+                         "ahead and consecutive steps overlap)")
     ap.add_argument("--select-ahead", type=int, default=-1,
                     help="layers selected ahead of attention in the step (0 = all; -1 = library default)")
     ap.add_argument("--host-alloc", type=int, default=0, choices=[0, 1],

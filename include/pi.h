@@ -295,11 +295,15 @@ pi_status pi_decode_step(pi_pool* p, const void* q_all, const void* k_new_all, c
                          const int* k_budget, int method, void* out_all, float* lse_all, pi_stream compute,
                          pi_stream copy, pi_step_stats* stats);
 
-/* How far selection (append + select + plan) runs ahead of attention inside
- * pi_decode_step: select_ahead layers (1 = the next layer only), or 0 = every
- * layer's selection first. Results are identical for every depth; depth only
- * changes how well the copy stream stays busy. */
-pi_status pi_pool_set_pipeline(pi_pool* p, int select_ahead);
+/* Shape of pi_decode_step's pipeline (default: attention_stream = 1).
+ * attention_stream = 0: two streams, the
+ * caller's compute stream runs append, selection and attention, selection running
+ * select_ahead layers in front of attention (1 = the next layer only, 0 = every
+ * layer first). attention_stream = 1: attention runs on a stream the pool owns,
+ * selection runs ahead as far as the data allow, and consecutive steps overlap
+ * (select_ahead is ignored); the caller's compute stream still completes after
+ * the whole step. Results are identical in every shape. Synchronizes the device. */
+pi_status pi_pool_set_pipeline(pi_pool* p, int select_ahead, int attention_stream);
 
 /* Split count of the attention kernel (CTAs per request and KV head; 0 = the
  * default: one wave at the kernel's occupancy). Clamped to what the pool's

@@ -184,8 +184,8 @@ class Pool:
         check(self.lib.pi_pool_preload(self.h, layer, req, arr.ctypes.data if arr.size else None, int(arr.size),
                                        _stream(stream)), "pi_pool_preload")
 
-    def set_pipeline(self, select_ahead: int):
-        check(self.lib.pi_pool_set_pipeline(self.h, select_ahead), "pi_pool_set_pipeline")
+    def set_pipeline(self, select_ahead: int = 1, attention_stream: bool = True):
+        check(self.lib.pi_pool_set_pipeline(self.h, select_ahead, int(attention_stream)), "pi_pool_set_pipeline")
 
     def set_attention(self, splits: int):
         check(self.lib.pi_pool_set_attention(self.h, splits), "pi_pool_set_attention")

@@ -73,7 +73,7 @@ _SIGS = {
     "pi_pool_preload": (c_int, [_P, c_int, c_int, _P, c_int, _P]),
     "pi_pool_flush": (c_int, [_P, c_int, _P]),
     "pi_pool_set_gather": (c_int, [_P, c_int, c_int, c_int]),
-    "pi_pool_set_pipeline": (c_int, [_P, c_int]),
+    "pi_pool_set_pipeline": (c_int, [_P, c_int, c_int]),
     "pi_pool_set_attention": (c_int, [_P, c_int]),
     "pi_pool_set_evict": (c_int, [_P, c_int]),
     "pi_sparse_decode": (c_int, [_P, c_int, _P, _P, _P, _P, _P, _P, _P, _P]),

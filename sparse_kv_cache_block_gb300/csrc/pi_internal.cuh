@@ -107,6 +107,11 @@ struct pi_pool {
 
   // decode-step pipeline: layers selected ahead of attention (0 = all)
   int select_ahead = 1;
+  // attention on a library-owned third stream (selection then runs freely ahead
+  // and consecutive steps overlap); ev_att[l] = attention of layer l done
+  bool attn_stream_on = true;
+  cudaStream_t attn_stream = nullptr;
+  std::vector<cudaEvent_t> ev_att;
   // gather on a few SMs of its own (1024-thread CTAs holding enough shared memory
   // to keep attention CTAs away)
   bool gather_exclusive = true;

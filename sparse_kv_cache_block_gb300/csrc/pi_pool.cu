@@ -44,6 +44,8 @@ static void pool_free(pi_pool* p) {
   for (auto e : p->ev_sel) cudaEventDestroy(e);
   for (auto e : p->ev_rec) cudaEventDestroy(e);
   if (p->ev_start) cudaEventDestroy(p->ev_start);
+  for (auto e : p->ev_att) cudaEventDestroy(e);
+  if (p->attn_stream) cudaStreamDestroy(p->attn_stream);
   for (auto e : p->tev) cudaEventDestroy(e);
   void* dev_ptrs[] = {p->pool,       p->slot_base,  p->P,          p->kmean,       p->tail_sum,    p->ntok,
                       p->slot_of,    p->block_of,   p->dev_status, p->sel_scores,  p->sel_counter, p->plan_n,
@@ -265,6 +267,16 @@ extern "C" pi_status pi_pool_create(const pi_config* cfg, pi_pool** out) {
   }
 
   if (cudaEventCreateWithFlags(&p->ev_start, cudaEventDisableTiming) != cudaSuccess) {
+    pool_free(p);
+    return PI_ERR_CUDA;
+  }
+  p->ev_att.resize(p->L, nullptr);
+  for (int l = 0; l < p->L; l++)
+    if (cudaEventCreateWithFlags(&p->ev_att[l], cudaEventDisableTiming) != cudaSuccess) {
+      pool_free(p);
+      return PI_ERR_CUDA;
+    }
+  if (cudaStreamCreateWithFlags(&p->attn_stream, cudaStreamNonBlocking) != cudaSuccess) {
     pool_free(p);
     return PI_ERR_CUDA;
   }

@@ -72,23 +72,7 @@ static pi_status step_impl(pi_pool* p, const uint8_t* q_all, const uint8_t* k_ne
     return PI_OK;
   };
 
-  // selections run `ahead` layers in front of attention (0: every layer first).
-  // Any depth gives the same results: a layer's plan reads only maps committed by
-  // the previous step's gather of that layer, which the compute stream has
-  // already waited for; deeper lookahead only keeps the copy stream fed.
-  const int ahead = (p->select_ahead <= 0 || p->select_ahead > p->L) ? p->L : p->select_ahead;
-  int next_sel = 0;
-  pi_status st = PI_OK;
-  auto select_upto = [&](int upto) -> pi_status {
-    for (; next_sel <= upto && next_sel < p->L; next_sel++) {
-      pi_status s2 = select(next_sel);
-      if (s2 != PI_OK) return s2;
-    }
-    return PI_OK;
-  };
-  st = select_upto(ahead - 1);
-  if (st != PI_OK) return st;
-  for (int l = 0; l < p->L; l++) {
+  auto recall_layer = [&](int l) -> pi_status {
     PI_CUDA_TRY(cudaStreamWaitEvent(ys, p->ev_sel[l], 0));
     if (uva) {
       p->recall_calls++;
@@ -97,23 +81,72 @@ static pi_status step_impl(pi_pool* p, const uint8_t* q_all, const uint8_t* k_ne
                pi_launch_gather(p, l, nullptr, true, true, ys, append ? k_new_all + (size_t)l * kv_bytes : nullptr,
                                 append ? v_new_all + (size_t)l * kv_bytes : nullptr));
     } else {
-      st = pi_recall_impl(p, l, sel_of(l), nsel_of(l), method, tab_of(l), nullptr, ys);
-      if (st != PI_OK) return st;
+      pi_status s2 = pi_recall_impl(p, l, sel_of(l), nsel_of(l), method, tab_of(l), nullptr, ys);
+      if (s2 != PI_OK) return s2;
     }
     PI_CUDA_TRY(cudaEventRecord(p->ev_rec[l], ys));
-    st = select_upto(l + ahead);
-    if (st != PI_OK) return st;
-    PI_CUDA_TRY(cudaStreamWaitEvent(cs, p->ev_rec[l], 0));
-    PI_TIMED(l, PI_K_ATTENTION, cs,
+    return PI_OK;
+  };
+  auto attend_layer = [&](int l, cudaStream_t as) -> pi_status {
+    PI_CUDA_TRY(cudaStreamWaitEvent(as, p->ev_rec[l], 0));
+    PI_TIMED(l, PI_K_ATTENTION, as,
              pi_launch_attention(p, l, q_all + (size_t)l * q_bytes, sel_of(l), tab_of(l), nsel_of(l),
                                  out_all + (size_t)l * q_bytes, lse_all ? lse_all + (size_t)l * p->R * p->Hq : nullptr,
-                                 nullptr, cs));
+                                 nullptr, as));
+    return PI_OK;
+  };
+  pi_status st = PI_OK;
+  if (p->attn_stream_on) {
+    // three streams: compute runs append + select, copy runs the gather, the
+    // pool's own stream runs attention. append(l) of this step waits for
+    // attention(l) of the previous step (which reads the token count, selection
+    // and table this step overwrites); nothing else orders the layers, so
+    // selection runs ahead and consecutive steps overlap.
+    cudaStream_t as = p->attn_stream;
+    PI_CUDA_TRY(cudaStreamWaitEvent(as, p->ev_start, 0));
+    for (int l = 0; l < p->L; l++) {
+      PI_CUDA_TRY(cudaStreamWaitEvent(cs, p->ev_att[l], 0));
+      st = select(l);
+      if (st != PI_OK) return st;
+      st = recall_layer(l);
+      if (st != PI_OK) return st;
+      st = attend_layer(l, as);
+      if (st != PI_OK) return st;
+      PI_CUDA_TRY(cudaEventRecord(p->ev_att[l], as));
+    }
+    // the caller's compute stream completes after every layer's attention
+    PI_CUDA_TRY(cudaStreamWaitEvent(cs, p->ev_att[p->L - 1], 0));
+  } else {
+    // selections run `ahead` layers in front of attention (0: every layer first).
+    // Any depth gives the same results: a layer's plan reads only maps committed by
+    // the previous step's gather of that layer, which the compute stream has
+    // already waited for; deeper lookahead only keeps the copy stream fed.
+    const int ahead = (p->select_ahead <= 0 || p->select_ahead > p->L) ? p->L : p->select_ahead;
+    int next_sel = 0;
+    auto select_upto = [&](int upto) -> pi_status {
+      for (; next_sel <= upto && next_sel < p->L; next_sel++) {
+        pi_status s2 = select(next_sel);
+        if (s2 != PI_OK) return s2;
+      }
+      return PI_OK;
+    };
+    st = select_upto(ahead - 1);
+    if (st != PI_OK) return st;
+    for (int l = 0; l < p->L; l++) {
+      st = recall_layer(l);
+      if (st != PI_OK) return st;
+      st = select_upto(l + ahead);
+      if (st != PI_OK) return st;
+      st = attend_layer(l, cs);
+      if (st != PI_OK) return st;
+    }
   }
   if (p->timing_used < p->timing_steps) p->timing_used++;
   if (stats) {
     std::vector<long long> c((size_t)4 * p->L);
     PI_CUDA_TRY(cudaStreamSynchronize(cs));
     PI_CUDA_TRY(cudaStreamSynchronize(ys));
+    PI_CUDA_TRY(cudaStreamSynchronize(p->attn_stream));
     PI_CUDA_TRY(cudaMemcpy(c.data(), p->recall_counts, sizeof(long long) * 4 * p->L, cudaMemcpyDeviceToHost));
     std::vector<int> ns((size_t)p->L * RU);
     PI_CUDA_TRY(cudaMemcpy(ns.data(), p->step_nsel, sizeof(int) * ns.size(), cudaMemcpyDeviceToHost));
@@ -207,9 +240,11 @@ extern "C" pi_status pi_pool_get_timing(pi_pool* p, pi_kernel_timing* out) {
   return PI_OK;
 }
 
-extern "C" pi_status pi_pool_set_pipeline(pi_pool* p, int select_ahead) {
+extern "C" pi_status pi_pool_set_pipeline(pi_pool* p, int select_ahead, int attention_stream) {
   if (!p || select_ahead < 0) return PI_ERR_INVALID;
+  PI_CUDA_TRY(cudaDeviceSynchronize());  // no step of the old mode may still run
   p->select_ahead = select_ahead;
+  p->attn_stream_on = attention_stream != 0;
   return PI_OK;
 }
 

@@ -172,7 +172,8 @@ def test_small_config_layer_calls(method):
                          [(pi.PI_RECALL_UVA, 1, 1, "default"), (pi.PI_RECALL_MEMCPY, 1, 1, "default"),
                           (pi.PI_RECALL_UVA, 0, 0, "default"), (pi.PI_RECALL_UVA, 1, 0, "default"),
                           (pi.PI_RECALL_UVA, 0, 1, "few"), (pi.PI_RECALL_UVA, 1, 1, "shared"),
-                          (pi.PI_RECALL_UVA, 0, 1, "shared")])
+                          (pi.PI_RECALL_UVA, 0, 1, "shared"), (pi.PI_RECALL_UVA, 0, -1, "default"),
+                          (pi.PI_RECALL_UVA, 1, -1, "default"), (pi.PI_RECALL_MEMCPY, 0, -1, "default")])
 def test_multistep_pipeline_8b_shape(method, evict, ahead, placement):
     """Llama-3-8B-shaped heads (32 q / 8 KV, d 128, blocks of 64), 2 layers, 2
     requests with ragged tails, heavy-hitter blocks, AR(1) queries, 4 pipelined
@@ -182,7 +183,7 @@ def test_multistep_pipeline_8b_shape(method, evict, ahead, placement):
                  pool_slots=14, steps=4, rho=0.9, heavy_frac=0.05, heavy_shift=2.0, seed=3, evict_policy=evict)
     L, R = w.layers, w.batch
     with make_pool(w) as pool:
-        pool.set_pipeline(ahead)
+        pool.set_pipeline(max(ahead, 0), attention_stream=(ahead < 0))  # -1: attention on its own stream (default)
         if placement == "few":
             pool.set_gather(5, 8, True)  # few exclusive CTAs: every CTA loops over many chunks
         elif placement == "shared":
