@@ -300,6 +300,8 @@ def run_ours(args, cfg, rank, world, local_rank):
         pool.set_pipeline(max(args.select_ahead, 0) if args.select_ahead >= 0 else 1, not args.two_streams)
     if args.gather_placement == "shared" or args.gather_ctas or args.gather_depth:
         pool.set_gather(args.gather_ctas, args.gather_depth or 8, args.gather_placement == "exclusive")
+    if args.attn_splits:
+        pool.set_attention(args.attn_splits)
     t0 = time.time()
     for hl in range(host_layers):
         for r in range(R):
@@ -458,6 +460,44 @@ def run_ours(args, cfg, rank, world, local_rank):
                "d2h_bytes_per_step": d2h_b, "api": "pi_decode_step_host (pinned host buffers)"}
     assert pool.device_status() == pi.PI_OK
 
+    # ---- pass D: attention and selection each launched alone, back to back on one
+    # stream over the layers in turn (each launch reads another layer's blocks and
+    # summaries, so nothing is served from L2), on the last step's selection
+    torch.cuda.synchronize()
+    sel_v, nsel_v, tab_v = pool.view_step()
+    q_last, kb_last = q_d[step - 1], kb_d[step - 1]
+    out_i = torch.empty_like(out)
+    lse_i = torch.empty_like(lse)
+    sel_i = torch.empty((R * pool.U, cfg["k"] + cfg["window"]), dtype=torch.int32, device=dev)
+    nsel_i = torch.empty((R * pool.U,), dtype=torch.int32, device=dev)
+    n_iso = max(2 * L, 16)
+
+    def timed(fn):
+        for i in range(L):
+            fn(i)
+        torch.cuda.synchronize()
+        ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ea.record(compute)
+        for i in range(n_iso):
+            fn(i % L)
+        eb.record(compute)
+        torch.cuda.synchronize()
+        return ea.elapsed_time(eb) / 1e3 / n_iso
+
+    t_att = timed(lambda l: pool.sparse_decode(l, q_last[l], sel_v[l], tab_v[l], nsel_v[l], out_i[l], lse_i[l],
+                                               stream=compute))
+    t_sel = timed(lambda l: pool.select_topk(l, q_last[l], kb_last[l], sel_i, nsel_i, stream=compute))
+    assert pool.device_status() == pi.PI_OK
+    att_b = (int(nsel_v.sum().item()) * BB + L * (2 * R * Hq * D * 2 + R * Hq * 4)) / L
+    nb_now = -(-(ntok0 + step) // B)
+    sel_b = R * (max(nb_now - cfg["window"], 0) * Hkv * D * 4 + Hq * D * 2 + (cfg["k"] + cfg["window"] + 1) * 4)
+    roofline["isolated"] = {
+        k_: {"avg_us": 1e6 * t_, "bytes_per_launch": b_, "achieved_gbs": b_ / t_ / 1e9, "bound": "hbm",
+             "peak_gbs": hbm_peak, "frac": b_ / t_ / 1e9 / hbm_peak}
+        for k_, t_, b_ in (("attention", t_att, att_b), ("select", t_sel, sel_b))}
+    roofline["isolated"]["note"] = ("each kernel alone, back to back over the layers on one stream (no L2 reuse), "
+                                    "CUDA events; the select launch here is the standalone one (no fused plan)")
+
     # ---- the other eviction policy on the same pool: flush, warm up, time K steps
     variant = None
     if not args.no_variant and fracs is None:
@@ -504,7 +544,8 @@ def run_ours(args, cfg, rank, world, local_rank):
                    "select_ahead": ("library default" if args.select_ahead < 0 else (args.select_ahead or "all")),
                    "streams": 2 if args.two_streams else 3,
                    "gather_ctas": args.gather_ctas or "default",
-                   "gather_depth": args.gather_depth or 8, "gather_placement": args.gather_placement, "host_alloc": ["cudaHostAlloc", "mmap+THP+register"][args.host_alloc],
+                   "gather_depth": args.gather_depth or 8, "gather_placement": args.gather_placement,
+                   "attn_splits": args.attn_splits or "one wave", "host_alloc": ["cudaHostAlloc", "mmap+THP+register"][args.host_alloc],
                    "parallelism": f"replicas{world}" if world > 1 else "single",
                    "l2": "inputs larger than L2 (host store and pool far exceed 129 MB)"},
         "recall": {"gbs": recall_gbs, "h2d_peak_gbs": h2d_peak,
@@ -674,6 +715,8 @@ def main():
                     help="layers selected ahead of attention in the step (0 = all; -1 = library default)")
     ap.add_argument("--host-alloc", type=int, default=0, choices=[0, 1],
                     help="0 cudaHostAlloc, 1 mmap + transparent huge pages + cudaHostRegister")
+    ap.add_argument("--attn-splits", type=int, default=0,
+                    help="attention CTAs per (request, KV head); 0 = one wave at the kernel's occupancy")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ref-units", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")

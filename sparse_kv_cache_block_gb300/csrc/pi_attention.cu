@@ -56,9 +56,20 @@ struct AttnShape {
   static constexpr int kSub = B * 128;      // one 64-column swizzled sub-tile
   static constexpr int kSelCap = 512;        // selected blocks one CTA may take
   static constexpr int kSmem = kNS * kStage + 1024 + 2 * kNS * 8 + 64 + 2 * kSelCap * 4;
+  static constexpr int kMergeCap = (kNS * kStage) / 8;  // split (m, l) pairs the merge stages in shared memory
 };
 
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// one output element: O = acc / l in bf16; d == 0 also writes lse = (M + log2 l) ln 2
+__device__ __forceinline__ void store_out(const AttnParams& p, int r, int hq, int d, int D, float acc, float lsum,
+                                          float M) {
+  const float v = (lsum > 0.0f) ? acc / lsum : 0.0f;
+  const __nv_bfloat16 bv = __float2bfloat16_rn(v);
+  p.out[((size_t)r * p.Hq + hq) * D + d] = *reinterpret_cast<const uint16_t*>(&bv);
+  if (p.lse && d == 0)
+    p.lse[(size_t)r * p.Hq + hq] = (lsum > 0.0f) ? (M + log2f(lsum)) * 0.69314718055994530942f : -INFINITY;
+}
 
 template <int D, int B>
 __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ CUtensorMap tmap, AttnParams p) {
@@ -82,20 +93,34 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
   const int* selu = p.sel + (size_t)su * p.cap;
   const int* tabu = p.table + (size_t)su * p.cap;
   int n = p.nsel[su];
-  if (n < 0 || n > p.cap) {
-    if (threadIdx.x == 0) pi_flag(p.status, PI_DEV_BAD_INDEX);
-    n = 0;
-  }
   const int split = blockIdx.x;
   const int i0 = split * p.bps;
-  const int nblk = min(S::kSelCap, max(0, min(n, i0 + p.bps) - i0));
-  for (int i = threadIdx.x; i < nblk; i += kThreads) {
+  // the split's table entries are read up to the split's end (a row holds cap
+  // entries) without waiting for the selection count, so that every load of
+  // the prologue is in flight at once
+  const int span = min(S::kSelCap, max(0, min(p.bps, p.cap - i0)));
+  for (int i = threadIdx.x; i < span; i += kThreads) {
     s_blk[i] = selu[i0 + i];
     s_slot[i] = tabu[i0 + i];
   }
   const int nt = p.ntok[(size_t)r * p.L + p.layer];
   const int Pr = p.P[r];
   const long long gbase = p.slot_base[r] + (long long)p.layer * Pr;
+  const int gid = lane >> 2, tig = lane & 3;
+  uint32_t qb[KS][2];  // this group's query rows as the mma's B fragments (consumer warps)
+  if (warp < kConsumerWarps) {
+    const uint16_t* qrow = p.q + ((size_t)r * p.Hq + (size_t)g * p.G + gid) * D;
+#pragma unroll
+    for (int ks = 0; ks < KS; ks++) {
+      qb[ks][0] = (gid < p.G) ? *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * tig) : 0u;
+      qb[ks][1] = (gid < p.G) ? *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 8 + 2 * tig) : 0u;
+    }
+  }
+  if (n < 0 || n > p.cap) {
+    if (threadIdx.x == 0) pi_flag(p.status, PI_DEV_BAD_INDEX);
+    n = 0;
+  }
+  const int nblk = min(span, max(0, n - i0));
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; s++) {
@@ -135,16 +160,6 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
     }
   } else {
     // ------------------------------------------------------------ consumers
-    const int gid = lane >> 2, tig = lane & 3;
-    uint32_t qb[KS][2];
-    {
-      const uint16_t* qrow = p.q + ((size_t)r * p.Hq + (size_t)g * p.G + gid) * D;
-#pragma unroll
-      for (int ks = 0; ks < KS; ks++) {
-        qb[ks][0] = (gid < p.G) ? *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * tig) : 0u;
-        qb[ks][1] = (gid < p.G) ? *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 8 + 2 * tig) : 0u;
-      }
-    }
     float o[KS][4];
 #pragma unroll
     for (int mt = 0; mt < KS; mt++) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.0f;
@@ -256,58 +271,104 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
       if (h1 < p.G) { mlw[(warp * p.G + h1) * 2] = m1; mlw[(warp * p.G + h1) * 2 + 1] = l1; }
     }
     consumer_sync();
-    const int au = r * p.Hkv + g;
-    float* po = p.part_o + ((size_t)au * p.splits_max + split) * p.G * D;
-    float2* pml = p.part_ml + ((size_t)au * p.splits_max + split) * p.G;
-    for (int e = threadIdx.x; e < p.G * D; e += 128) {
-      const int h = e / D, d = e % D;
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < kConsumerWarps; w++) M = fmaxf(M, mlw[(w * p.G + h) * 2]);
-      float acc = 0.0f, lsum = 0.0f;
-      if (M != -INFINITY) {
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; w++) {
-          const float f = pi_exp2(mlw[(w * p.G + h) * 2] - M);
-          acc += f * ow[(w * p.G + h) * D + d];
-          lsum += f * mlw[(w * p.G + h) * 2 + 1];
-        }
-      }
-      po[h * D + d] = acc;
-      if (d == 0) pml[h] = make_float2(M, lsum);
-    }
-    __threadfence();
-    consumer_sync();
-    if (threadIdx.x == 0) {
-      const unsigned done = atomicAdd(p.counter + au, 1u);
-      flags[0] = (done == (unsigned)p.splits - 1) ? 1 : 0;
-    }
-    consumer_sync();
-    if (flags[0]) {
-      if (threadIdx.x == 0) p.counter[au] = 0;
-      __threadfence();
-      const float* pob = p.part_o + (size_t)au * p.splits_max * p.G * D;
-      const float2* pmb = p.part_ml + (size_t)au * p.splits_max * p.G;
+    if (p.splits == 1) {
+      // one CTA holds the whole unit: normalise and write the output here
       for (int e = threadIdx.x; e < p.G * D; e += 128) {
         const int h = e / D, d = e % D;
         float M = -INFINITY;
-        for (int s = 0; s < p.splits; s++) M = fmaxf(M, __ldcg(&pmb[s * p.G + h]).x);
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; w++) M = fmaxf(M, mlw[(w * p.G + h) * 2]);
         float acc = 0.0f, lsum = 0.0f;
         if (M != -INFINITY) {
-          for (int s = 0; s < p.splits; s++) {
-            const float2 ml = __ldcg(&pmb[s * p.G + h]);
-            const float f = pi_exp2(ml.x - M);
-            acc += f * __ldcg(&pob[(s * p.G + h) * D + d]);
-            lsum += f * ml.y;
+#pragma unroll
+          for (int w = 0; w < kConsumerWarps; w++) {
+            const float f = pi_exp2(mlw[(w * p.G + h) * 2] - M);
+            acc += f * ow[(w * p.G + h) * D + d];
+            lsum += f * mlw[(w * p.G + h) * 2 + 1];
           }
         }
-        const int hq = g * p.G + h;
-        const float v = (lsum > 0.0f) ? acc / lsum : 0.0f;
-        const __nv_bfloat16 bv = __float2bfloat16_rn(v);
-        p.out[((size_t)r * p.Hq + hq) * D + d] = *reinterpret_cast<const uint16_t*>(&bv);
-        if (p.lse && d == 0) p.lse[(size_t)r * p.Hq + hq] = (lsum > 0.0f) ? (M + log2f(lsum)) * 0.69314718055994530942f : -INFINITY;
+        store_out(p, r, g * p.G + h, d, D, acc, lsum, M);
       }
-    }
+    } else {
+      const int au = r * p.Hkv + g;
+      float* po = p.part_o + ((size_t)au * p.splits_max + split) * p.G * D;
+      float2* pml = p.part_ml + ((size_t)au * p.splits_max + split) * p.G;
+      for (int e = threadIdx.x; e < p.G * D; e += 128) {
+        const int h = e / D, d = e % D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; w++) M = fmaxf(M, mlw[(w * p.G + h) * 2]);
+        float acc = 0.0f, lsum = 0.0f;
+        if (M != -INFINITY) {
+#pragma unroll
+          for (int w = 0; w < kConsumerWarps; w++) {
+            const float f = pi_exp2(mlw[(w * p.G + h) * 2] - M);
+            acc += f * ow[(w * p.G + h) * D + d];
+            lsum += f * mlw[(w * p.G + h) * 2 + 1];
+          }
+        }
+        po[h * D + d] = acc;
+        if (d == 0) pml[h] = make_float2(M, lsum);
+      }
+      __threadfence();
+      consumer_sync();
+      if (threadIdx.x == 0) {
+        const unsigned done = atomicAdd(p.counter + au, 1u);
+        flags[0] = (done == (unsigned)p.splits - 1) ? 1 : 0;
+      }
+      consumer_sync();
+      if (flags[0]) {
+        if (threadIdx.x == 0) p.counter[au] = 0;
+        __threadfence();
+        const int G = p.G, ns = p.splits;
+        const float* pob = p.part_o + (size_t)au * p.splits_max * G * D;
+        const float2* pmb = p.part_ml + (size_t)au * p.splits_max * G;
+        // every split's (m, l) in one round of loads into the (now idle) stage
+        // memory; more than fits is read from L2 where it is used
+        float2* sml = reinterpret_cast<float2*>(smem);
+        const bool staged = ns * G <= S::kMergeCap;
+        if (staged)
+          for (int t = threadIdx.x; t < ns * G; t += 128) sml[t] = __ldcg(&pmb[t]);
+        consumer_sync();
+        auto ml_at = [&](int i) -> float2 { return staged ? sml[i] : __ldcg(&pmb[i]); };
+        float2* shead = reinterpret_cast<float2*>(s_blk);  // [G] merged (M, l)
+        if (threadIdx.x < G) {
+          const int h = threadIdx.x;
+          float M = -INFINITY;
+          for (int s = 0; s < ns; s++) M = fmaxf(M, ml_at(s * G + h).x);
+          float lsum = 0.0f;
+          if (M != -INFINITY)
+            for (int s = 0; s < ns; s++) {
+              const float2 ml = ml_at(s * G + h);
+              lsum += pi_exp2(ml.x - M) * ml.y;
+            }
+          shead[h] = make_float2(M, lsum);
+        }
+        consumer_sync();
+        const float4* pob4 = reinterpret_cast<const float4*>(pob);
+        for (int e4 = threadIdx.x; e4 < G * D / 4; e4 += 128) {
+          const int h = (4 * e4) / D, d = (4 * e4) % D;
+          const float2 head = shead[h];
+          float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+          if (head.x != -INFINITY) {
+#pragma unroll 4
+            for (int s = 0; s < ns; s++) {
+              const float f = pi_exp2(ml_at(s * G + h).x - head.x);
+              const float4 v = __ldcg(pob4 + (size_t)s * (G * D / 4) + e4);
+              acc.x += f * v.x;
+              acc.y += f * v.y;
+              acc.z += f * v.z;
+              acc.w += f * v.w;
+            }
+          }
+          const int hq = g * G + h;
+          store_out(p, r, hq, d, D, acc.x, head.y, head.x);
+          store_out(p, r, hq, d + 1, D, acc.y, head.y, head.x);
+          store_out(p, r, hq, d + 2, D, acc.z, head.y, head.x);
+          store_out(p, r, hq, d + 3, D, acc.w, head.y, head.x);
+        }
+      }
+    }  // more than one split
   }
   __syncthreads();
 }

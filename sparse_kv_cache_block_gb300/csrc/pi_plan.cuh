@@ -44,6 +44,10 @@ __device__ __forceinline__ int cta_excl_scan(int v, int* warp_sums, int& total) 
   return before + x - v;
 }
 
+// free-slot counts up to this are ordered by counting ranks, larger ones by a
+// bitonic sort
+constexpr int kRankSortMax = 1024;
+
 struct UnitArgs {
   const int* sel;        // this unit's selection [n], ascending
   int n;
@@ -123,31 +127,43 @@ __device__ void plan_unit(const UnitArgs& a, unsigned* bits, int* miss_pos, int*
       }
       nf += tot;
     }
-    int n2 = 1;
-    while (n2 < nf) n2 <<= 1;
-    if (n2 > lru_p2) {
-      if (threadIdx.x == 0) pi_flag(a.status, PI_DEV_BAD_INDEX);
-      n2 = 0;
-      nf = 0;
-    }
-    for (int i = nf + threadIdx.x; i < n2; i += NT) keys[i] = ~0ull;
     __syncthreads();
-    for (int k = 2; k <= n2; k <<= 1)
-      for (int j = k >> 1; j > 0; j >>= 1) {
-        for (int i = threadIdx.x; i < n2; i += NT) {
-          const int ix = i ^ j;
-          if (ix > i) {
-            const unsigned long long x = keys[i], y = keys[ix];
-            const bool up = (i & k) == 0;
-            if ((x > y) == up) {
-              keys[i] = y;
-              keys[ix] = x;
+    if (nf <= kRankSortMax) {
+      // few free slots: each key's rank is the number of smaller keys (keys are
+      // unique: the slot index is in the low word); the nm lowest ranks are taken
+      for (int i = threadIdx.x; i < nf; i += NT) {
+        const unsigned long long x = keys[i];
+        int rank = 0;
+        for (int j = 0; j < nf; j++) rank += (keys[j] < x) ? 1 : 0;
+        if (rank < nm) free_list[rank] = (int)(x & 0xffffffffu);
+      }
+    } else {
+      int n2 = 1;
+      while (n2 < nf) n2 <<= 1;
+      if (n2 > lru_p2) {
+        if (threadIdx.x == 0) pi_flag(a.status, PI_DEV_BAD_INDEX);
+        n2 = 0;
+        nf = 0;
+      }
+      for (int i = nf + threadIdx.x; i < n2; i += NT) keys[i] = ~0ull;
+      __syncthreads();
+      for (int k = 2; k <= n2; k <<= 1)
+        for (int j = k >> 1; j > 0; j >>= 1) {
+          for (int i = threadIdx.x; i < n2; i += NT) {
+            const int ix = i ^ j;
+            if (ix > i) {
+              const unsigned long long x = keys[i], y = keys[ix];
+              const bool up = (i & k) == 0;
+              if ((x > y) == up) {
+                keys[i] = y;
+                keys[ix] = x;
+              }
             }
           }
+          __syncthreads();
         }
-        __syncthreads();
-      }
-    for (int j = threadIdx.x; j < nm && j < nf; j += NT) free_list[j] = (int)(keys[j] & 0xffffffffu);
+      for (int j = threadIdx.x; j < nm && j < nf; j += NT) free_list[j] = (int)(keys[j] & 0xffffffffu);
+    }
     // stamp the slots of the hits now; new entries are stamped at commit
     for (int i = threadIdx.x; i < n; i += NT) {
       const int b = a.sel[i];

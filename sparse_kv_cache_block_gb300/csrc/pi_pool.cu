@@ -360,6 +360,9 @@ extern "C" pi_status pi_clear_device_status(pi_pool* p) {
   if (!p) return PI_ERR_INVALID;
   PI_CUDA_TRY(cudaDeviceSynchronize());
   PI_CUDA_TRY(cudaMemset(p->dev_status, 0, sizeof(unsigned)));
+  // a kernel that gave up on a wait may have left its completion counters behind
+  PI_CUDA_TRY(cudaMemset(p->sel_counter, 0, sizeof(unsigned) * p->L * p->R * p->U));
+  PI_CUDA_TRY(cudaMemset(p->attn_counter, 0, sizeof(unsigned) * p->L * p->R * p->Hkv));
   return PI_OK;
 }
 

@@ -150,7 +150,6 @@ struct SelParams {
   unsigned* counter;   // [R*U] for this layer
   unsigned* status;
   int layer, L, Hq, Hkv, G, D, B, max_blocks, W, k_max, cap, U, bpc;
-  int keys_smem;       // candidate keys cached in shared memory (0: read from global)
   // fused recall plan (decode-step pipeline); table == nullptr disables it
   int* table;
   const int* slot_of;
@@ -173,12 +172,32 @@ __device__ __forceinline__ uint32_t order_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+constexpr int kKeysPerThread = 16;  // candidates a thread keeps in registers (4096 per CTA)
+
+// dst[0..n) = src[0..n): PER loads per thread in flight before the first store
+template <int PER>
+__device__ __forceinline__ void stage_ints(int* dst, const int* src, int n) {
+  for (int base = 0; base < n; base += PER * kSelThreads) {
+    int v[PER];
+#pragma unroll
+    for (int i = 0; i < PER; i++) {
+      const int j = base + threadIdx.x + i * kSelThreads;
+      v[i] = (j < n) ? __ldcg(src + j) : 0;
+    }
+#pragma unroll
+    for (int i = 0; i < PER; i++) {
+      const int j = base + threadIdx.x + i * kSelThreads;
+      if (j < n) dst[j] = v[i];
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kSelThreads) select_kernel(SelParams p) {
   __shared__ __align__(16) float qs[1024];
-  __shared__ int hist[256];
+  __shared__ int hist[512];
   __shared__ int warp_sums[kSelThreads / 32];
   __shared__ int bcast[4];
-  extern __shared__ __align__(16) uint32_t dyn[];  // [keys_smem] + plan scratch
+  extern __shared__ __align__(16) uint32_t dyn[];  // plan scratch, then the slot-map cache
   const int u = blockIdx.y;
   const int r = u / p.U;
   const int g = (p.U == 1) ? 0 : u % p.U;
@@ -267,28 +286,32 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelParams p) {
   kreq = max(0, min(kreq, p.k_max));
   const int kk = min(kreq, ncand);
   int* out = p.sel + (size_t)u * p.cap;
-  uint32_t* keys = dyn;
-  // fused plan: start reading this unit's slot maps now, so their latency hides
-  // behind the radix passes and the plan runs from shared memory
+  // fused plan: read this unit's slot maps now (one round of loads, held in
+  // registers, then stored), so the plan runs from shared memory
   const size_t rlu_m = rl * p.U + g;
   const int P_r = p.P[r];
   int* sob_c = nullptr;
   int* bos_c = nullptr;
   if (p.table && p.map_cache_blocks >= nb && p.map_cache_slots >= P_r) {
-    unsigned char* after = reinterpret_cast<unsigned char*>(dyn + ((p.keys_smem + 3) & ~3)) +
+    unsigned char* after = reinterpret_cast<unsigned char*>(dyn) +
                            pi_plan::plan_smem_bytes(p.max_blocks, p.cap, p.slot_stamp ? p.lru_p2 : 0);
     sob_c = reinterpret_cast<int*>(after);
     bos_c = sob_c + p.map_cache_blocks;
-    const int* sob_g = p.slot_of + rlu_m * p.max_blocks;
-    const int* bos_g = p.block_of + rlu_m * p.p_max;
-    for (int b = threadIdx.x; b < nb; b += kSelThreads) sob_c[b] = sob_g[b];
-    for (int s = threadIdx.x; s < P_r; s += kSelThreads) bos_c[s] = bos_g[s];
+    stage_ints<kKeysPerThread>(sob_c, p.slot_of + rlu_m * p.max_blocks, nb);
+    stage_ints<kKeysPerThread>(bos_c, p.block_of + rlu_m * p.p_max, P_r);
   }
-  const bool cached = ncand <= p.keys_smem;
-  if (cached)
-    for (int b = threadIdx.x; b < ncand; b += kSelThreads) keys[b] = order_key(__ldcg(sc + b));
+  // candidate keys: up to kKeysPerThread per thread in registers, each thread
+  // owning a contiguous run of block ids; more candidates than that are read
+  // from the score buffer where they are used
+  const bool in_regs = ncand <= kKeysPerThread * kSelThreads;
+  const int per = in_regs ? (ncand + kSelThreads - 1) / kSelThreads : 0;
+  const int b_lo = threadIdx.x * per;
+  uint32_t kr[kKeysPerThread];
+#pragma unroll
+  for (int i = 0; i < kKeysPerThread; i++)
+    kr[i] = (i < per && b_lo + i < ncand) ? order_key(__ldcg(sc + b_lo + i)) : 0u;
+  hist[threadIdx.x] = 0;  // kSelThreads == 256 bins, two buffers
   __syncthreads();
-  auto key_at = [&](int b) -> uint32_t { return cached ? keys[b] : order_key(__ldcg(sc + b)); };
 
   uint32_t T = 0;      // key of the kk-th largest candidate
   int need_eq = 0;     // how many candidates equal to T to take (lowest indices)
@@ -296,12 +319,19 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelParams p) {
   if (kk > 0 && !take_all) {
     uint32_t prefix = 0, mask = 0;
     int remaining = kk;
-    for (int shift = 24; shift >= 0; shift -= 8) {
-      hist[threadIdx.x] = 0;  // kSelThreads == 256 bins
-      __syncthreads();
-      for (int b = threadIdx.x; b < ncand; b += kSelThreads) {
-        const uint32_t key = key_at(b);
-        if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255], 1);
+    int pass = 0;
+    for (int shift = 24; shift >= 0; shift -= 8, pass++) {
+      int* h_cur = hist + 256 * (pass & 1);
+      int* h_nxt = hist + 256 * ((pass + 1) & 1);
+      if (in_regs) {
+#pragma unroll
+        for (int i = 0; i < kKeysPerThread; i++)
+          if (i < per && b_lo + i < ncand && (kr[i] & mask) == prefix) atomicAdd(&h_cur[(kr[i] >> shift) & 255], 1);
+      } else {
+        for (int b = threadIdx.x; b < ncand; b += kSelThreads) {
+          const uint32_t key = order_key(__ldcg(sc + b));
+          if ((key & mask) == prefix) atomicAdd(&h_cur[(key >> shift) & 255], 1);
+        }
       }
       __syncthreads();
       if (warp == 0) {
@@ -309,7 +339,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelParams p) {
         int cnt[8], own = 0;
 #pragma unroll
         for (int j = 0; j < 8; j++) {
-          cnt[j] = hist[255 - 8 * lane - j];
+          cnt[j] = h_cur[255 - 8 * lane - j];
           own += cnt[j];
         }
         int incl = own;
@@ -334,20 +364,53 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelParams p) {
           bcast[1] = digit;
           bcast[2] = remaining - before;
         }
+      } else {
+        // the other warps clear the next pass's histogram meanwhile
+        for (int i = threadIdx.x - 32; i < 256; i += kSelThreads - 32) h_nxt[i] = 0;
       }
       __syncthreads();
+      // (bcast is rewritten only after the next pass's first barrier, which every
+      // thread reaches after reading it here)
       prefix |= (uint32_t)bcast[1] << shift;
       mask |= 0xFFu << shift;
       remaining = bcast[2];
-      __syncthreads();
     }
     T = prefix;
     need_eq = remaining;
   }
 
   // stable compaction in block order: all keys > T, then the first need_eq == T
-  int out_n = 0, eq_seen = 0;
-  if (kk > 0) {
+  int out_n = 0;
+  if (kk > 0 && in_regs) {
+    // one scan of (greater, equal) counts per thread, then each thread places
+    // its own run in order
+    int gt_c = 0, eq_c = 0;
+#pragma unroll
+    for (int i = 0; i < kKeysPerThread; i++)
+      if (i < per && b_lo + i < ncand) {
+        gt_c += (take_all || kr[i] > T) ? 1 : 0;
+        eq_c += (!take_all && kr[i] == T) ? 1 : 0;
+      }
+    int tot;
+    const int ex = pi_plan::cta_excl_scan<kSelThreads>((gt_c << 16) | eq_c, warp_sums, tot);
+    int gt_before = ex >> 16, eq_before = ex & 0xffff;
+#pragma unroll
+    for (int i = 0; i < kKeysPerThread; i++)
+      if (i < per && b_lo + i < ncand) {
+        const bool gt = take_all || kr[i] > T;
+        const bool eq = !take_all && kr[i] == T;
+        if (gt) {
+          const int pos = gt_before + min(eq_before, need_eq);
+          if (pos < kk) out[pos] = b_lo + i;
+          gt_before++;
+        } else if (eq) {
+          if (eq_before < need_eq && gt_before + eq_before < kk) out[gt_before + eq_before] = b_lo + i;
+          eq_before++;
+        }
+      }
+    out_n = (tot >> 16) + min(tot & 0xffff, need_eq);
+  } else if (kk > 0) {
+    int eq_seen = 0;
     for (int base = 0; base < ncand; base += kSelThreads) {
       const int b = base + threadIdx.x;
       int gt = 0, eq = 0;
@@ -355,7 +418,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelParams p) {
         if (take_all) {
           gt = 1;
         } else {
-          const uint32_t key = key_at(b);
+          const uint32_t key = order_key(__ldcg(sc + b));
           gt = key > T;
           eq = key == T;
         }
@@ -383,7 +446,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelParams p) {
   // by this CTA; the barrier makes it visible to every thread of the CTA)
   __syncthreads();
   const int words = (p.max_blocks + 31) / 32;
-  unsigned char* plb = reinterpret_cast<unsigned char*>(dyn + (p.keys_smem > 0 ? ((p.keys_smem + 3) & ~3) : 0));
+  unsigned char* plb = reinterpret_cast<unsigned char*>(dyn);
   unsigned long long* lkeys = reinterpret_cast<unsigned long long*>(plb);
   uint32_t* pl = reinterpret_cast<uint32_t*>(plb + sizeof(unsigned long long) * (p.slot_stamp ? p.lru_p2 : 0));
   pi_plan::UnitArgs a;
@@ -488,7 +551,6 @@ cudaError_t pi_launch_select(pi_pool* p, int layer, const void* q, const int* k_
   bpc = ((max(bpc, 8) + 7) / 8) * 8;
   chunks = max(1, (ncand_max + bpc - 1) / bpc);
   sp.bpc = bpc;
-  sp.keys_smem = (ncand_max <= 4096) ? ncand_max : 0;
   sp.table = fused_table;
   sp.slot_of = p->slot_of;
   sp.block_of = p->block_of;
@@ -501,7 +563,7 @@ cudaError_t pi_launch_select(pi_pool* p, int layer, const void* q, const int* k_
   sp.slot_stamp = lru ? p->slot_stamp : nullptr;
   sp.epoch = lru ? p->epoch : nullptr;
   sp.lru_p2 = lru ? p->lru_p2 : 0;
-  size_t smem = sizeof(uint32_t) * (size_t)((sp.keys_smem + 3) & ~3);
+  size_t smem = 0;
   if (fused_table) smem += pi_plan::plan_smem_bytes(p->max_blocks, p->cap, sp.lru_p2);
   // slot maps cached for the fused plan when they are small (cached only up to
   // the largest block count of this layer; nothing beyond it is ever looked up)

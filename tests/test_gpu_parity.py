@@ -417,3 +417,31 @@ def test_query_group_sizes(hq, hkv):
         q = queries(w)[0]
         for l in range(w.layers):
             run_layer(pool, om, w, l, q[l], [w.k, 7], pi.PI_RECALL_UVA)
+
+
+@pytest.mark.parametrize("splits", [0, 1, 3], ids=["one_wave", "one_cta", "three"])
+@pytest.mark.parametrize("D,B", [(64, 16), (64, 32), (64, 64), (64, 128), (128, 16), (128, 32), (128, 64), (128, 128)])
+def test_attention_every_shape_and_split(D, B, splits):
+    """The attention kernel at every head size and block size it is built for,
+    under three split counts; ragged tails, a request shorter than one block, one
+    budget of 0, logits checked."""
+    w = Workload(layers=1, batch=3, hq=16, hkv=4, head_dim=D, block_tokens=B, ntok=[3000, 1777, 70], k=12, window=2,
+                 pool_slots=14, steps=1, seed=41 + D + B)
+    with make_pool(w) as pool:
+        pool.set_attention(splits)
+        prefill(pool, w)
+        om = OracleModel(w)
+        run_layer(pool, om, w, 0, queries(w)[0][0], [w.k, 5, 0], pi.PI_RECALL_UVA)
+
+
+@pytest.mark.parametrize("splits", [0, 1], ids=["one_wave", "one_cta"])
+def test_empty_selection_gives_zero_output(splits):
+    """No recent window and a budget of 0: nothing is selected for that request;
+    its output is zero and its log-sum-exp is -inf, the others are unaffected."""
+    w = Workload(layers=1, batch=3, hq=32, hkv=8, head_dim=128, block_tokens=64, ntok=[2000, 900, 4100], k=6,
+                 window=0, pool_slots=6, steps=1, seed=47)
+    with make_pool(w) as pool:
+        pool.set_attention(splits)
+        prefill(pool, w)
+        om = OracleModel(w)
+        run_layer(pool, om, w, 0, queries(w)[0][0], [6, 0, 3], pi.PI_RECALL_UVA)
