@@ -323,7 +323,23 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelParams p) {
     for (int shift = 24; shift >= 0; shift -= 8, pass++) {
       int* h_cur = hist + 256 * (pass & 1);
       int* h_nxt = hist + 256 * ((pass + 1) & 1);
-      if (in_regs) {
+      if (in_regs && per <= 4) {
+        // few keys per thread: lanes of a warp with the same digit add once (the
+        // leading digits of nearby scores coincide, so plain atomics would queue
+        // on a few bins); with more keys per thread the matching costs more
+        // than the queueing it saves (measured)
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+          if (i >= per) break;
+          const bool take = b_lo + i < ncand && (kr[i] & mask) == prefix;
+          const unsigned act = __ballot_sync(0xffffffffu, take);
+          if (take) {
+            const unsigned digit = (kr[i] >> shift) & 255;
+            const unsigned peers = __match_any_sync(act, digit);
+            if (lane == __ffs(peers) - 1) atomicAdd(&h_cur[digit], __popc(peers));
+          }
+        }
+      } else if (in_regs) {
 #pragma unroll
         for (int i = 0; i < kKeysPerThread; i++)
           if (i < per && b_lo + i < ncand && (kr[i] & mask) == prefix) atomicAdd(&h_cur[(kr[i] >> shift) & 255], 1);
