@@ -255,6 +255,47 @@ def cpu_baseline(cfg, seed, qs, max_blocks, region_source, budget_s=15.0, n_unit
                       f"tokens/s = 1 / (s per unit-step x {L} layers)"}
 
 
+def _oracle_worker(args):
+    """One process of the all-cores oracle leg: its own (request, layer) units,
+    stepped through decode steps until the budget; returns (unit-steps, seconds)."""
+    cfg, seed, units, max_blocks, budget_s, n_steps = args
+    import synth
+    qs = synth.q_ar1(seed, cfg["layers"], cfg["batch"], cfg["hq"], cfg["head_dim"], n_steps, cfg["rho"])
+    samp = OracleSample(cfg, seed, units, max_blocks)
+    done, secs, steps = 0, 0.0, 0
+    while secs < budget_s and steps < n_steps:
+        d, t = samp.step(qs[steps], steps, budget_s - secs)
+        done += d
+        secs += t
+        steps += 1
+    return done, secs
+
+
+def cpu_baseline_all_cores(cfg, seed, max_blocks, budget_s=10.0, units_per_proc=2, procs=None):
+    """The same oracle on every host core: one spawned process per core, each
+    stepping its own (request, layer) units (the units are independent). Returns
+    tokens/s from the summed unit-steps over the slowest process's time."""
+    import multiprocessing as mp
+    procs = procs or os.cpu_count() or 1
+    L, R = cfg["layers"], cfg["batch"]
+    rng = np.random.default_rng(seed + 29)
+    all_units = [(r, l) for r in range(R) for l in range(L)]
+    n = min(len(all_units), procs * units_per_proc)
+    pick = [all_units[i] for i in sorted(rng.choice(len(all_units), size=n, replace=False))]
+    groups = [pick[i::procs] for i in range(procs) if pick[i::procs]]
+    n_steps = 64
+    t0 = time.perf_counter()
+    with mp.get_context("spawn").Pool(len(groups)) as pool_:
+        res = pool_.map(_oracle_worker, [(cfg, seed, g, max_blocks, budget_s, n_steps) for g in groups])
+    wall = time.perf_counter() - t0
+    done = sum(d for d, _ in res)
+    slowest = max(t for _, t in res)
+    return {"value": done / slowest / L, "unit": "tok/s", "cores": len(groups), "kind": "oracle",
+            "sample": f"{len(pick)} (request, layer) units over {len(groups)} spawned processes (one per core), "
+                      f"{done} unit-steps in {slowest:.1f} s of the slowest process ({wall:.1f} s wall including "
+                      f"start-up and input generation); tokens/s = unit-steps / s / {L} layers"}
+
+
 # ------------------------------------------------------------------ main arm
 def run_ours(args, cfg, rank, world, local_rank):
     import torch
@@ -525,11 +566,13 @@ def run_ours(args, cfg, rank, world, local_rank):
 
     # ---- CPU oracle baseline on a bounded sample (rank 0, N = 1)
     cpu = None
+    cpu_all = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        src = lambda l, r: pool.host_kv(l % host_layers, r)
         # the live host store has the appended tokens of the GPU steps; the oracle
         # sample starts from a fresh prefill region of the same seed instead
         cpu = cpu_baseline(cfg, seed, qs, max_blocks, None, budget_s=args.cpu_budget)
+        if args.cpu_all_cores:
+            cpu_all = cpu_baseline_all_cores(cfg, seed, max_blocks, budget_s=min(args.cpu_budget, 10.0))
 
     recall_gbs = kernels.get("gather", {}).get("achieved_gbs")
     line = {
@@ -556,6 +599,7 @@ def run_ours(args, cfg, rank, world, local_rank):
         "roofline": roofline,
         "evict_variant": variant,
         "cpu_baseline": cpu,
+        "cpu_baseline_all_cores": cpu_all,
         "e2e": e2e,
         "gpu_launches": K * L * 5,
         "clocks": clocks.summary(),
@@ -720,6 +764,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ref-units", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-all-cores", type=int, default=1, choices=[0, 1],
+                    help="also time the oracle with one process per host core (reported separately)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (small profiling cases)")
     ap.add_argument("--batch", type=int, default=0, help="override the batch (small profiling cases)")
