@@ -343,6 +343,8 @@ def run_ours(args, cfg, rank, world, local_rank):
         pool.set_gather(args.gather_ctas, args.gather_depth or 8, args.gather_placement == "exclusive")
     if args.attn_splits:
         pool.set_attention(args.attn_splits)
+    if not args.attn_cluster:
+        pool.set_attention_cluster(False)
     t0 = time.time()
     for hl in range(host_layers):
         for r in range(R):
@@ -588,7 +590,8 @@ def run_ours(args, cfg, rank, world, local_rank):
                    "streams": 2 if args.two_streams else 3,
                    "gather_ctas": args.gather_ctas or "default",
                    "gather_depth": args.gather_depth or 8, "gather_placement": args.gather_placement,
-                   "attn_splits": args.attn_splits or "one wave", "host_alloc": ["cudaHostAlloc", "mmap+THP+register"][args.host_alloc],
+                   "attn_splits": args.attn_splits or "one wave",
+                   "attn_merge": "cluster" if args.attn_cluster else "global", "host_alloc": ["cudaHostAlloc", "mmap+THP+register"][args.host_alloc],
                    "parallelism": f"replicas{world}" if world > 1 else "single",
                    "l2": "inputs larger than L2 (host store and pool far exceed 129 MB)"},
         "recall": {"gbs": recall_gbs, "h2d_peak_gbs": h2d_peak,
@@ -761,6 +764,8 @@ def main():
                     help="0 cudaHostAlloc, 1 mmap + transparent huge pages + cudaHostRegister")
     ap.add_argument("--attn-splits", type=int, default=0,
                     help="attention CTAs per (request, KV head); 0 = one wave at the kernel's occupancy")
+    ap.add_argument("--attn-cluster", type=int, default=1, choices=[0, 1],
+                    help="1: a unit's 2..8 attention splits merge through DSMEM in one cluster; 0: global merge")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ref-units", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")

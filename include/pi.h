@@ -310,6 +310,15 @@ pi_status pi_pool_set_pipeline(pi_pool* p, int select_ahead, int attention_strea
  * scratch holds. Results change only by floating-point summation order. */
 pi_status pi_pool_set_attention(pi_pool* p, int splits);
 
+/* How the splits of one (request, KV head) combine. on = 1 (the default): when a
+ * unit has 2..8 splits they are launched as one thread-block cluster and merge
+ * their partial (m, l, O) through distributed shared memory; otherwise (on = 0,
+ * one split, or more than 8) they merge through a global partial buffer
+ * finalised by the unit's last CTA. Results change only by floating-point
+ * summation order (the same order in both merges). PI_ERR_INVALID unless on is
+ * 0 or 1. Library tuning; the pages have no counterpart. */
+pi_status pi_pool_set_attention_cluster(pi_pool* p, int on);
+
 /* pi_decode_step with HOST inputs and outputs (pinned or pageable): copies
  * q_all, k_new_all, v_new_all, k_budget host->device into pool-owned buffers,
  * runs the step and copies out_all (and lse_all if non-NULL) back. Returns after

@@ -190,6 +190,9 @@ class Pool:
     def set_attention(self, splits: int):
         check(self.lib.pi_pool_set_attention(self.h, splits), "pi_pool_set_attention")
 
+    def set_attention_cluster(self, on: bool):
+        check(self.lib.pi_pool_set_attention_cluster(self.h, int(bool(on))), "pi_pool_set_attention_cluster")
+
     def set_evict(self, policy: int):
         check(self.lib.pi_pool_set_evict(self.h, policy), "pi_pool_set_evict")
 

@@ -75,6 +75,7 @@ _SIGS = {
     "pi_pool_set_gather": (c_int, [_P, c_int, c_int, c_int]),
     "pi_pool_set_pipeline": (c_int, [_P, c_int, c_int]),
     "pi_pool_set_attention": (c_int, [_P, c_int]),
+    "pi_pool_set_attention_cluster": (c_int, [_P, c_int]),
     "pi_pool_set_evict": (c_int, [_P, c_int]),
     "pi_sparse_decode": (c_int, [_P, c_int, _P, _P, _P, _P, _P, _P, _P, _P]),
     "pi_sparse_decode_noalloc": (c_int, [_P, c_ll, c_int, c_int, c_int, c_int, c_int, c_int, _P, _P, _P, _P, _P,

@@ -46,6 +46,7 @@ struct AttnParams {
   float* logits;
   unsigned* status;
   int layer, L, Hq, Hkv, G, U, cap, splits, splits_max, bps;
+  int cluster;        // 1: the splits of a unit form one thread-block cluster and merge through DSMEM
   float scale, scale_log2;
 };
 
@@ -57,6 +58,10 @@ struct AttnShape {
   static constexpr int kSelCap = 512;        // selected blocks one CTA may take
   static constexpr int kSmem = kNS * kStage + 1024 + 2 * kNS * 8 + 64 + 2 * kSelCap * 4;
   static constexpr int kMergeCap = (kNS * kStage) / 8;  // split (m, l) pairs the merge stages in shared memory
+  // a CTA's merged partial for the cluster merge ([8][D] fp32 + [8] (m, l)), after
+  // the warps' [4][G][D] + [4][G][2] in the (idle) stage memory
+  static constexpr int kClusterPart = kConsumerWarps * 8 * D * 4 + kConsumerWarps * 8 * 2 * 4;
+  static_assert(kClusterPart + 8 * D * 4 + 8 * 8 <= kNS * kStage, "cluster partial must fit the stage memory");
 };
 
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
@@ -289,6 +294,27 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
         }
         store_out(p, r, g * p.G + h, d, D, acc, lsum, M);
       }
+    } else if (p.cluster) {
+      // this CTA's partial stays in its own shared memory; the cluster merges below
+      float* cpo = reinterpret_cast<float*>(smem + S::kClusterPart);  // [G][D]
+      float2* cpml = reinterpret_cast<float2*>(cpo + p.G * D);        // [G]
+      for (int e = threadIdx.x; e < p.G * D; e += 128) {
+        const int h = e / D, d = e % D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; w++) M = fmaxf(M, mlw[(w * p.G + h) * 2]);
+        float acc = 0.0f, lsum = 0.0f;
+        if (M != -INFINITY) {
+#pragma unroll
+          for (int w = 0; w < kConsumerWarps; w++) {
+            const float f = pi_exp2(mlw[(w * p.G + h) * 2] - M);
+            acc += f * ow[(w * p.G + h) * D + d];
+            lsum += f * mlw[(w * p.G + h) * 2 + 1];
+          }
+        }
+        cpo[h * D + d] = acc;
+        if (d == 0) cpml[h] = make_float2(M, lsum);
+      }
     } else {
       const int au = r * p.Hkv + g;
       float* po = p.part_o + ((size_t)au * p.splits_max + split) * p.G * D;
@@ -371,6 +397,42 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
     }  // more than one split
   }
   __syncthreads();
+  if (p.cluster) {
+    // every CTA of the cluster (the unit's splits, rank = split) merges a slice of
+    // the output from all the partials, read from the peers' shared memory
+    pi_cluster_sync();
+    const int G = p.G, ns = p.splits;
+    const int n4 = G * D / 4;
+    const int per = (n4 + ns - 1) / ns;
+    const uint32_t cpo_local = pi_smem_addr(smem + S::kClusterPart);
+    const uint32_t cpml_local = cpo_local + G * D * 4;
+    const int e_end = min(n4, (split + 1) * per);
+    for (int e4 = split * per + threadIdx.x; e4 < e_end; e4 += kThreads) {
+      const int h = (4 * e4) / D, d = (4 * e4) % D;
+      float M = -INFINITY;
+      for (int c = 0; c < ns; c++) M = fmaxf(M, pi_ld_cluster_f2(pi_cluster_map(cpml_local + h * 8, c)).x);
+      float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      float lsum = 0.0f;
+      if (M != -INFINITY) {
+        for (int c = 0; c < ns; c++) {
+          const float2 ml = pi_ld_cluster_f2(pi_cluster_map(cpml_local + h * 8, c));
+          const float f = pi_exp2(ml.x - M);
+          const float4 v = pi_ld_cluster_f4(pi_cluster_map(cpo_local + e4 * 16, c));
+          acc.x += f * v.x;
+          acc.y += f * v.y;
+          acc.z += f * v.z;
+          acc.w += f * v.w;
+          lsum += f * ml.y;
+        }
+      }
+      const int hq = g * G + h;
+      store_out(p, r, hq, d, D, acc.x, lsum, M);
+      store_out(p, r, hq, d + 1, D, acc.y, lsum, M);
+      store_out(p, r, hq, d + 2, D, acc.z, lsum, M);
+      store_out(p, r, hq, d + 3, D, acc.w, lsum, M);
+    }
+    pi_cluster_sync();  // a CTA's partial must outlive every peer's reads of it
+  }
 }
 
 template <int D, int B>
@@ -383,6 +445,21 @@ cudaError_t launch_attn(pi_pool* p, const AttnParams& ap, cudaStream_t s) {
     configured = true;
   }
   dim3 grid(ap.splits, p->R * p->Hkv);
+  if (ap.cluster) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = S::kSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = ap.splits;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, attn_kernel<D, B>, p->tmap, ap);
+  }
   attn_kernel<D, B><<<grid, kThreads, S::kSmem, s>>>(p->tmap, ap);
   return cudaGetLastError();
 }
@@ -448,6 +525,7 @@ cudaError_t pi_launch_attention(pi_pool* p, int layer, const void* q, const int*
   splits = (p->cap + bps - 1) / bps;
   ap.splits = splits;
   ap.bps = bps;
+  ap.cluster = (p->attn_cluster && splits >= 2 && splits <= 8) ? 1 : 0;
   ap.scale = 1.0f / sqrtf((float)p->D);
   ap.scale_log2 = ap.scale * 1.4426950408889634f;
   if (p->D == 128) {
@@ -637,6 +715,7 @@ extern "C" pi_status pi_sparse_decode_noalloc(const void* kv_slots, long long n_
   ap.splits = splits;
   ap.splits_max = splits;
   ap.bps = bps;
+  ap.cluster = 0;
   ap.scale = 1.0f / sqrtf((float)head_dim);
   ap.scale_log2 = ap.scale * 1.4426950408889634f;
   cudaError_t e = cudaErrorInvalidValue;

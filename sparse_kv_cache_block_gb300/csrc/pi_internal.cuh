@@ -115,6 +115,7 @@ struct pi_pool {
   // gather on a few SMs of its own (1024-thread CTAs holding enough shared memory
   // to keep attention CTAs away)
   bool gather_exclusive = true;
+  bool attn_cluster = true;       // splits 2..8 of a unit merge through DSMEM in a cluster
   int attn_splits = 0;            // attention split count override (0 = one wave at full occupancy)
 
   // fault injection
@@ -206,6 +207,32 @@ __device__ __forceinline__ void pi_tma_load_2d(void* smem_dst, const CUtensorMap
           "r"(pi_smem_addr(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(pi_smem_addr(bar))
       : "memory");
+}
+
+// Thread-block clusters: the same shared-memory offset in CTA `rank` of this
+// cluster, loads through that window, and a full cluster barrier (every thread
+// of every CTA arrives; release/acquire order shared-memory writes before peers'
+// reads).
+__device__ __forceinline__ uint32_t pi_cluster_map(uint32_t smem_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float2 pi_ld_cluster_f2(uint32_t addr) {
+  float2 v;
+  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ float4 pi_ld_cluster_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ void pi_cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void pi_ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {

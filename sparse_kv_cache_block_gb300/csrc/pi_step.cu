@@ -248,6 +248,12 @@ extern "C" pi_status pi_pool_set_pipeline(pi_pool* p, int select_ahead, int atte
   return PI_OK;
 }
 
+extern "C" pi_status pi_pool_set_attention_cluster(pi_pool* p, int on) {
+  if (!p || (on != 0 && on != 1)) return PI_ERR_INVALID;
+  p->attn_cluster = on != 0;
+  return PI_OK;
+}
+
 extern "C" pi_status pi_pool_set_attention(pi_pool* p, int splits) {
   if (!p || splits < 0) return PI_ERR_INVALID;
   p->attn_splits = splits;

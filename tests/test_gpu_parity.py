@@ -419,16 +419,21 @@ def test_query_group_sizes(hq, hkv):
             run_layer(pool, om, w, l, q[l], [w.k, 7], pi.PI_RECALL_UVA)
 
 
-@pytest.mark.parametrize("splits", [0, 1, 3], ids=["one_wave", "one_cta", "three"])
+@pytest.mark.parametrize("splits,cluster", [(0, 1), (1, 1), (3, 1), (3, 0), (8, 1), (14, 1)],
+                         ids=["one_wave_global", "one_cta", "three_cluster", "three_global", "seven_cluster",
+                              "fourteen_global"])
 @pytest.mark.parametrize("D,B", [(64, 16), (64, 32), (64, 64), (64, 128), (128, 16), (128, 32), (128, 64), (128, 128)])
-def test_attention_every_shape_and_split(D, B, splits):
+def test_attention_every_shape_and_split(D, B, splits, cluster):
     """The attention kernel at every head size and block size it is built for,
-    under three split counts; ragged tails, a request shorter than one block, one
-    budget of 0, logits checked."""
+    under split counts that take each merge (one CTA writes directly; 2..8 splits
+    merge in a cluster through DSMEM, or through the global partial buffer; more
+    than 8 always through the buffer); ragged tails, a request shorter than one
+    block, one budget of 0, logits checked."""
     w = Workload(layers=1, batch=3, hq=16, hkv=4, head_dim=D, block_tokens=B, ntok=[3000, 1777, 70], k=12, window=2,
                  pool_slots=14, steps=1, seed=41 + D + B)
     with make_pool(w) as pool:
         pool.set_attention(splits)
+        pool.set_attention_cluster(bool(cluster))
         prefill(pool, w)
         om = OracleModel(w)
         run_layer(pool, om, w, 0, queries(w)[0][0], [w.k, 5, 0], pi.PI_RECALL_UVA)
