@@ -72,6 +72,12 @@ def lib():
         L.or_select_topk.argtypes = [vp, i32, i32, i32, vp]
         L.or_select_shared.restype = i32
         L.or_select_shared.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, vp, vp]
+        L.or_head_score.restype = f32
+        L.or_head_score.argtypes = [vp, vp, i32]
+        L.or_consensus_score.restype = f32
+        L.or_consensus_score.argtypes = [vp, vp, i32, i32, i32, f32]
+        L.or_select_consensus.restype = i32
+        L.or_select_consensus.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, f32, vp, vp]
         L.or_select_headwise.restype = None
         L.or_select_headwise.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp]
         L.or_recall_plan.restype = i32
@@ -158,6 +164,41 @@ def select_shared(q: np.ndarray, kmean: np.ndarray, k: int, W: int, return_score
     sel = np.empty(max(nb, 1), dtype=np.int32)
     sc = np.empty(max(nb, 1), dtype=np.float32)
     n = lib().or_select_shared(_p(q), _p(kmean), nb, hq, hkv, D, k, W, _p(sel), _p(sc))
+    if return_scores:
+        return sel[:n].copy(), sc[: max(nb - W, 0)].copy()
+    return sel[:n].copy()
+
+
+def head_score(qh: np.ndarray, kmg: np.ndarray) -> float:
+    """S(h, b) = q_h . kmean[b, group(h)] in the library's fixed fp32 order
+    (guide, "SoloHead Sparse Selection"). qh [D] bf16 bits, kmg [D] fp32."""
+    qh = _c(qh, np.uint16).ravel()
+    kmg = _c(kmg, np.float32).ravel()
+    assert qh.size == kmg.size and qh.size in (64, 128)
+    return float(np.float32(lib().or_head_score(_p(qh), _p(kmg), qh.size)))
+
+
+def consensus_score(q: np.ndarray, km_b: np.ndarray, lam: float) -> float:
+    """Consensus score of one block (guide, "SoloHead Sparse Selection",
+    "1. Consensus Scoring Mechanism"): per GQA group, the largest per-head score
+    plus lam times their mean; summed over the groups. q [Hq][D] bf16 bits,
+    km_b [Hkv][D] fp32."""
+    q = _c(q, np.uint16)
+    km_b = _c(km_b, np.float32)
+    hkv, D = km_b.shape
+    return float(np.float32(lib().or_consensus_score(_p(q), _p(km_b), q.shape[0], hkv, D, float(lam))))
+
+
+def select_consensus(q: np.ndarray, kmean: np.ndarray, k: int, W: int, lam: float, return_scores: bool = False):
+    """Shared block set of one (request, layer) ranked by consensus scores: the
+    top-k rule of select_shared over consensus_score (same ties, same recent
+    window, ascending output)."""
+    q = _c(q, np.uint16)
+    kmean = _c(kmean, np.float32)
+    nb, hkv, D = kmean.shape
+    sel = np.empty(max(nb, 1), dtype=np.int32)
+    sc = np.empty(max(nb, 1), dtype=np.float32)
+    n = lib().or_select_consensus(_p(q), _p(kmean), nb, q.shape[0], hkv, D, k, W, float(lam), _p(sel), _p(sc))
     if return_scores:
         return sel[:n].copy(), sc[: max(nb - W, 0)].copy()
     return sel[:n].copy()

@@ -19,7 +19,9 @@
  * library fixes it: every KV block keeps the per-KV-head mean of its keys, and
  * score(b) = sum over all query heads h of q_h . kmean[b, group(h)] in fp32,
  * group(h) = h / (Hq/Hkv). Top-k over the non-recent blocks (score descending,
- * lower block index first on ties) plus the W most recent blocks.
+ * lower block index first on ties) plus the W most recent blocks. The guide's
+ * consensus rule (largest per-head score + lambda x mean, per GQA group) is a
+ * second ranking over the same summaries (or_consensus_score).
  *
  * Precision: the score decides integer outputs (selected block ids), so the
  * oracle evaluates it in fp32 in one fixed order (below) that the GPU follows
@@ -187,6 +189,66 @@ void or_select_headwise(const uint16_t* q, const float* kmean_all, int nb, int H
   }
   free(qs);
   free(sc);
+}
+
+/* ------------------------------------------------------------------ consensus score */
+/* [G] "SoloHead Sparse Selection", "1. Consensus Scoring Mechanism": within one
+ * GQA group, a block's consensus score is the largest of the group's per-head
+ * scores plus lambda times their mean (the guide's figure uses lambda = 1, its
+ * formula "typically" 0.5). The per-head score S(h, b) is left undefined there;
+ * this library reads it the same way as the shared score: S(h, b) = q_h .
+ * kmean[b, group(h)], in one fixed fp32 order (D/4 partial sums, partial i takes
+ * d = 4i + j, j = 0..3, by fused multiply-add, then butterfly rounds acc[i] <-
+ * acc[i] + acc[i ^ off] for off = D/8 .. 1). The pages speak of one group; a
+ * request with several KV heads sums the groups' consensus scores (g ascending)
+ * so that one block set serves the whole request, as in the shared selection. */
+float or_head_score(const uint16_t* qh, const float* kmg, int D) {
+  float acc[32], nxt[32];
+  int n = D / 4;
+  for (int i = 0; i < n; i++) {
+    acc[i] = 0.0f;
+    for (int j = 0; j < 4; j++) acc[i] = fmaf(or_bf16(qh[4 * i + j]), kmg[4 * i + j], acc[i]);
+  }
+  for (int off = n / 2; off >= 1; off >>= 1) {
+    for (int i = 0; i < n; i++) nxt[i] = acc[i] + acc[i ^ off];
+    for (int i = 0; i < n; i++) acc[i] = nxt[i];
+  }
+  return acc[0];
+}
+
+/* km_b: one block's summaries [Hkv][D]. Per group: m = the largest per-head
+ * score, s = their sum (heads ascending), c = m + lambda * (s / G), each step
+ * rounded to fp32; the result is the sum of c over the groups (g ascending). */
+float or_consensus_score(const uint16_t* q, const float* km_b, int Hq, int Hkv, int D, float lambda) {
+  int G = Hq / Hkv;
+  float total = 0.0f;
+  for (int g = 0; g < Hkv; g++) {
+    float m = 0.0f, s = 0.0f;
+    for (int j = 0; j < G; j++) {
+      float sh = or_head_score(q + (size_t)(g * G + j) * D, km_b + (size_t)g * D, D);
+      if (j == 0 || sh > m) m = sh;
+      s = s + sh;
+    }
+    float mean = s / (float)G;
+    float t = lambda * mean;
+    float c = m + t;
+    total = total + c;
+  }
+  return total;
+}
+
+/* Consensus selection of one (request, layer): the same top-k rule as the
+ * shared selection over consensus scores. */
+int or_select_consensus(const uint16_t* q, const float* kmean_all, int nb, int Hq, int Hkv, int D, int k, int W,
+                        float lambda, int* sel, float* scores_out) {
+  int E = Hkv * D;
+  float* sc = (float*)malloc(sizeof(float) * (size_t)(nb > 0 ? nb : 1));
+  int ncand = nb - W > 0 ? nb - W : 0;
+  for (int b = 0; b < ncand; b++) sc[b] = or_consensus_score(q, kmean_all + (size_t)b * E, Hq, Hkv, D, lambda);
+  if (scores_out) memcpy(scores_out, sc, sizeof(float) * (size_t)ncand);
+  int n = or_select_topk(sc, nb, k, W, sel);
+  free(sc);
+  return n;
 }
 
 /* ------------------------------------------------------------------ a-3 pool plan */

@@ -450,3 +450,115 @@ def test_attention_headwise_selection_per_head():
         o1, l1, _ = oracle.attention(q, reg, sels[g], ntok, hkv)
         G = hq // hkv
         assert np.array_equal(out[g * G:(g + 1) * G], o1[g * G:(g + 1) * G])
+
+
+# ------------------------------------------------------------------ consensus score
+def _consensus_fixture():
+    heads, top3, top4, lam = {}, {}, None, None
+    with open(os.path.join(GOLD, "solohead_consensus_example.txt")) as f:
+        for line in f:
+            if line.startswith("scores head"):
+                h = int(line.split(":")[0].split()[-1])
+                heads[h] = {int(kv.split("=")[0]): int(kv.split("=")[1]) for kv in line.split(":")[1].split()}
+            elif line.startswith("top3 head"):
+                h = int(line.split(":")[0].split()[-1])
+                top3[h] = [int(x) for x in line.split(":")[1].split()]
+            elif line.startswith("consensus_lambda"):
+                lam = float(line.split(":")[1])
+            elif line.startswith("consensus_top4"):
+                top4 = [int(x) for x in line.split(":")[1].split()]
+    return heads, top3, top4, lam
+
+
+def _one_hot_problem(heads, nb=105, D=128):
+    """q[h][b] = S(h, b) and kmean[b] = e_b (one KV head), so q_h . kmean[b] = S(h, b) exactly."""
+    hq = len(heads)
+    q = np.zeros((hq, D), dtype=np.float64)
+    for h, sc in heads.items():
+        for b, v in sc.items():
+            q[h, b] = v
+    km = np.zeros((nb, 1, D), dtype=np.float32)
+    for b in range(nb):
+        km[b, 0, b] = 1.0
+    return synth.f32_to_bf16(q.astype(np.float32)), km
+
+
+def test_consensus_worked_example_of_the_guide():
+    heads, top3, top4, lam = _consensus_fixture()
+    q, km = _one_hot_problem(heads)
+    nb = km.shape[0]
+    for h, want in top3.items():
+        sc = np.array([oracle.head_score(q[h], km[b, 0]) for b in range(nb)], dtype=np.float32)
+        assert list(oracle.select_topk(sc, nb, 3, 0)) == sorted(want)
+    assert list(oracle.select_consensus(q, km, 4, 0, lam)) == sorted(top4)
+    # the rule needs both terms: the largest head score alone, or the mean alone, picks another set
+    max_only = np.array([max(heads[h].get(b, 0) for h in heads) for b in range(nb)], dtype=np.float32)
+    mean_only = np.array([sum(heads[h].get(b, 0) for h in heads) / 3 for b in range(nb)], dtype=np.float32)
+    assert list(oracle.select_topk(max_only, nb, 4, 0)) != sorted(top4)
+    assert list(oracle.select_topk(mean_only, nb, 4, 0)) != sorted(top4)
+    # the union a head-wise recall would move, against the consensus set
+    assert oracle.union_fragments(list(top3.values())) == 7 and len(top4) == 4
+
+
+@pytest.mark.parametrize("hq,hkv,D", [(8, 8, 128), (16, 8, 128), (32, 8, 128), (64, 8, 128), (8, 2, 64), (12, 3, 64)])
+@pytest.mark.parametrize("lam", [0.0, 0.25, 0.5, 1.0])
+def test_consensus_score_exact_small_integers(hq, hkv, D, lam):
+    """Small integer queries and quarter-integer summaries keep every product and
+    sum exact in fp32 (G a power of two keeps the mean exact), so the oracle must
+    equal the formula evaluated in exact rational arithmetic: per group the largest
+    head score plus lam times their mean, summed over groups."""
+    from fractions import Fraction
+    G = hq // hkv
+    if G & (G - 1):
+        pytest.skip("mean exact only for power-of-two groups")
+    rng = np.random.default_rng(hq * 131 + hkv * 7 + D + int(lam * 4))
+    nb = 40
+    qi = rng.integers(-3, 4, size=(hq, D))
+    ki = rng.integers(-8, 9, size=(nb, hkv, D))
+    q = synth.f32_to_bf16(qi.astype(np.float32))
+    km = (ki / 4.0).astype(np.float32)
+    want = []
+    for b in range(nb):
+        tot = Fraction(0)
+        for g in range(hkv):
+            s_h = [Fraction(int(np.dot(qi[g * G + j], ki[b, g])), 4) for j in range(G)]
+            tot += max(s_h) + Fraction(lam).limit_denominator() * sum(s_h) / G
+        want.append(tot)
+    got = [Fraction(oracle.consensus_score(q, km[b], lam)) for b in range(nb)]
+    assert got == want
+    # the selection is the (score desc, index asc) order of those exact scores
+    order = sorted(range(nb - 2), key=lambda b: (-want[b], b))[:7]
+    assert list(oracle.select_consensus(q, km, 7, 2, lam)) == sorted(order + [nb - 2, nb - 1])
+
+
+def test_consensus_one_head_per_group_is_the_scaled_shared_score():
+    """G = 1: max = mean = the head's score, so consensus = (1 + lam) x shared score;
+    with exact inputs the two selections coincide."""
+    rng = np.random.default_rng(5)
+    hkv, D, nb = 8, 128, 60
+    qi = rng.integers(-3, 4, size=(hkv, D))
+    ki = rng.integers(-8, 9, size=(nb, hkv, D))
+    q = synth.f32_to_bf16(qi.astype(np.float32))
+    km = (ki / 4.0).astype(np.float32)
+    s_shared, sc_shared = oracle.select_shared(q, km, 10, 2, return_scores=True)
+    s_cons, sc_cons = oracle.select_consensus(q, km, 10, 2, 0.5, return_scores=True)
+    assert np.array_equal(sc_cons, (1.5 * sc_shared).astype(np.float32))
+    assert np.array_equal(s_shared, s_cons)
+
+
+def test_consensus_score_close_to_fp64_formula_on_gaussian_inputs():
+    """Realistic values: the fp32 score agrees with the formula in fp64 within a
+    few fp32 rounding steps of the operands' magnitude."""
+    rng = np.random.default_rng(9)
+    hq, hkv, D, nb = 32, 8, 128, 30
+    q = synth.f32_to_bf16(rng.standard_normal((hq, D)).astype(np.float32))
+    km = rng.standard_normal((nb, hkv, D)).astype(np.float32)
+    qf = synth.bf16_to_f32(q).astype(np.float64)
+    G = hq // hkv
+    for b in range(nb):
+        tot = 0.0
+        for g in range(hkv):
+            s_h = qf[g * G:(g + 1) * G] @ km[b, g].astype(np.float64)
+            tot += s_h.max() + 0.5 * s_h.mean()
+        got = oracle.consensus_score(q, km[b], 0.5)
+        assert abs(got - tot) <= 1e-4 * (1.0 + np.abs(qf).sum() * 0.1)
