@@ -336,7 +336,10 @@ def run_ours(args, cfg, rank, world, local_rank):
     pool = pi.Pool(L, R, Hq, Hkv, D, B, max_blocks, cfg["pool_slots"] or cfg["k"] + cfg["window"], cfg["k"],
                    cfg["window"], host_layers=(host_layers if host_layers < L else 0), gather_ctas=args.gather_ctas,
                    pool_slots_per_req=slots_per_req, gather_depth=args.gather_depth, host_alloc=args.host_alloc,
-                   evict_policy=(pi.PI_EVICT_LRU if args.evict == "lru" else pi.PI_EVICT_ASCENDING))
+                   evict_policy=(pi.PI_EVICT_LRU if args.evict == "lru" else pi.PI_EVICT_ASCENDING),
+                   select_mode=(pi.PI_CONSENSUS if args.select == "consensus" else pi.PI_SHARED))
+    if args.select == "consensus":
+        pool.set_consensus_lambda(args.consensus_lambda)
     if args.select_ahead >= 0 or args.two_streams:
         pool.set_pipeline(max(args.select_ahead, 0) if args.select_ahead >= 0 else 1, not args.two_streams)
     if args.gather_placement == "shared" or args.gather_ctas or args.gather_depth:
@@ -602,6 +605,8 @@ def run_ours(args, cfg, rank, world, local_rank):
                    "pool_slots": cfg["pool_slots"] or (f"per request {min(slots_per_req)}..{max(slots_per_req)}"
                                                        if slots_per_req else None),
                    "recall": args.method, "evict": args.evict, "host_layers": host_layers,
+                   "select": (args.select if args.select == "shared"
+                              else f"consensus (lambda {args.consensus_lambda})"),
                    "select_ahead": ("library default" if args.select_ahead < 0 else (args.select_ahead or "all")),
                    "streams": 2 if args.two_streams else 3,
                    "gather_ctas": args.gather_ctas or "default",
@@ -780,6 +785,9 @@ def main():
                     help="0 cudaHostAlloc, 1 mmap + transparent huge pages + cudaHostRegister")
     ap.add_argument("--attn-splits", type=int, default=0,
                     help="attention CTAs per (request, KV head); 0 = one wave at the kernel's occupancy")
+    ap.add_argument("--select", default="shared", choices=["shared", "consensus"],
+                    help="block ranking: mean-key shared score, or the consensus score (max + lambda x mean per group)")
+    ap.add_argument("--consensus-lambda", type=float, default=0.5)
     ap.add_argument("--attn-cluster", type=int, default=1, choices=[0, 1],
                     help="1: a unit's 2..8 attention splits merge through DSMEM in one cluster; 0: global merge")
     ap.add_argument("--cpu-budget", type=float, default=15.0)

@@ -69,7 +69,7 @@ typedef enum {
   PI_ERR_FAULT_INJECTED = 9  /* host-side fault injection fired */
 } pi_status;
 
-enum { PI_SHARED = 0, PI_HEADWISE = 1 };
+enum { PI_SHARED = 0, PI_HEADWISE = 1, PI_CONSENSUS = 2 };
 enum { PI_RECALL_UVA = 0, PI_RECALL_MEMCPY = 1, PI_RECALL_STAGED = 2 };
 enum { PI_EVICT_ASCENDING = 0, PI_EVICT_LRU = 1 };
 
@@ -79,8 +79,10 @@ typedef struct pi_config {
   int pool_slots;            /* P per (request, layer); must be >= k_max + window */
   int k_max;                 /* largest top-k a call may ask for */
   int window;                /* W most recent blocks always selected */
-  int select_mode;           /* PI_SHARED (one block set per request and layer) or
-                                PI_HEADWISE (one per KV head: the comparison arm) */
+  int select_mode;           /* PI_SHARED (one block set per request and layer),
+                                PI_CONSENSUS (the same, ranked by the consensus
+                                score) or PI_HEADWISE (one per KV head: the
+                                comparison arm) */
   int host_layers;           /* 0 = layers. Else the host store holds host_layers
                                 layers and layer l reads host layer l % host_layers
                                 (capacity fallback; appends must then carry the same
@@ -190,8 +192,16 @@ pi_status pi_append_kv(pi_pool* p, int layer, const void* k_new, const void* v_n
  * by (score descending, block index ascending; -0.0 equals +0.0), add the W most
  * recent blocks, write ascending to sel[r][0..nsel[r]). k_per_req: device [R],
  * each clamped to [0, k_max]. Head-wise pools (PI_HEADWISE) select per KV head g
- * with score_g(b) = qsum_g . kmean[b, g] into sel[r][g][..]. `mode` must equal
- * the pool's select_mode. Scores must be finite (NaN inputs are a caller error).
+ * with score_g(b) = qsum_g . kmean[b, g] into sel[r][g][..]. mode = PI_CONSENSUS
+ * ranks by the consensus score instead (PulseInfer Guide, "SoloHead Sparse
+ * Selection", "1. Consensus Scoring Mechanism"): per GQA group g the per-head
+ * scores S(h, b) = q_h . kmean[b, g] (D/4 lanes, lane i accumulates d = 4i + j by
+ * fused multiply-add, then a xor-butterfly D/8 .. 1), c_g = max_h S + lambda x
+ * (sum_h S / G) with each operation rounded to fp32, score(b) = sum of c_g over
+ * g ascending; same candidates, ties and output. Pools of one block set per
+ * request (select_mode PI_SHARED or PI_CONSENSUS) accept PI_SHARED and
+ * PI_CONSENSUS; head-wise pools accept PI_HEADWISE; otherwise PI_ERR_STATE.
+ * Scores must be finite (NaN inputs are a caller error).
  * Source: PulseInfer Guide, "SoloHead Sparse Selection"; the abstract of the
  * PulseInfer paper (SoloHead coalesces head-wise fragmented recalls). */
 pi_status pi_select_topk(pi_pool* p, int layer, const void* q, const int* k_per_req, int mode, int* sel,
@@ -230,6 +240,11 @@ pi_status pi_pool_preload(pi_pool* p, int layer, int req, const int* blocks, int
  * or PI_EVICT_LRU; head-wise pools included). Least-recently-selected is this
  * library's variant: the pages leave eviction open. */
 pi_status pi_pool_set_evict(pi_pool* p, int policy);
+
+/* Weight lambda of the group mean in the consensus score (default 0.5, the
+ * guide's "typical" value; its worked example uses 1). Applies to later
+ * PI_CONSENSUS selections. PI_ERR_INVALID unless 0 <= lambda <= 1e30. */
+pi_status pi_pool_set_consensus_lambda(pi_pool* p, float lambda);
 
 /* Retune the UVA gather: grid size (CTAs; 0 = default), 16-byte loads in flight
  * per thread (2, 4, 8 or 16) and placement: exclusive = 1 (the default) runs

@@ -197,11 +197,14 @@ void or_select_headwise(const uint16_t* q, const float* kmean_all, int nb, int H
  * scores plus lambda times their mean (the guide's figure uses lambda = 1, its
  * formula "typically" 0.5). The per-head score S(h, b) is left undefined there;
  * this library reads it the same way as the shared score: S(h, b) = q_h .
- * kmean[b, group(h)], in one fixed fp32 order (D/4 partial sums, partial i takes
- * d = 4i + j, j = 0..3, by fused multiply-add, then butterfly rounds acc[i] <-
- * acc[i] + acc[i ^ off] for off = D/8 .. 1). The pages speak of one group; a
- * request with several KV heads sums the groups' consensus scores (g ascending)
- * so that one block set serves the whole request, as in the shared selection. */
+ * kmean[b, group(h)], in one fixed fp32 order (below). The pages speak of one
+ * group; a request with several KV heads sums the groups' consensus scores
+ * (g ascending) so that one block set serves the whole request, as in the
+ * shared selection. */
+
+/* One head's score alone: D/4 partial sums, partial i takes d = 4i + j (j =
+ * 0..3) by fused multiply-add, then butterfly rounds acc[i] <- acc[i] +
+ * acc[i ^ off] for off = D/8 .. 1. (The group order below with one head.) */
 float or_head_score(const uint16_t* qh, const float* kmg, int D) {
   float acc[32], nxt[32];
   int n = D / 4;
@@ -216,20 +219,61 @@ float or_head_score(const uint16_t* qh, const float* kmg, int D) {
   return acc[0];
 }
 
-/* km_b: one block's summaries [Hkv][D]. Per group: m = the largest per-head
- * score, s = their sum (heads ascending), c = m + lambda * (s / G), each step
- * rounded to fp32; the result is the sum of c over the groups (g ascending). */
+/* The G scores of one group's heads together, in the fixed order: P = the
+ * smallest power of two >= G (heads G..P-1 are zero rows); n = D/4 partials per
+ * head, partial i of head j = fused multiply-add over d = 4i + t (t = 0..3).
+ * Then for m = P, P/2, .., 2 with off = n*m/(2P): partial i keeps the half of
+ * its m values selected by bit `off` of i (the upper half when set) and adds,
+ * position by position, what partial i^off holds at the same positions; then
+ * butterfly rounds on the one value left for off = n/(2P) .. 1. Head j's score
+ * is then held by partial j*(n/P). out[0..G). */
+void or_group_head_scores(const uint16_t* qg, const float* kmg, int G, int D, float* out) {
+  int n = D / 4, P = 1;
+  while (P < G) P <<= 1;
+  float v[32][8], nv[32][8];
+  for (int i = 0; i < n; i++)
+    for (int j = 0; j < P; j++) {
+      v[i][j] = 0.0f;
+      if (j < G)
+        for (int t = 0; t < 4; t++) v[i][j] = fmaf(or_bf16(qg[(size_t)j * D + 4 * i + t]), kmg[4 * i + t], v[i][j]);
+    }
+  for (int m = P; m >= 2; m >>= 1) {
+    int off = n * m / (2 * P), h = m / 2;
+    for (int i = 0; i < n; i++) {
+      int up = (i & off) != 0;
+      for (int x = 0; x < h; x++) nv[i][x] = v[i][up ? x + h : x] + v[i ^ off][up ? x + h : x];
+    }
+    for (int i = 0; i < n; i++)
+      for (int x = 0; x < h; x++) v[i][x] = nv[i][x];
+  }
+  for (int off = n / (2 * P); off >= 1; off >>= 1) {
+    for (int i = 0; i < n; i++) nv[i][0] = v[i][0] + v[i ^ off][0];
+    for (int i = 0; i < n; i++) v[i][0] = nv[i][0];
+  }
+  for (int j = 0; j < G; j++) out[j] = v[j * (n / P)][0];
+}
+
+/* km_b: one block's summaries [Hkv][D]. Per group: the head scores as above;
+ * m = the largest; s = their sum as a pairwise tree over the P padded heads
+ * (pairs j, j^1; then j, j^2; ...; zero for padded heads); c = m + lambda *
+ * (s / G), each step rounded to fp32; the result is the sum of c over the
+ * groups (g ascending). */
 float or_consensus_score(const uint16_t* q, const float* km_b, int Hq, int Hkv, int D, float lambda) {
-  int G = Hq / Hkv;
+  int G = Hq / Hkv, P = 1;
+  while (P < G) P <<= 1;
   float total = 0.0f;
   for (int g = 0; g < Hkv; g++) {
-    float m = 0.0f, s = 0.0f;
-    for (int j = 0; j < G; j++) {
-      float sh = or_head_score(q + (size_t)(g * G + j) * D, km_b + (size_t)g * D, D);
-      if (j == 0 || sh > m) m = sh;
-      s = s + sh;
+    float hs[8], w[8], nw[8];
+    or_group_head_scores(q + (size_t)g * G * D, km_b + (size_t)g * D, G, D, hs);
+    float m = hs[0];
+    for (int j = 1; j < G; j++)
+      if (hs[j] > m) m = hs[j];
+    for (int j = 0; j < P; j++) w[j] = (j < G) ? hs[j] : 0.0f;
+    for (int o = 1; o < P; o <<= 1) {
+      for (int j = 0; j < P; j++) nw[j] = w[j] + w[j ^ o];
+      for (int j = 0; j < P; j++) w[j] = nw[j];
     }
-    float mean = s / (float)G;
+    float mean = w[0] / (float)G;
     float t = lambda * mean;
     float c = m + t;
     total = total + c;

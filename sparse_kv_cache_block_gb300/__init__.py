@@ -14,11 +14,11 @@ import numpy as np
 from . import _lib
 from ._lib import (PI_EVICT_ASCENDING, PI_EVICT_LRU, PI_ERR_CUDA, PI_ERR_DEVICE, PI_ERR_FAULT_INJECTED, PI_ERR_HOST_ALLOC, PI_ERR_INVALID, PI_ERR_OOM,
                    PI_ERR_POOL_FULL, PI_ERR_STATE, PI_ERR_TIMEOUT, PI_HEADWISE, PI_OK, PI_RECALL_MEMCPY,
-                   PI_RECALL_STAGED, PI_RECALL_UVA, PI_SHARED, PiError, check, declared_functions, load, pi_config,
+                   PI_RECALL_STAGED, PI_RECALL_UVA, PI_SHARED, PI_CONSENSUS, PiError, check, declared_functions, load, pi_config,
                    pi_pool_views, pi_recall_stats, pi_step_stats)
 from .build import build
 
-__all__ = ["Pool", "PiError", "build", "load", "declared_functions", "PI_SHARED", "PI_HEADWISE", "PI_RECALL_UVA",
+__all__ = ["Pool", "PiError", "build", "load", "declared_functions", "PI_SHARED", "PI_HEADWISE", "PI_CONSENSUS", "PI_RECALL_UVA",
            "PI_RECALL_MEMCPY", "PI_RECALL_STAGED"]
 
 
@@ -189,6 +189,9 @@ class Pool:
 
     def set_attention(self, splits: int):
         check(self.lib.pi_pool_set_attention(self.h, splits), "pi_pool_set_attention")
+
+    def set_consensus_lambda(self, lam: float):
+        check(self.lib.pi_pool_set_consensus_lambda(self.h, float(lam)), "pi_pool_set_consensus_lambda")
 
     def set_attention_cluster(self, on: bool):
         check(self.lib.pi_pool_set_attention_cluster(self.h, int(bool(on))), "pi_pool_set_attention_cluster")

@@ -17,7 +17,7 @@ c_int, c_ll, c_double, c_void_p, c_char_p, c_size_t = (
 
 PI_OK, PI_ERR_INVALID, PI_ERR_CUDA, PI_ERR_OOM, PI_ERR_HOST_ALLOC = 0, 1, 2, 3, 4
 PI_ERR_POOL_FULL, PI_ERR_TIMEOUT, PI_ERR_DEVICE, PI_ERR_STATE, PI_ERR_FAULT_INJECTED = 5, 6, 7, 8, 9
-PI_SHARED, PI_HEADWISE = 0, 1
+PI_SHARED, PI_HEADWISE, PI_CONSENSUS = 0, 1, 2
 PI_RECALL_UVA, PI_RECALL_MEMCPY, PI_RECALL_STAGED = 0, 1, 2
 PI_EVICT_ASCENDING, PI_EVICT_LRU = 0, 1
 
@@ -76,6 +76,7 @@ _SIGS = {
     "pi_pool_set_pipeline": (c_int, [_P, c_int, c_int]),
     "pi_pool_set_attention": (c_int, [_P, c_int]),
     "pi_pool_set_attention_cluster": (c_int, [_P, c_int]),
+    "pi_pool_set_consensus_lambda": (c_int, [_P, ctypes.c_float]),
     "pi_pool_set_evict": (c_int, [_P, c_int]),
     "pi_sparse_decode": (c_int, [_P, c_int, _P, _P, _P, _P, _P, _P, _P, _P]),
     "pi_sparse_decode_noalloc": (c_int, [_P, c_ll, c_int, c_int, c_int, c_int, c_int, c_int, _P, _P, _P, _P, _P,

@@ -38,6 +38,7 @@ struct pi_pool {
   pi_config cfg{};
   int L = 0, R = 0, Hq = 0, Hkv = 0, D = 0, B = 0, G = 0;
   int max_blocks = 0, cap = 0, W = 0, k_max = 0, mode = PI_SHARED, U = 1, host_layers = 0;
+  float consensus_lambda = 0.5f;  // PI_CONSENSUS: weight of the group mean
   int p_max = 0;
   size_t block_bytes = 0, frag_bytes = 0, copy_bytes = 0, region_bytes = 0;
   int device = 0, num_sms = 0;
@@ -134,8 +135,10 @@ cudaError_t pi_launch_summaries(pi_pool* p, int layer, const uint8_t* src, bool 
 cudaError_t pi_launch_append(pi_pool* p, int layer, const void* k_new, const void* v_new, cudaStream_t s,
                              bool write_host = true);
 // fused_table != nullptr: the last CTA of each unit also writes the recall plan and the table
+// mode: PI_SHARED / PI_CONSENSUS ranking on pools of one block set per request
+// (U = 1), PI_HEADWISE on head-wise pools; -1 = the pool's own mode
 cudaError_t pi_launch_select(pi_pool* p, int layer, const void* q, const int* k_per_req, int* sel, int* nsel,
-                             cudaStream_t s, int* fused_table = nullptr);
+                             cudaStream_t s, int* fused_table = nullptr, int mode = -1);
 cudaError_t pi_launch_plan(pi_pool* p, int layer, const int* sel, const int* nsel, int* table, cudaStream_t s);
 cudaError_t pi_launch_gather(pi_pool* p, int layer, const uint8_t* stage_src, bool copy, bool commit,
                              cudaStream_t s, const void* k_new = nullptr, const void* v_new = nullptr);
@@ -206,6 +209,16 @@ __device__ __forceinline__ void pi_tma_load_2d(void* smem_dst, const CUtensorMap
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
           "r"(pi_smem_addr(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(pi_smem_addr(bar))
+      : "memory");
+}
+
+// 1D bulk copy global -> this CTA's shared memory (both addresses 16-byte
+// aligned, size a multiple of 16), completing on an mbarrier's transaction count.
+__device__ __forceinline__ void pi_bulk_load(void* smem_dst, const void* src, unsigned bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          pi_smem_addr(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(pi_smem_addr(bar))
       : "memory");
 }
 

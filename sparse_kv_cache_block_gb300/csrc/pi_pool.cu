@@ -87,7 +87,7 @@ static bool valid_config(const pi_config& c) {
   if (c.max_blocks <= 0 || c.max_blocks > 65536) return false;
   if (c.k_max < 0 || c.window < 0 || c.k_max + c.window <= 0) return false;
   if ((long long)c.max_blocks * c.block_tokens > (1LL << 30)) return false;
-  if (c.select_mode != PI_SHARED && c.select_mode != PI_HEADWISE) return false;
+  if (c.select_mode != PI_SHARED && c.select_mode != PI_HEADWISE && c.select_mode != PI_CONSENSUS) return false;
   if (c.host_layers < 0 || c.host_layers > c.layers) return false;
   if (c.hkv * c.head_dim > 1024) return false;  // selection keeps one block's summary per warp pass
   if (c.gather_depth != 0 && c.gather_depth != 2 && c.gather_depth != 4 && c.gather_depth != 8 &&
@@ -385,7 +385,7 @@ extern "C" pi_status pi_pool_flush(pi_pool* p, int layer, pi_stream s) {
 extern "C" pi_status pi_pool_preload(pi_pool* p, int layer, int req, const int* blocks, int n, pi_stream s) {
   if (!p || layer < 0 || layer >= p->L || req < 0 || req >= p->R || n < 0 || (n > 0 && !blocks))
     return PI_ERR_INVALID;
-  if (p->mode != PI_SHARED) return PI_ERR_STATE;
+  if (p->U != 1) return PI_ERR_STATE;
   if (n > p->P_h[req]) return PI_ERR_INVALID;
   for (int i = 0; i < n; i++) {
     if (blocks[i] < 0 || blocks[i] >= p->max_blocks) return PI_ERR_INVALID;
@@ -465,6 +465,12 @@ extern "C" pi_status pi_pool_set_gather(pi_pool* p, int ctas, int depth, int exc
   p->cfg.gather_ctas = ctas;
   p->cfg.gather_depth = depth;
   p->gather_exclusive = exclusive != 0;
+  return PI_OK;
+}
+
+extern "C" pi_status pi_pool_set_consensus_lambda(pi_pool* p, float lambda) {
+  if (!p || !(lambda >= 0.0f) || !(lambda <= 1e30f)) return PI_ERR_INVALID;
+  p->consensus_lambda = lambda;
   return PI_OK;
 }
 

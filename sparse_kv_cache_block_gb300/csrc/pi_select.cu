@@ -164,6 +164,11 @@ struct SelParams {
   int lru_p2;
   int map_cache_blocks;  // fused plan: blocks of slot_of_block cached in shared memory (0: read global)
   int map_cache_slots;   // and slots of block_of_slot
+  int consensus;         // rank blocks by the consensus score (shared selection only)
+  float lambda;          // its weight on the group mean
+  int P2;                // the smallest power of two >= G
+  int ring_stages;       // consensus: bulk-copy stages of 8 blocks' summaries
+  int dyn_plan_off;      // bytes of dynamic shared memory before the plan scratch (consensus: ring + c_g)
 };
 
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -173,6 +178,98 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 }
 
 constexpr int kKeysPerThread = 16;  // candidates a thread keeps in registers (4096 per CTA)
+
+// Consensus ranking ("PulseInfer Guide", "SoloHead Sparse Selection", "1.
+// Consensus Scoring Mechanism"): per GQA group g, c_g = max_h S(h, b) + lambda x
+// (sum_h S(h, b) / G) with S(h, b) = q_h . kmean[b, g]; the block's score is
+// the sum of c_g over g ascending. The CTA streams its candidates' summaries
+// through a ring of bulk-copy stages (8 blocks each); warp w owns one 128-float
+// chunk of [Hkv][D] (one group for D = 128, two for D = 64) and keeps its lanes'
+// query values of that chunk's heads in registers. Per (block, chunk): lane i of
+// a group holds the partial dot of each head over d = 4i .. 4i+3 (fused
+// multiply-add); the group's P = pow2(G) head sums are formed by a reduce-
+// scatter (each round a lane keeps half its values and adds its partner's at
+// the same positions) and butterfly rounds, so head j ends in lane j*(n/P); the
+// max is a butterfly max, the sum a pairwise tree over the padded heads. Every
+// step is rounded exactly as the oracle's fixed order prescribes.
+// Shape of the reduction for one lane, fixed for a warp (n = D/4 lanes per
+// group, P = pow2(G); every offset a power of two).
+struct ConsShape {
+  int off[3];      // reduce-scatter offset of the rounds with 8, 4, 2 values (0: round skipped)
+  int bfly;        // first butterfly offset after the scatter, n / (2P) (0: none)
+  int tree;        // lane distance between neighbouring heads, n / P
+  int n;           // lanes per group
+  int jh;          // the head this lane holds after the scatter
+  int G;
+  float inv_g;     // 1 / G when G is a power of two (exact), else 0: divide
+};
+
+__device__ __forceinline__ ConsShape cons_shape(int lane, int D, int G) {
+  ConsShape c;
+  c.n = D / 4;
+  int P = 1, lgP = 0;
+  while (P < G) {
+    P <<= 1;
+    lgP++;
+  }
+  int lgn = (D == 128) ? 5 : 4;
+#pragma unroll
+  for (int lv = 0; lv < 3; lv++) {
+    const int lgm = 3 - lv;  // rounds with m = 2^lgm values
+    c.off[lv] = (lgm <= lgP) ? (1 << (lgn + lgm - 1 - lgP)) : 0;
+  }
+  c.bfly = (lgn - 1 - lgP >= 0) ? (1 << (lgn - 1 - lgP)) : 0;
+  c.tree = 1 << (lgn - lgP);
+  c.jh = (lane & (c.n - 1)) >> (lgn - lgP);
+  c.G = G;
+  c.inv_g = (P == G) ? 1.0f / (float)G : 0.0f;
+  return c;
+}
+
+__device__ __forceinline__ float consensus_chunk(const float4 k4, const float4 (&qv)[8], bool valid, int lane,
+                                                 const ConsShape& cs, float lambda) {
+  float a[8];
+#pragma unroll
+  for (int j = 0; j < 8; j++) {
+    a[j] = 0.0f;
+    if (j < cs.G && valid) {
+      a[j] = __fmaf_rn(qv[j].x, k4.x, a[j]);
+      a[j] = __fmaf_rn(qv[j].y, k4.y, a[j]);
+      a[j] = __fmaf_rn(qv[j].z, k4.z, a[j]);
+      a[j] = __fmaf_rn(qv[j].w, k4.w, a[j]);
+    }
+  }
+#pragma unroll
+  for (int lv = 0; lv < 3; lv++) {
+    const int h = 4 >> lv;  // values kept this round
+    const int off = cs.off[lv];
+    if (off == 0) continue;
+    const bool up = (lane & off) != 0;
+#pragma unroll
+    for (int x = 0; x < h; x++) {
+      const float send = up ? a[x] : a[x + h];
+      const float keep = up ? a[x + h] : a[x];
+      a[x] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, off));
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < 5; k++) {
+    const int off = cs.bfly >> k;
+    if (off == 0) break;
+    a[0] = __fadd_rn(a[0], __shfl_xor_sync(0xffffffffu, a[0], off));
+  }
+  float mv = (cs.jh < cs.G) ? a[0] : -INFINITY;
+  float sv = (cs.jh < cs.G) ? a[0] : 0.0f;
+#pragma unroll
+  for (int k = 0; k < 3; k++) {
+    const int o = cs.tree << k;
+    if (o >= cs.n) break;
+    mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, o));
+    sv = __fadd_rn(sv, __shfl_xor_sync(0xffffffffu, sv, o));
+  }
+  const float mean = (cs.inv_g != 0.0f) ? __fmul_rn(sv, cs.inv_g) : __fdiv_rn(sv, (float)cs.G);
+  return __fadd_rn(mv, __fmul_rn(lambda, mean));
+}
 
 // dst[0..n) = src[0..n): PER loads per thread in flight before the first store
 template <int PER>
@@ -227,7 +324,79 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelParams p) {
   float* sc = p.scores + (size_t)u * p.max_blocks;
   const int chunks = (E + 127) / 128;
   constexpr int NW = kSelThreads / 32;
-  for (int b = b_begin + warp; b < b_end; b += 2 * NW) {
+  if (p.consensus) {
+    // ring of bulk-copy stages of NW blocks' summaries; then the groups' c_g
+    // per block in shared memory, summed over the groups at the end
+    const int NS = p.ring_stages;
+    const int stage_bytes = NW * E * 4;
+    uint8_t* ring = reinterpret_cast<uint8_t*>(dyn);
+    uint64_t* full = reinterpret_cast<uint64_t*>(ring + (size_t)NS * stage_bytes);
+    float* cg_s = reinterpret_cast<float*>(full + NS);  // [bpc][Hkv]
+    const int nblk = max(0, b_end - b_begin);
+    const int nst = (nblk + NW - 1) / NW;
+    const float* src0 = p.kmean + (rl * p.max_blocks + (size_t)b_begin) * E;
+    auto issue = [&](int it) {
+      const int s = it % NS;
+      const unsigned bytes = (unsigned)(min(NW, nblk - it * NW) * E * 4);
+      pi_mbar_arrive_expect_tx(&full[s], bytes);
+      pi_bulk_load(ring + (size_t)s * stage_bytes, src0 + (size_t)it * NW * E, bytes, &full[s]);
+    };
+    if (threadIdx.x == 0) {
+      for (int s = 0; s < NS; s++) pi_mbar_init(&full[s], 1);
+      pi_fence_barrier_init();
+      for (int it = 0; it < min(NS, nst); it++) issue(it);
+    }
+    // warp w: chunk c = w % chunks, block slot w / chunks of every wpc blocks
+    const int wpc = NW / chunks;
+    const bool active = warp < chunks * wpc;
+    const int c = warp % chunks, slot = warp / chunks;
+    const int e0 = 128 * c + 4 * lane;
+    const bool valid = active && e0 < E;
+    const int gl = valid ? e0 / p.D : 0;
+    const int d0 = e0 % p.D;
+    const int n = p.D / 4;
+    const ConsShape cs = cons_shape(lane, p.D, p.G);
+    float4 qv[8];
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+      qv[j] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      if (valid && j < p.G) {
+        const uint16_t* qh = p.q + ((size_t)r * p.Hq + (size_t)gl * p.G + j) * p.D + d0;
+        const uint32_t lo = *reinterpret_cast<const uint32_t*>(qh);
+        const uint32_t hi = *reinterpret_cast<const uint32_t*>(qh + 2);
+        qv[j] = make_float4(__uint_as_float(lo << 16), __uint_as_float(lo & 0xffff0000u), __uint_as_float(hi << 16),
+                            __uint_as_float(hi & 0xffff0000u));
+      }
+    }
+    __syncthreads();  // the ring's barriers are initialised
+    bool ok = true;
+    for (int it = 0; it < nst; it++) {
+      const int s = it % NS;
+      if (!pi_mbar_wait_bounded(&full[s], (it / NS) & 1, p.status)) ok = false;
+      if (ok && active) {
+        const int nb_it = min(NW, nblk - it * NW);
+        for (int x = slot; x < nb_it; x += wpc) {
+          const float* kb = reinterpret_cast<const float*>(ring + (size_t)s * stage_bytes) + (size_t)x * E;
+          const float4 k4 = valid ? *reinterpret_cast<const float4*>(kb + e0) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+          const float cg = consensus_chunk(k4, qv, valid, lane, cs, p.lambda);
+          if (valid && (lane & (n - 1)) == 0) cg_s[(size_t)(it * NW + x) * p.Hkv + gl] = cg;
+        }
+      }
+      // every warp is done with stage s: refill it (a failed wait stops the ring)
+      ok = __syncthreads_and(ok) != 0;
+      if (!ok) break;
+      if (threadIdx.x == 0 && it + NS < nst) issue(it + NS);
+    }
+    if (!ok && threadIdx.x == 0)
+      for (int it = 0; it < nst; it++) pi_mbar_wait_bounded(&full[it % NS], (it / NS) & 1, p.status);
+    __syncthreads();
+    for (int bl = threadIdx.x; bl < nblk; bl += kSelThreads) {
+      float total = 0.0f;
+      for (int g2 = 0; g2 < p.Hkv; g2++) total = __fadd_rn(total, cg_s[(size_t)bl * p.Hkv + g2]);
+      sc[b_begin + bl] = total;
+    }
+  }
+  for (int b = b_begin + warp; b < b_end && !p.consensus; b += 2 * NW) {
     const int b2 = b + NW;
     const bool two = b2 < b_end;
     const float* km = p.kmean + ((rl * p.max_blocks + b) * p.Hkv) * p.D + goff;
@@ -293,7 +462,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelParams p) {
   int* sob_c = nullptr;
   int* bos_c = nullptr;
   if (p.table && p.map_cache_blocks >= nb && p.map_cache_slots >= P_r) {
-    unsigned char* after = reinterpret_cast<unsigned char*>(dyn) +
+    unsigned char* after = reinterpret_cast<unsigned char*>(dyn) + p.dyn_plan_off +
                            pi_plan::plan_smem_bytes(p.max_blocks, p.cap, p.slot_stamp ? p.lru_p2 : 0);
     sob_c = reinterpret_cast<int*>(after);
     bos_c = sob_c + p.map_cache_blocks;
@@ -462,7 +631,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelParams p) {
   // by this CTA; the barrier makes it visible to every thread of the CTA)
   __syncthreads();
   const int words = (p.max_blocks + 31) / 32;
-  unsigned char* plb = reinterpret_cast<unsigned char*>(dyn);
+  unsigned char* plb = reinterpret_cast<unsigned char*>(dyn) + p.dyn_plan_off;
   unsigned long long* lkeys = reinterpret_cast<unsigned long long*>(plb);
   uint32_t* pl = reinterpret_cast<uint32_t*>(plb + sizeof(unsigned long long) * (p.slot_stamp ? p.lru_p2 : 0));
   pi_plan::UnitArgs a;
@@ -529,7 +698,8 @@ cudaError_t pi_launch_append(pi_pool* p, int layer, const void* k_new, const voi
 }
 
 cudaError_t pi_launch_select(pi_pool* p, int layer, const void* q, const int* k_per_req, int* sel, int* nsel,
-                             cudaStream_t s, int* fused_table) {
+                             cudaStream_t s, int* fused_table, int mode) {
+  if (mode < 0) mode = p->mode;
   SelParams sp;
   sp.q = (const uint16_t*)q;
   sp.k_per_req = k_per_req;
@@ -579,7 +749,20 @@ cudaError_t pi_launch_select(pi_pool* p, int layer, const void* q, const int* k_
   sp.slot_stamp = lru ? p->slot_stamp : nullptr;
   sp.epoch = lru ? p->epoch : nullptr;
   sp.lru_p2 = lru ? p->lru_p2 : 0;
-  size_t smem = 0;
+  sp.consensus = (mode == PI_CONSENSUS) ? 1 : 0;
+  sp.lambda = p->consensus_lambda;
+  sp.P2 = 1;
+  while (sp.P2 < p->G) sp.P2 <<= 1;
+  sp.ring_stages = 0;
+  sp.dyn_plan_off = 0;
+  if (sp.consensus) {
+    // about 64 KiB of summaries in flight per CTA (two CTAs per SM), then the
+    // groups' c_g of the chunk
+    const int stage_bytes = 8 * p->Hkv * p->D * 4;
+    sp.ring_stages = max(2, min(8, 65536 / stage_bytes));
+    sp.dyn_plan_off = sp.ring_stages * stage_bytes + sp.ring_stages * 8 + ((bpc * p->Hkv * 4 + 15) & ~15);
+  }
+  size_t smem = sp.dyn_plan_off;
   if (fused_table) smem += pi_plan::plan_smem_bytes(p->max_blocks, p->cap, sp.lru_p2);
   // slot maps cached for the fused plan when they are small (cached only up to
   // the largest block count of this layer; nothing beyond it is ever looked up)
@@ -632,8 +815,9 @@ extern "C" pi_status pi_append_kv(pi_pool* p, int layer, const void* k_new, cons
 extern "C" pi_status pi_select_topk(pi_pool* p, int layer, const void* q, const int* k_per_req, int mode, int* sel,
                                     int* nsel, pi_stream s) {
   if (!p || layer < 0 || layer >= p->L || !q || !k_per_req || !sel || !nsel) return PI_ERR_INVALID;
-  if (mode != p->mode) return PI_ERR_STATE;
+  // pools of one block set per request rank by either score; head-wise pools only per head
+  if (p->U == 1 ? (mode != PI_SHARED && mode != PI_CONSENSUS) : mode != PI_HEADWISE) return PI_ERR_STATE;
   if (reinterpret_cast<uintptr_t>(q) & 3) return PI_ERR_INVALID;
-  PI_CUDA_TRY(pi_launch_select(p, layer, q, k_per_req, sel, nsel, reinterpret_cast<cudaStream_t>(s), nullptr));
+  PI_CUDA_TRY(pi_launch_select(p, layer, q, k_per_req, sel, nsel, reinterpret_cast<cudaStream_t>(s), nullptr, mode));
   return PI_OK;
 }

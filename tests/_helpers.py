@@ -30,7 +30,8 @@ class Workload:
     heavy_shift: float = 2.0
     seed: int = 0
     host_layers: int = 0
-    select_mode: int = 0       # 0 shared, 1 head-wise
+    select_mode: int = 0       # 0 shared, 1 head-wise, 2 consensus (one set per request)
+    lam: float = 0.5           # consensus: weight of the group mean
     max_blocks: int = 0        # 0: enough for the prefill plus `steps` appended tokens
     slots_per_req: list | None = None
     evict_policy: int = 0      # 0 lowest free slot first, 1 least recently selected first
@@ -149,7 +150,9 @@ class OracleModel:
             nb = self.nb(r, l)
             k = max(0, min(int(kreq[r]), w.k))
             km = self.kmean[(r, l)][:nb]
-            if self.U == 1:
+            if w.select_mode == 2:
+                out.append(oracle.select_consensus(q[r], km, k, w.window, w.lam))
+            elif self.U == 1:
                 out.append(oracle.select_shared(q[r], km, k, w.window))
             else:
                 out.append(oracle.select_headwise(q[r], km, k, w.window))

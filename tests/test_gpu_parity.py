@@ -450,3 +450,112 @@ def test_empty_selection_gives_zero_output(splits):
         prefill(pool, w)
         om = OracleModel(w)
         run_layer(pool, om, w, 0, queries(w)[0][0], [6, 0, 3], pi.PI_RECALL_UVA)
+
+
+@pytest.mark.parametrize("hq,hkv,D,lam", [(8, 2, 64, 0.5), (32, 8, 128, 0.5), (32, 8, 128, 1.0), (64, 8, 128, 0.0),
+                                          (16, 8, 128, 0.5), (8, 8, 128, 0.5), (12, 3, 64, 0.25)],
+                         ids=["C1_shape", "8B", "8B_lam1", "70B_max_only", "G2", "G1", "G4_odd_hkv_d64"])
+def test_consensus_selection_layer_calls(hq, hkv, D, lam):
+    """Consensus-ranked shared selection (guide, "SoloHead Sparse Selection",
+    "1. Consensus Scoring Mechanism"): selected ids bit-exact against the oracle,
+    then recall and attention over them; ragged tails, a short request."""
+    w = Workload(layers=1, batch=3, hq=hq, hkv=hkv, head_dim=D, block_tokens=64 if D == 128 else 16,
+                 ntok=[4000, 2500, 90], k=12, window=2, pool_slots=16, steps=1, seed=51 + hq + D, heavy_frac=0.05,
+                 select_mode=pi.PI_CONSENSUS, lam=lam)
+    with make_pool(w) as pool:
+        pool.set_consensus_lambda(lam)
+        prefill(pool, w)
+        om = OracleModel(w)
+        check_kmean(pool, om, w)
+        run_layer(pool, om, w, 0, queries(w)[0][0], [w.k, 5, 3], pi.PI_RECALL_UVA)
+
+
+def test_consensus_worked_example_on_the_gpu():
+    """The guide's SoloHead example through the library: three query heads of one
+    KV head, block b's keys all equal to the unit vector e_b (so its summary is e_b
+    exactly) and q_h[b] = the fixture's S(h, b); lambda = 1 selects the page's four
+    consensus blocks, lambda = 0 (the largest head score alone) does not."""
+    import test_oracle_pins as pins
+    heads, _, top4, lam = pins._consensus_fixture()
+    nb, D, B = 105, 128, 16
+    w = Workload(layers=1, batch=1, hq=3, hkv=1, head_dim=D, block_tokens=B, ntok=[nb * B], k=4, window=0,
+                 pool_slots=8, steps=1, select_mode=pi.PI_CONSENSUS, lam=lam)
+    q_bits, _ = pins._one_hot_problem(heads, nb=nb, D=D)
+    with make_pool(w) as pool:
+        region = np.zeros((w.max_blocks, 1, 2, B, D), dtype=np.uint16)
+        one = synth.f32_to_bf16(np.ones(1, dtype=np.float32))[0]
+        for b in range(nb):
+            region[b, 0, 0, :, b] = one
+        host = pool.host_kv(0, 0)
+        host[...] = region.reshape(host.shape)
+        pool.update_summaries(0, [nb * B])
+        torch.cuda.synchronize()
+        sel = torch.empty((1, 4), dtype=torch.int32, device="cuda")
+        nsel = torch.empty((1,), dtype=torch.int32, device="cuda")
+        kreq = torch.tensor([4], dtype=torch.int32, device="cuda")
+        for lam_, want_page in ((lam, True), (0.0, False)):
+            pool.set_consensus_lambda(lam_)
+            pool.select_topk(0, dev(q_bits[None]), kreq, sel, nsel)
+            torch.cuda.synchronize()
+            got = sorted(sel[0, : int(nsel[0])].cpu().tolist())
+            assert (got == sorted(top4)) == want_page, (lam_, got)
+            assert got == list(oracle.select_consensus(q_bits, np.eye(nb, D, dtype=np.float32)[:, None, :], 4, 0,
+                                                       lam_))
+
+
+@pytest.mark.parametrize("evict", [0, 1])
+def test_consensus_multistep_pipeline(evict):
+    """A consensus pool through pi_decode_step: 3 pipelined steps with appends,
+    selections, tables, maps, bytes and attention checked against the oracle."""
+    w = Workload(layers=2, batch=2, hq=32, hkv=8, head_dim=128, block_tokens=64, ntok=[4000, 2500], k=8, window=2,
+                 pool_slots=14, steps=3, rho=0.9, heavy_frac=0.05, heavy_shift=2.0, seed=57, evict_policy=evict,
+                 select_mode=pi.PI_CONSENSUS)
+    L, R = w.layers, w.batch
+    with make_pool(w) as pool:
+        prefill(pool, w)
+        om = OracleModel(w)
+        qs = queries(w)
+        for step in range(w.steps):
+            kn, vn = new_tokens(w, step)
+            kbud = np.full((L, R), w.k, dtype=np.int32)
+            out = torch.empty((L, R, w.hq, w.head_dim), dtype=torch.int16, device="cuda")
+            lse = torch.empty((L, R, w.hq), dtype=torch.float32, device="cuda")
+            pool.decode_step(dev(qs[step]), dev(kn), dev(vn), dev(kbud), out, lse)
+            torch.cuda.synchronize()
+            assert pool.device_status() == pi.PI_OK
+            sel_v, nsel_v, tab_v = pool.view_step()
+            for l in range(L):
+                om.append(l, kn[l], vn[l])
+                ref_sel = om.select(l, qs[step][l], kbud[l])
+                check_selection(sel_v[l], nsel_v[l], ref_sel, 1)
+                ref_tab = om.recall(l, ref_sel)
+                check_tables_maps_bytes(pool, om, w, l, ref_sel, ref_tab, tab_v[l])
+                ref_out, ref_lse, _ = om.attention(l, qs[step][l], ref_sel)
+                check_attention(out[l], lse[l], ref_out, ref_lse)
+
+
+def test_selection_modes_accepted_per_pool():
+    """A shared pool ranks by either score per call; a head-wise pool only per
+    head; mismatches return PI_ERR_STATE; lambda must be finite and >= 0."""
+    w = C1
+    with make_pool(w) as pool:
+        prefill(pool, w)
+        q = dev(queries(w)[0][0])
+        kreq = torch.tensor([w.k], dtype=torch.int32, device="cuda")
+        sel = torch.empty((1, w.k + w.window), dtype=torch.int32, device="cuda")
+        nsel = torch.empty((1,), dtype=torch.int32, device="cuda")
+        om = OracleModel(w)
+        for mode in (pi.PI_SHARED, pi.PI_CONSENSUS):
+            pool.select_topk(0, q, kreq, sel, nsel, mode=mode)
+            torch.cuda.synchronize()
+            km = om.kmean[(0, 0)][: om.nb(0, 0)]
+            qn = queries(w)[0][0][0]
+            want = (oracle.select_shared(qn, km, w.k, w.window) if mode == pi.PI_SHARED
+                    else oracle.select_consensus(qn, km, w.k, w.window, 0.5))
+            assert np.array_equal(sel[0, : int(nsel[0])].cpu().numpy(), want)
+        with pytest.raises(pi.PiError) as ei:
+            pool.select_topk(0, q, kreq, sel, nsel, mode=pi.PI_HEADWISE)
+        assert ei.value.status == pi.PI_ERR_STATE
+        for bad in (-1.0, float("nan"), float("inf")):
+            with pytest.raises(pi.PiError):
+                pool.set_consensus_lambda(bad)
