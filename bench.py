@@ -340,6 +340,8 @@ def run_ours(args, cfg, rank, world, local_rank):
                    select_mode=(pi.PI_CONSENSUS if args.select == "consensus" else pi.PI_SHARED))
     if args.select == "consensus":
         pool.set_consensus_lambda(args.consensus_lambda)
+    if args.schedule == "dependent":
+        pool.set_schedule(True, args.groups)
     if args.select_ahead >= 0 or args.two_streams:
         pool.set_pipeline(max(args.select_ahead, 0) if args.select_ahead >= 0 else 1, not args.two_streams)
     if args.gather_placement == "shared" or args.gather_ctas or args.gather_depth:
@@ -609,6 +611,8 @@ def run_ours(args, cfg, rank, world, local_rank):
                               else f"consensus (lambda {args.consensus_lambda})"),
                    "select_ahead": ("library default" if args.select_ahead < 0 else (args.select_ahead or "all")),
                    "streams": 2 if args.two_streams else 3,
+                   "schedule": ("queries known up front, selections run ahead" if args.schedule == "ahead" else
+                                f"dependent queries, {args.groups} interleaved request group(s)"),
                    "gather_ctas": args.gather_ctas or "default",
                    "gather_depth": args.gather_depth or 8, "gather_placement": args.gather_placement,
                    "attn_splits": args.attn_splits or "one wave",
@@ -785,6 +789,9 @@ def main():
                     help="0 cudaHostAlloc, 1 mmap + transparent huge pages + cudaHostRegister")
     ap.add_argument("--attn-splits", type=int, default=0,
                     help="attention CTAs per (request, KV head); 0 = one wave at the kernel's occupancy")
+    ap.add_argument("--schedule", default="ahead", choices=["ahead", "dependent"],
+                    help="dependent: a request's selection of layer l+1 waits for its attention of layer l")
+    ap.add_argument("--groups", type=int, default=2, help="request groups interleaved under --schedule dependent")
     ap.add_argument("--select", default="shared", choices=["shared", "consensus"],
                     help="block ranking: mean-key shared score, or the consensus score (max + lambda x mean per group)")
     ap.add_argument("--consensus-lambda", type=float, default=0.5)

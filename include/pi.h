@@ -320,6 +320,27 @@ pi_status pi_decode_step(pi_pool* p, const void* q_all, const void* k_new_all, c
  * the whole step. Results are identical in every shape. Synchronizes the device. */
 pi_status pi_pool_set_pipeline(pi_pool* p, int select_ahead, int attention_stream);
 
+/* Interruptible layer-wise scheduling (PulseInfer Guide, "Interruptible
+ * Layer-Wise Scheduling"). dependent = 1 models a model whose query of layer
+ * l+1 comes out of its layer l: in pi_decode_step a request's selection of
+ * layer l+1 waits for its attention of layer l (the query is still read from
+ * q_all). The batch splits into `groups` contiguous request groups (request r
+ * in group g when g*R/groups <= r < (g+1)*R/groups); each group's chain (append,
+ * selection + plan, recall, attention, layer after layer) runs on its own
+ * stream (group 0 on the caller's compute stream, the others on streams the
+ * pool owns) and the copy stream takes the groups' recalls in turn, so one
+ * group's recall of layer l streams over the host link while the others
+ * compute. groups = 1 is the rigid order (nothing overlaps the recall).
+ * dependent = 0 (the default): every layer's query is known up front and
+ * selections run ahead (pi_pool_set_pipeline). The dependent schedule takes
+ * UVA recall only (pi_decode_step returns PI_ERR_INVALID for other methods).
+ * Selections, tables, slot maps and recalled bytes are identical under every
+ * schedule; attention outputs may differ in floating-point summation order
+ * (a launch over fewer requests splits the selected blocks over more CTAs).
+ * Synchronizes the device.
+ * PI_ERR_INVALID unless dependent is 0 or 1 and 1 <= groups <= min(8, batch). */
+pi_status pi_pool_set_schedule(pi_pool* p, int dependent, int groups);
+
 /* Split count of the attention kernel (CTAs per request and KV head; 0 = the
  * default: one wave at the kernel's occupancy). Clamped to what the pool's
  * scratch holds. Results change only by floating-point summation order. */

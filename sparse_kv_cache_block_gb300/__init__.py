@@ -190,6 +190,10 @@ class Pool:
     def set_attention(self, splits: int):
         check(self.lib.pi_pool_set_attention(self.h, splits), "pi_pool_set_attention")
 
+    def set_schedule(self, dependent: bool, groups: int = 1):
+        dep = dependent if isinstance(dependent, int) and not isinstance(dependent, bool) else int(bool(dependent))
+        check(self.lib.pi_pool_set_schedule(self.h, dep, groups), "pi_pool_set_schedule")
+
     def set_consensus_lambda(self, lam: float):
         check(self.lib.pi_pool_set_consensus_lambda(self.h, float(lam)), "pi_pool_set_consensus_lambda")
 

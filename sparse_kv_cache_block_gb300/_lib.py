@@ -76,6 +76,7 @@ _SIGS = {
     "pi_pool_set_pipeline": (c_int, [_P, c_int, c_int]),
     "pi_pool_set_attention": (c_int, [_P, c_int]),
     "pi_pool_set_attention_cluster": (c_int, [_P, c_int]),
+    "pi_pool_set_schedule": (c_int, [_P, c_int, c_int]),
     "pi_pool_set_consensus_lambda": (c_int, [_P, ctypes.c_float]),
     "pi_pool_set_evict": (c_int, [_P, c_int]),
     "pi_sparse_decode": (c_int, [_P, c_int, _P, _P, _P, _P, _P, _P, _P, _P]),

@@ -47,6 +47,7 @@ struct AttnParams {
   unsigned* status;
   int layer, L, Hq, Hkv, G, U, cap, splits, splits_max, bps;
   int cluster;        // 1: the splits of a unit form one thread-block cluster and merge through DSMEM
+  int u0, nunits;     // the launch covers units u0 .. u0+nunits-1 (grid.y)
   float scale, scale_log2;
 };
 
@@ -92,7 +93,7 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
   int* s_slot = s_blk + S::kSelCap;   // and their pool slots
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int u = blockIdx.y;
+  const int u = p.u0 + blockIdx.y;
   const int r = u / p.Hkv, g = u % p.Hkv;
   const int su = (p.U == 1) ? r : u;
   const int* selu = p.sel + (size_t)su * p.cap;
@@ -444,7 +445,7 @@ cudaError_t launch_attn(pi_pool* p, const AttnParams& ap, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  dim3 grid(ap.splits, p->R * p->Hkv);
+  dim3 grid(ap.splits, ap.nunits);
   if (ap.cluster) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
@@ -488,8 +489,13 @@ int attn_smem_bytes(int D, int B) {
 int pi_attention_smem(int D, int B) { return attn_smem_bytes(D, B); }
 
 cudaError_t pi_launch_attention(pi_pool* p, int layer, const void* q, const int* sel, const int* table,
-                                const int* nsel, void* out, float* lse, float* logits, cudaStream_t s) {
+                                const int* nsel, void* out, float* lse, float* logits, cudaStream_t s, int r0,
+                                int nr) {
+  if (nr < 0) nr = p->R;
+  if (nr == 0) return cudaSuccess;
   AttnParams ap;
+  ap.u0 = r0 * p->Hkv;
+  ap.nunits = nr * p->Hkv;
   ap.q = (const uint16_t*)q;
   ap.sel = sel;
   ap.table = table;
@@ -517,7 +523,7 @@ cudaError_t pi_launch_attention(pi_pool* p, int layer, const void* q, const int*
   // occupancy, with at most 512 selected blocks per CTA
   const int smem = attn_smem_bytes(p->D, p->B);
   const int per_sm = max(1, (228 * 1024) / (smem + 1024));
-  int splits = (int)(((long long)per_sm * p->num_sms) / (long long)units);
+  int splits = (int)(((long long)per_sm * p->num_sms) / (long long)ap.nunits);
   if (p->attn_splits > 0) splits = p->attn_splits;
   splits = max(splits, (p->cap + 511) / 512);
   splits = max(1, min(splits, p->attn_max_splits));
@@ -715,6 +721,8 @@ extern "C" pi_status pi_sparse_decode_noalloc(const void* kv_slots, long long n_
   ap.splits = splits;
   ap.splits_max = splits;
   ap.bps = bps;
+  ap.u0 = 0;
+  ap.nunits = (int)units;
   ap.cluster = 0;
   ap.scale = 1.0f / sqrtf((float)head_dim);
   ap.scale_log2 = ap.scale * 1.4426950408889634f;

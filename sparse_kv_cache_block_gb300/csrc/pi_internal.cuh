@@ -105,6 +105,7 @@ struct pi_pool {
   // per-kernel timing inside pi_decode_step: events [step][layer][kind][2]
   std::vector<cudaEvent_t> tev;
   int timing_steps = 0, timing_used = 0;
+  int timing_groups = 1;  // event slots per layer (request groups of the dependent schedule)
 
   // decode-step pipeline: layers selected ahead of attention (0 = all)
   int select_ahead = 1;
@@ -113,6 +114,14 @@ struct pi_pool {
   bool attn_stream_on = true;
   cudaStream_t attn_stream = nullptr;
   std::vector<cudaEvent_t> ev_att;
+  // interruptible layer-wise scheduling: with dependent queries a request
+  // group's selection of layer l+1 follows its attention of layer l; groups
+  // interleave on the copy stream (group 0 on the caller's compute stream)
+  int sched_dependent = 0;
+  int sched_groups = 1;
+  cudaStream_t grp_stream[8] = {};
+  std::vector<cudaEvent_t> grp_ev;  // [L][8][2]: selected, recalled
+  cudaEvent_t grp_done[8] = {};
   // gather on a few SMs of its own (1024-thread CTAs holding enough shared memory
   // to keep attention CTAs away)
   bool gather_exclusive = true;
@@ -132,18 +141,21 @@ static inline long long pi_global_slot(const pi_pool* p, int r, int l, int s) {
 // kernel launchers (return cudaGetLastError of the launch)
 cudaError_t pi_launch_summaries(pi_pool* p, int layer, const uint8_t* src, bool src_is_host, int b0, int b1,
                                 cudaStream_t s, const int* ntok_new);
+// r0, nr: the launch covers requests r0 .. r0+nr-1 (nr < 0: every request)
 cudaError_t pi_launch_append(pi_pool* p, int layer, const void* k_new, const void* v_new, cudaStream_t s,
-                             bool write_host = true);
+                             bool write_host = true, int r0 = 0, int nr = -1);
 // fused_table != nullptr: the last CTA of each unit also writes the recall plan and the table
 // mode: PI_SHARED / PI_CONSENSUS ranking on pools of one block set per request
 // (U = 1), PI_HEADWISE on head-wise pools; -1 = the pool's own mode
 cudaError_t pi_launch_select(pi_pool* p, int layer, const void* q, const int* k_per_req, int* sel, int* nsel,
-                             cudaStream_t s, int* fused_table = nullptr, int mode = -1);
+                             cudaStream_t s, int* fused_table = nullptr, int mode = -1, int r0 = 0, int nr = -1);
 cudaError_t pi_launch_plan(pi_pool* p, int layer, const int* sel, const int* nsel, int* table, cudaStream_t s);
 cudaError_t pi_launch_gather(pi_pool* p, int layer, const uint8_t* stage_src, bool copy, bool commit,
-                             cudaStream_t s, const void* k_new = nullptr, const void* v_new = nullptr);
+                             cudaStream_t s, const void* k_new = nullptr, const void* v_new = nullptr, int r0 = 0,
+                             int nr = -1);
 cudaError_t pi_launch_attention(pi_pool* p, int layer, const void* q, const int* sel, const int* table,
-                                const int* nsel, void* out, float* lse, float* logits, cudaStream_t s);
+                                const int* nsel, void* out, float* lse, float* logits, cudaStream_t s, int r0 = 0,
+                                int nr = -1);
 bool pi_make_tmap(pi_pool* p);
 int pi_attention_smem(int D, int B);  // dynamic shared memory of one attention CTA
 

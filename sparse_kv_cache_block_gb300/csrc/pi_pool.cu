@@ -46,6 +46,12 @@ static void pool_free(pi_pool* p) {
   if (p->ev_start) cudaEventDestroy(p->ev_start);
   for (auto e : p->ev_att) cudaEventDestroy(e);
   if (p->attn_stream) cudaStreamDestroy(p->attn_stream);
+  for (auto st : p->grp_stream)
+    if (st) cudaStreamDestroy(st);
+  for (auto e : p->grp_ev)
+    if (e) cudaEventDestroy(e);
+  for (auto e : p->grp_done)
+    if (e) cudaEventDestroy(e);
   for (auto e : p->tev) cudaEventDestroy(e);
   void* dev_ptrs[] = {p->pool,       p->slot_base,  p->P,          p->kmean,       p->tail_sum,    p->ntok,
                       p->slot_of,    p->block_of,   p->dev_status, p->sel_scores,  p->sel_counter, p->plan_n,

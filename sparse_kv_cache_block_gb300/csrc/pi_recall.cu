@@ -92,6 +92,7 @@ struct GatherParams {
   long long region_bytes;
   long long e_begin, e_end;  // entry range to process (global plan order)
   int layer, L, R, U, Hkv, B, D, max_blocks, p_max, cap, units, copy_bytes, block_bytes, do_copy, do_commit;
+  int r0, nr;                // requests of this launch: r0 .. r0+nr-1 (units r0*U ..; plan pointers offset)
 };
 
 __device__ __forceinline__ uint4 ld_stream(const uint4* ptr) {
@@ -118,8 +119,8 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(GatherParams g) 
   // write-through of the new tokens (host store), one request per pass
   if (g.k_new && blockIdx.x == 0) {
     const int per_req = g.Hkv * 2 * row_words;  // 16-byte words of K and V rows
-    for (int w = threadIdx.x; w < g.R * per_req; w += kGatherThreads) {
-      const int r = w / per_req, rem = w % per_req;
+    for (int w = threadIdx.x; w < g.nr * per_req; w += kGatherThreads) {
+      const int r = g.r0 + w / per_req, rem = w % per_req;
       const int g_ = rem / (2 * row_words), kv = (rem / row_words) & 1, x = rem % row_words;
       const int t = g.ntok[(size_t)r * g.L + g.layer] - 1;
       if (t < 0 || t / g.B >= g.max_blocks) continue;
@@ -172,7 +173,7 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(GatherParams g) 
     const int u = lo;
     const int j = (int)(e - prefix[u]);
     const int4 pe = g.plan[(size_t)u * g.cap + j];
-    const int r = u / g.U, gu = u % g.U;
+    const int r = g.r0 + u / g.U, gu = u % g.U;
     const int Pr = g.P[r];
     const bool ok = pe.x >= 0 && pe.x < g.max_blocks && pe.y >= 0 && pe.y < Pr && pe.z < g.max_blocks;
     if (!ok) {
@@ -295,6 +296,8 @@ static GatherParams gather_params(pi_pool* p, int layer) {
   g.p_max = p->p_max;
   g.cap = p->cap;
   g.units = (int)RU;
+  g.r0 = 0;
+  g.nr = p->R;
   g.copy_bytes = (int)p->copy_bytes;
   g.block_bytes = (int)p->block_bytes;
   g.do_copy = 1;
@@ -348,8 +351,16 @@ static cudaError_t launch_gather(pi_pool* p, const GatherParams& g, cudaStream_t
 }
 
 cudaError_t pi_launch_gather(pi_pool* p, int layer, const uint8_t* stage_src, bool copy, bool commit,
-                             cudaStream_t s, const void* k_new, const void* v_new) {
+                             cudaStream_t s, const void* k_new, const void* v_new, int r0, int nr) {
   GatherParams g = gather_params(p, layer);
+  if (nr >= 0) {
+    // requests r0 .. r0+nr-1 only: their units' plans (the staged arm always takes every request)
+    g.plan_n += (size_t)r0 * p->U;
+    g.plan += (size_t)r0 * p->U * p->cap;
+    g.r0 = r0;
+    g.nr = nr;
+    g.units = nr * p->U;
+  }
   g.stage_src = stage_src;
   g.k_new = (const uint8_t*)k_new;
   g.v_new = (const uint8_t*)v_new;

@@ -77,12 +77,13 @@ struct AppendParams {
   float* tail_sum;
   unsigned* status;
   int layer, L, R, Hkv, B, D, U, max_blocks, host_layer;
+  int r0;                 // first request of this launch (one CTA per request)
   int write_host;         // 0: the decode-step gather writes the host copy instead
 };
 
 // grid R; one thread per 8 consecutive elements of one head
 __global__ void append_kernel(AppendParams a) {
-  const int r = blockIdx.x;
+  const int r = a.r0 + blockIdx.x;
   const size_t rl = (size_t)r * a.L + a.layer;
   const int t = a.ntok[rl];
   const int b = t / a.B, tp = t % a.B;
@@ -164,6 +165,7 @@ struct SelParams {
   int lru_p2;
   int map_cache_blocks;  // fused plan: blocks of slot_of_block cached in shared memory (0: read global)
   int map_cache_slots;   // and slots of block_of_slot
+  int u0;                // first unit of this launch (grid.y covers u0 ..)
   int consensus;         // rank blocks by the consensus score (shared selection only)
   float lambda;          // its weight on the group mean
   int P2;                // the smallest power of two >= G
@@ -295,7 +297,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelParams p) {
   __shared__ int warp_sums[kSelThreads / 32];
   __shared__ int bcast[4];
   extern __shared__ __align__(16) uint32_t dyn[];  // plan scratch, then the slot-map cache
-  const int u = blockIdx.y;
+  const int u = p.u0 + blockIdx.y;
   const int r = u / p.U;
   const int g = (p.U == 1) ? 0 : u % p.U;
   const int E = (p.U == 1) ? p.Hkv * p.D : p.D;
@@ -669,7 +671,7 @@ cudaError_t pi_launch_summaries(pi_pool* p, int layer, const uint8_t* src, bool 
 }
 
 cudaError_t pi_launch_append(pi_pool* p, int layer, const void* k_new, const void* v_new, cudaStream_t s,
-                             bool write_host) {
+                             bool write_host, int r0, int nr) {
   AppendParams a;
   a.write_host = write_host ? 1 : 0;
   a.k_new = (const uint8_t*)k_new;
@@ -693,13 +695,18 @@ cudaError_t pi_launch_append(pi_pool* p, int layer, const void* k_new, const voi
   a.max_blocks = p->max_blocks;
   a.host_layer = layer % p->host_layers;
   int threads = (p->Hkv * p->D) / 8;
-  append_kernel<<<p->R, threads, 0, s>>>(a);
+  if (nr < 0) nr = p->R;
+  a.r0 = r0;
+  if (nr == 0) return cudaSuccess;
+  append_kernel<<<nr, threads, 0, s>>>(a);
   return cudaGetLastError();
 }
 
 cudaError_t pi_launch_select(pi_pool* p, int layer, const void* q, const int* k_per_req, int* sel, int* nsel,
-                             cudaStream_t s, int* fused_table, int mode) {
+                             cudaStream_t s, int* fused_table, int mode, int r0, int nr) {
   if (mode < 0) mode = p->mode;
+  if (nr < 0) nr = p->R;
+  if (nr == 0) return cudaSuccess;
   SelParams sp;
   sp.q = (const uint16_t*)q;
   sp.k_per_req = k_per_req;
@@ -777,7 +784,8 @@ cudaError_t pi_launch_select(pi_pool* p, int layer, const void* q, const int* k_
     cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  dim3 grid(chunks, (unsigned)RU);
+  sp.u0 = r0 * p->U;
+  dim3 grid(chunks, (unsigned)(nr * p->U));
   select_kernel<<<grid, kSelThreads, smem, s>>>(sp);
   return cudaGetLastError();
 }

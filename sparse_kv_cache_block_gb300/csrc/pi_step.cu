@@ -17,15 +17,16 @@
 pi_status pi_recall_impl(pi_pool* p, int layer, const int* sel, const int* nsel, int method, int* table,
                          pi_recall_stats* stats, cudaStream_t st);
 
-// event pair of (layer, kind) for the step being recorded, or nullptr
-static cudaEvent_t* tev_of(pi_pool* p, int l, int kind) {
-  if (p->timing_used >= p->timing_steps) return nullptr;
-  return &p->tev[(((size_t)p->timing_used * p->L + l) * PI_K_KINDS + kind) * 2];
+// event pair of (layer, request group, kind) for the step being recorded, or nullptr
+static cudaEvent_t* tev_of(pi_pool* p, int l, int kind, int grp = 0) {
+  if (p->timing_used >= p->timing_steps || grp >= p->timing_groups) return nullptr;
+  return &p->tev[((((size_t)p->timing_used * p->L + l) * p->timing_groups + grp) * PI_K_KINDS + kind) * 2];
 }
 
-#define PI_TIMED(l, kind, stream, launch_expr)                     \
+#define PI_TIMED(l, kind, stream, launch_expr) PI_TIMED_G(l, 0, kind, stream, launch_expr)
+#define PI_TIMED_G(l, grp, kind, stream, launch_expr)              \
   do {                                                             \
-    cudaEvent_t* _ev = tev_of(p, (l), (kind));                     \
+    cudaEvent_t* _ev = tev_of(p, (l), (kind), (grp));              \
     if (_ev) PI_CUDA_TRY(cudaEventRecord(_ev[0], (stream)));       \
     PI_CUDA_TRY(launch_expr);                                      \
     if (_ev) PI_CUDA_TRY(cudaEventRecord(_ev[1], (stream)));       \
@@ -96,7 +97,57 @@ static pi_status step_impl(pi_pool* p, const uint8_t* q_all, const uint8_t* k_ne
     return PI_OK;
   };
   pi_status st = PI_OK;
-  if (p->attn_stream_on) {
+  if (p->sched_dependent) {
+    // Interruptible layer-wise scheduling ("PulseInfer Guide", section
+    // "Interruptible Layer-Wise Scheduling"): a request's query of layer l+1
+    // comes out of its layer l, so each request group's chain runs append,
+    // selection (+ plan), recall, attention layer after layer on its own
+    // stream; the copy stream takes the groups' recalls in turn, so one group's
+    // recall of layer l streams while the others compute.
+    if (!uva) return PI_ERR_INVALID;
+    const int M = p->sched_groups;
+    cudaStream_t gs[8];
+    int r0[8], nr[8];
+    for (int g = 0; g < M; g++) {
+      r0[g] = (int)((long long)g * p->R / M);
+      nr[g] = (int)((long long)(g + 1) * p->R / M) - r0[g];
+      gs[g] = (g == 0) ? cs : p->grp_stream[g];
+      if (g > 0) PI_CUDA_TRY(cudaStreamWaitEvent(gs[g], p->ev_start, 0));
+    }
+    for (int l = 0; l < p->L; l++)
+      for (int g = 0; g < M; g++) {
+        cudaStream_t s = gs[g];
+        cudaEvent_t* ev = &p->grp_ev[((size_t)l * 8 + g) * 2];
+        if (append) {
+          PI_TIMED_G(l, g, PI_K_APPEND, s,
+                     pi_launch_append(p, l, k_new_all + (size_t)l * kv_bytes, v_new_all + (size_t)l * kv_bytes, s,
+                                      false, r0[g], nr[g]));
+          for (int r = r0[g]; r < r0[g] + nr[g]; r++) p->ntok_h[(size_t)r * p->L + l] += 1;
+        }
+        PI_TIMED_G(l, g, PI_K_SELECT, s,
+                   pi_launch_select(p, l, q_all + (size_t)l * q_bytes, k_budget + (size_t)l * p->R, sel_of(l),
+                                    nsel_of(l), s, tab_of(l), -1, r0[g], nr[g]));
+        PI_CUDA_TRY(cudaEventRecord(ev[0], s));
+        PI_CUDA_TRY(cudaStreamWaitEvent(ys, ev[0], 0));
+        p->recall_calls++;
+        if (p->fault_recall_at > 0 && p->recall_calls == p->fault_recall_at) return PI_ERR_FAULT_INJECTED;
+        PI_TIMED_G(l, g, PI_K_GATHER, ys,
+                   pi_launch_gather(p, l, nullptr, true, true, ys, append ? k_new_all + (size_t)l * kv_bytes : nullptr,
+                                    append ? v_new_all + (size_t)l * kv_bytes : nullptr, r0[g], nr[g]));
+        PI_CUDA_TRY(cudaEventRecord(ev[1], ys));
+        PI_CUDA_TRY(cudaStreamWaitEvent(s, ev[1], 0));
+        PI_TIMED_G(l, g, PI_K_ATTENTION, s,
+                   pi_launch_attention(p, l, q_all + (size_t)l * q_bytes, sel_of(l), tab_of(l), nsel_of(l),
+                                       out_all + (size_t)l * q_bytes,
+                                       lse_all ? lse_all + (size_t)l * p->R * p->Hq : nullptr, nullptr, s, r0[g],
+                                       nr[g]));
+      }
+    // the caller's compute stream completes after every group's last attention
+    for (int g = 1; g < M; g++) {
+      PI_CUDA_TRY(cudaEventRecord(p->grp_done[g], gs[g]));
+      PI_CUDA_TRY(cudaStreamWaitEvent(cs, p->grp_done[g], 0));
+    }
+  } else if (p->attn_stream_on) {
     // three streams: compute runs append + select, copy runs the gather, the
     // pool's own stream runs attention. append(l) of this step waits for
     // attention(l) of the previous step (which reads the token count, selection
@@ -147,6 +198,8 @@ static pi_status step_impl(pi_pool* p, const uint8_t* q_all, const uint8_t* k_ne
     PI_CUDA_TRY(cudaStreamSynchronize(cs));
     PI_CUDA_TRY(cudaStreamSynchronize(ys));
     PI_CUDA_TRY(cudaStreamSynchronize(p->attn_stream));
+    for (int g = 1; g < 8; g++)
+      if (p->grp_stream[g]) PI_CUDA_TRY(cudaStreamSynchronize(p->grp_stream[g]));
     PI_CUDA_TRY(cudaMemcpy(c.data(), p->recall_counts, sizeof(long long) * 4 * p->L, cudaMemcpyDeviceToHost));
     std::vector<int> ns((size_t)p->L * RU);
     PI_CUDA_TRY(cudaMemcpy(ns.data(), p->step_nsel, sizeof(int) * ns.size(), cudaMemcpyDeviceToHost));
@@ -214,7 +267,8 @@ extern "C" pi_status pi_pool_set_timing(pi_pool* p, int max_steps) {
   p->timing_steps = 0;
   p->timing_used = 0;
   if (max_steps == 0) return PI_OK;
-  const size_t n = (size_t)max_steps * p->L * PI_K_KINDS * 2;
+  p->timing_groups = p->sched_dependent ? p->sched_groups : 1;
+  const size_t n = (size_t)max_steps * p->L * p->timing_groups * PI_K_KINDS * 2;
   p->tev.resize(n, nullptr);
   for (size_t i = 0; i < n; i++) PI_CUDA_TRY(cudaEventCreate(&p->tev[i]));
   p->timing_steps = max_steps;
@@ -226,9 +280,9 @@ extern "C" pi_status pi_pool_get_timing(pi_pool* p, pi_kernel_timing* out) {
   PI_CUDA_TRY(cudaDeviceSynchronize());
   for (int k = 0; k < PI_K_KINDS; k++) out[k] = pi_kernel_timing{0, 0.0};
   for (int s = 0; s < p->timing_used; s++)
-    for (int l = 0; l < p->L; l++)
+    for (int lg = 0; lg < p->L * p->timing_groups; lg++)
       for (int k = 0; k < PI_K_KINDS; k++) {
-        cudaEvent_t* ev = &p->tev[(((size_t)s * p->L + l) * PI_K_KINDS + k) * 2];
+        cudaEvent_t* ev = &p->tev[(((size_t)s * p->L * p->timing_groups + lg) * PI_K_KINDS + k) * 2];
         float ms = 0.0f;
         // a kind that did not run in this step leaves its pair unrecorded
         if (cudaEventQuery(ev[1]) != cudaSuccess) { cudaGetLastError(); continue; }
@@ -245,6 +299,24 @@ extern "C" pi_status pi_pool_set_pipeline(pi_pool* p, int select_ahead, int atte
   PI_CUDA_TRY(cudaDeviceSynchronize());  // no step of the old mode may still run
   p->select_ahead = select_ahead;
   p->attn_stream_on = attention_stream != 0;
+  return PI_OK;
+}
+
+extern "C" pi_status pi_pool_set_schedule(pi_pool* p, int dependent, int groups) {
+  if (!p || (dependent != 0 && dependent != 1) || groups < 1 || groups > 8 || groups > p->R) return PI_ERR_INVALID;
+  PI_CUDA_TRY(cudaDeviceSynchronize());  // no step of the old schedule may still run
+  if (dependent) {
+    if (p->grp_ev.empty()) {
+      p->grp_ev.resize((size_t)p->L * 8 * 2, nullptr);
+      for (auto& e : p->grp_ev) PI_CUDA_TRY(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+    }
+    for (int g = 1; g < groups; g++) {
+      if (!p->grp_stream[g]) PI_CUDA_TRY(cudaStreamCreateWithFlags(&p->grp_stream[g], cudaStreamNonBlocking));
+      if (!p->grp_done[g]) PI_CUDA_TRY(cudaEventCreateWithFlags(&p->grp_done[g], cudaEventDisableTiming));
+    }
+  }
+  p->sched_dependent = dependent;
+  p->sched_groups = dependent ? groups : 1;
   return PI_OK;
 }
 

@@ -559,3 +559,89 @@ def test_selection_modes_accepted_per_pool():
         for bad in (-1.0, float("nan"), float("inf")):
             with pytest.raises(pi.PiError):
                 pool.set_consensus_lambda(bad)
+
+
+def _run_steps(w, setup, method=pi.PI_RECALL_UVA):
+    """Decode w.steps pipelined steps on a fresh pool configured by setup(pool);
+    returns every step's outputs and library state (host copies)."""
+    L, R = w.layers, w.batch
+    qs = queries(w)
+    res = []
+    with make_pool(w) as pool:
+        setup(pool)
+        prefill(pool, w)
+        for step in range(w.steps):
+            kn, vn = new_tokens(w, step)
+            kbud = np.full((L, R), w.k, dtype=np.int32)
+            kbud[-1, 0] = max(1, w.k // 2)
+            out = torch.empty((L, R, w.hq, w.head_dim), dtype=torch.int16, device="cuda")
+            lse = torch.empty((L, R, w.hq), dtype=torch.float32, device="cuda")
+            compute = torch.cuda.Stream()
+            pool.decode_step(dev(qs[step]), dev(kn), dev(vn), dev(kbud), out, lse, method=method, compute=compute)
+            torch.cuda.synchronize()
+            assert pool.device_status() == pi.PI_OK
+            sel_v, nsel_v, tab_v = pool.view_step()
+            res.append(dict(out=out.cpu().numpy(), lse=lse.cpu().numpy(), sel=sel_v.cpu().numpy(),
+                            nsel=nsel_v.cpu().numpy(), tab=tab_v.cpu().numpy(),
+                            sob=pool.view_slot_of_block().cpu().numpy(), bos=pool.view_block_of_slot().cpu().numpy(),
+                            pool=pool.view_pool().cpu().numpy()))
+    return res
+
+
+@pytest.mark.parametrize("mode,evict", [(pi.PI_SHARED, 0), (pi.PI_SHARED, 1), (pi.PI_CONSENSUS, 0)],
+                         ids=["shared", "shared_lru", "consensus"])
+def test_dependent_schedule_gives_identical_results(mode, evict):
+    """Interruptible layer-wise scheduling (guide, "Interruptible Layer-Wise
+    Scheduling"): with dependent queries and 1, 2 or 3 interleaved request groups
+    the decode step computes what the default schedule computes: selections,
+    tables, slot maps and pool bytes bit for bit, attention outputs within the
+    tolerances (a launch over fewer requests uses more splits, so the summation
+    order differs), every step; the default run is itself checked against the
+    oracle."""
+    w = Workload(layers=3, batch=5, hq=32, hkv=8, head_dim=128, block_tokens=64, ntok=[4000, 2500, 3100, 700, 5000],
+                 k=8, window=2, pool_slots=12, steps=3, rho=0.9, heavy_frac=0.05, seed=61, evict_policy=evict,
+                 select_mode=mode)
+    base = _run_steps(w, lambda pool: None)
+    om = OracleModel(w)
+    qs = queries(w)
+    for step in range(w.steps):
+        kn, vn = new_tokens(w, step)
+        kbud = np.full((w.layers, w.batch), w.k, dtype=np.int32)
+        kbud[-1, 0] = max(1, w.k // 2)
+        for l in range(w.layers):
+            om.append(l, kn[l], vn[l])
+            ref_sel = om.select(l, qs[step][l], kbud[l])
+            for r in range(w.batch):
+                assert np.array_equal(base[step]["sel"][l, r, 0, : len(ref_sel[r])], ref_sel[r])
+            om.recall(l, ref_sel)
+            ref_out, ref_lse, _ = om.attention(l, qs[step][l], ref_sel)
+            assert np.max(np.abs(bf16_to_f32(base[step]["out"][l].view(np.uint16)) - bf16_to_f32(ref_out))) <= OUT_ATOL
+    for groups in (1, 2, 3):
+        got = _run_steps(w, lambda pool, g=groups: pool.set_schedule(True, g))
+        for s in range(w.steps):
+            for key in ("sel", "nsel", "tab", "sob", "bos", "pool"):
+                assert np.array_equal(got[s][key], base[s][key]), (groups, s, key)
+            err = np.max(np.abs(bf16_to_f32(got[s]["out"].view(np.uint16)) - bf16_to_f32(base[s]["out"].view(np.uint16))))
+            assert err <= OUT_ATOL, (groups, s, err)
+            rel = np.abs(got[s]["lse"] - base[s]["lse"]) / np.maximum(np.abs(base[s]["lse"]), 1.0)
+            assert rel.max() <= LSE_RTOL, (groups, s)
+
+
+def test_schedule_arguments():
+    w = C1
+    with make_pool(w) as pool:
+        for dep, g in ((2, 1), (1, 0), (1, 9), (1, 2)):  # batch 1: at most one group
+            with pytest.raises(pi.PiError) as ei:
+                pool.set_schedule(bool(dep) if dep < 2 else dep, g)
+            assert ei.value.status == pi.PI_ERR_INVALID
+        pool.set_schedule(True, 1)
+        prefill(pool, w)
+        L, R = w.layers, w.batch
+        q = dev(queries(w)[0])
+        kn, vn = new_tokens(w, 0)
+        out = torch.empty((L, R, w.hq, w.head_dim), dtype=torch.int16, device="cuda")
+        with pytest.raises(pi.PiError) as ei:
+            pool.decode_step(q, dev(kn), dev(vn), dev(np.full((L, R), w.k, dtype=np.int32)), out,
+                             method=pi.PI_RECALL_MEMCPY)
+        assert ei.value.status == pi.PI_ERR_INVALID
+        pool.set_schedule(False, 1)
