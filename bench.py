@@ -310,7 +310,7 @@ def run_ours(args, cfg, rank, world, local_rank):
     L, R, Hq, Hkv, D, B = (cfg[k] for k in ("layers", "batch", "hq", "hkv", "head_dim", "block_tokens"))
     K, Wm = args.steps, args.warmup
     prewarm_cap = 400  # warm-up runs at least W steps and at least args.warmup_s seconds, at most this many
-    total_steps = prewarm_cap + Wm + 4 * K + 4
+    total_steps = prewarm_cap + Wm + 4 * K + 4 + ((4 * args.pin_layers + 12 + Wm) if args.admission else 0)
     ntok0 = cfg["ntok"]
     max_blocks = -(-(ntok0 + total_steps) // B) + 1
     seed = rank_seed(args.seed, rank)
@@ -337,7 +337,8 @@ def run_ours(args, cfg, rank, world, local_rank):
                    cfg["window"], host_layers=(host_layers if host_layers < L else 0), gather_ctas=args.gather_ctas,
                    pool_slots_per_req=slots_per_req, gather_depth=args.gather_depth, host_alloc=args.host_alloc,
                    evict_policy=(pi.PI_EVICT_LRU if args.evict == "lru" else pi.PI_EVICT_ASCENDING),
-                   select_mode=(pi.PI_CONSENSUS if args.select == "consensus" else pi.PI_SHARED))
+                   select_mode=(pi.PI_CONSENSUS if args.select == "consensus" else pi.PI_SHARED),
+                   pin_layers=(args.pin_layers if args.admission else 0))
     if args.select == "consensus":
         pool.set_consensus_lambda(args.consensus_lambda)
     if args.schedule == "dependent":
@@ -406,6 +407,7 @@ def run_ours(args, cfg, rank, world, local_rank):
     warm_stats = []
     for _ in range(min(Wm, 3)):
         warm_stats.append(run_step(stats=True))
+    admission = None
     t_w = time.time()
     warm_steps = len(warm_stats)
     while warm_steps < Wm or (time.time() - t_w < args.warmup_s and warm_steps < prewarm_cap):
@@ -415,6 +417,32 @@ def run_ours(args, cfg, rank, world, local_rank):
             torch.cuda.synchronize()
     torch.cuda.synchronize()
     assert pool.device_status() == pi.PI_OK
+
+    if args.admission:
+        # IO-adaptive admission in the steady state: one decision per window of two
+        # steps from the link utilisation the window measured (recalled bytes /
+        # window time / H2D peak), until three windows in a row change nothing
+        decisions = []
+        quiet = 0
+        for _ in range(2 * args.pin_layers + 6):
+            ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            ea.record(compute)
+            got = [run_step(stats=True) for _ in range(2)]
+            eb.record(compute)
+            torch.cuda.synchronize()
+            util = sum(g_["bytes"] for g_ in got) / (ea.elapsed_time(eb) / 1e3) / (h2d_peak * 1e9)
+            layer_, pinned_ = pool.admission(util)
+            decisions.append({"util": round(util, 3), "layer": layer_, "pinned": pinned_})
+            quiet = quiet + 1 if layer_ < 0 else 0
+            if quiet >= 3:
+                break
+        for _ in range(Wm):  # settle after the last change
+            run_step()
+        torch.cuda.synchronize()
+        pinned_layers = [l for l in range(L) if pool.slots(0, l) > pool.slots_per_req[0]]
+        admission = {"pin_layers": args.pin_layers, "pinned": pinned_layers, "decisions": decisions}
+        log(f"rank {rank}: admission pinned layers {pinned_layers} after {len(decisions)} windows")
 
     # ---- pass A: headline, device time over K steps, no per-kernel events
     barrier()
@@ -611,6 +639,7 @@ def run_ours(args, cfg, rank, world, local_rank):
                               else f"consensus (lambda {args.consensus_lambda})"),
                    "select_ahead": ("library default" if args.select_ahead < 0 else (args.select_ahead or "all")),
                    "streams": 2 if args.two_streams else 3,
+                   "admission": admission,
                    "schedule": ("queries known up front, selections run ahead" if args.schedule == "ahead" else
                                 f"dependent queries, {args.groups} interleaved request group(s)"),
                    "gather_ctas": args.gather_ctas or "default",
@@ -792,6 +821,9 @@ def main():
     ap.add_argument("--schedule", default="ahead", choices=["ahead", "dependent"],
                     help="dependent: a request's selection of layer l+1 waits for its attention of layer l")
     ap.add_argument("--groups", type=int, default=2, help="request groups interleaved under --schedule dependent")
+    ap.add_argument("--admission", action="store_true",
+                    help="IO-adaptive admission during warm-up: pin layers whole in HBM while the link is saturated")
+    ap.add_argument("--pin-layers", type=int, default=8, help="layers with room reserved for pinning (admission)")
     ap.add_argument("--select", default="shared", choices=["shared", "consensus"],
                     help="block ranking: mean-key shared score, or the consensus score (max + lambda x mean per group)")
     ap.add_argument("--consensus-lambda", type=float, default=0.5)

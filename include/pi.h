@@ -98,6 +98,10 @@ typedef struct pi_config {
   int host_alloc;            /* host store allocation: 0 = cudaHostAlloc (pinned,
                                 mapped); 1 = anonymous mmap advised for transparent huge
                                 pages, then cudaHostRegister (pinned, mapped) */
+  int pin_layers;            /* layers that can be held whole in HBM (IO-adaptive
+                                admission): the first ceil(n/2) and the last
+                                floor(n/2) layers get room for max_blocks blocks per
+                                request (0 = none) */
   const int* pool_slots_per_req; /* optional host [batch]: per-request P (each
                                 >= k_max + window); NULL = pool_slots for all */
 } pi_config;
@@ -122,9 +126,9 @@ typedef struct pi_step_stats {
 /* Pointers into library-owned device state, for inspection and tests. */
 typedef struct pi_pool_views {
   void* pool;                /* device pool base (slots of BB bytes) */
-  const long long* slot_base;/* host [batch]: first global slot of (r, layer 0);
-                                global slot of (r, l, s) = slot_base[r] + l*P_r + s */
-  const int* slots_per_req;  /* host [batch]: P_r */
+  const long long* slot_base;/* host [batch][layers]: first global slot of (r, l);
+                                global slot of (r, l, s) = slot_base[r*layers + l] + s */
+  const int* slots_per_req;  /* host [batch]: the configured P_r */
   float* kmean;              /* device [R][L][max_blocks][Hkv][D] fp32 summaries */
   int* ntok;                 /* device [R][L] tokens held */
   int* slot_of_block;        /* device [R][L][U][max_blocks], U = 1 or Hkv; -1 = absent */
@@ -136,6 +140,10 @@ typedef struct pi_pool_views {
   size_t block_bytes, frag_bytes, host_region_bytes;
   int* slot_stamp;           /* device [R][L][U][P_max]: epoch a slot's block was last
                                 selected (-1 never); maintained under PI_EVICT_LRU */
+  const int* slots_rl;       /* host [batch][layers]: slots in use for (r, l) (P_r, or
+                                the room of a pinned layer) */
+  const int* capacity_rl;    /* host [batch][layers]: slots reserved for (r, l) */
+  long long total_slots;     /* slots of the whole pool */
 } pi_pool_views;
 
 /* ------------------------------------------------------------------ lifetime */
@@ -240,6 +248,26 @@ pi_status pi_pool_preload(pi_pool* p, int layer, int req, const int* blocks, int
  * or PI_EVICT_LRU; head-wise pools included). Least-recently-selected is this
  * library's variant: the pages leave eviction open. */
 pi_status pi_pool_set_evict(pi_pool* p, int policy);
+
+/* IO-adaptive offloading admission (PulseInfer Guide, "Interruptible Layer-Wise
+ * Scheduling & Adaptive Admission", "2. IO-Adaptive Offloading Admission").
+ * pinned = 1 holds `layer` whole in HBM: each request of it uses the room the
+ * pool reserved for all its blocks (config pin_layers: the first ceil(n/2) and
+ * last floor(n/2) layers), so once a block has been recalled it stays and the
+ * layer recalls nothing new beyond first use; pinned = 0 returns the layer to
+ * P_r slots and drops the blocks held in slots >= P_r from the maps (their next
+ * selection recalls them). Selection, the recall rule and every result are
+ * unchanged; only residency differs. Synchronizes the device. PI_ERR_INVALID
+ * for a layer without reserved room. */
+pi_status pi_pool_pin_layer(pi_pool* p, int layer, int pinned);
+
+/* One admission decision from the host link's measured utilisation (recalled
+ * bytes per second over the link's peak, 0..1): above 0.85 the next pinnable
+ * layer in the order 0, L-1, 1, L-2, ... is pinned; below 0.5 the layer pinned
+ * last is released; otherwise nothing changes (the guide's thresholds). *layer =
+ * the layer changed (-1: none), *pinned = its new state. Synchronizes the device
+ * when it changes a layer. */
+pi_status pi_pool_admission(pi_pool* p, double link_util, int* layer, int* pinned);
 
 /* Weight lambda of the group mean in the consensus score (default 0.5, the
  * guide's "typical" value; its worked example uses 1). Applies to later

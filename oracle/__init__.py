@@ -80,6 +80,8 @@ def lib():
         L.or_select_consensus.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, f32, vp, vp]
         L.or_select_headwise.restype = None
         L.or_select_headwise.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp]
+        L.or_recall_plan_pinned.restype = i32
+        L.or_recall_plan_pinned.argtypes = [vp, i32, vp, vp, i32, vp, vp, vp, vp]
         L.or_recall_plan.restype = i32
         L.or_recall_plan.argtypes = [vp, i32, vp, vp, i32, vp, vp, vp, vp]
         L.or_recall_plan_lru.restype = i32
@@ -218,9 +220,11 @@ def select_headwise(q: np.ndarray, kmean: np.ndarray, k: int, W: int):
 
 
 # --------------------------------------------------------------------- a-3
-def recall_plan(sel: np.ndarray, slot_of_block: np.ndarray, block_of_slot: np.ndarray):
+def recall_plan(sel: np.ndarray, slot_of_block: np.ndarray, block_of_slot: np.ndarray, empty_first: bool = False):
     """Updates the two maps in place. Returns (table, miss_blocks, miss_slots, evicted)
-    or None when the pool is too small (maps untouched)."""
+    or None when the pool is too small (maps untouched). empty_first: the rule of a
+    layer held whole in HBM (guide, "2. IO-Adaptive Offloading Admission"): empty
+    slots are taken before slots holding an unselected block."""
     sel = _c(sel, np.int32)
     assert slot_of_block.dtype == np.int32 and block_of_slot.dtype == np.int32
     assert slot_of_block.flags["C_CONTIGUOUS"] and block_of_slot.flags["C_CONTIGUOUS"]
@@ -230,7 +234,8 @@ def recall_plan(sel: np.ndarray, slot_of_block: np.ndarray, block_of_slot: np.nd
     mb = np.empty(max(n, 1), dtype=np.int32)
     ms = np.empty(max(n, 1), dtype=np.int32)
     ev = np.empty(max(n, 1), dtype=np.int32)
-    nm = lib().or_recall_plan(_p(sel), n, _p(slot_of_block), _p(block_of_slot), P, _p(table), _p(mb), _p(ms), _p(ev))
+    fn = lib().or_recall_plan_pinned if empty_first else lib().or_recall_plan
+    nm = fn(_p(sel), n, _p(slot_of_block), _p(block_of_slot), P, _p(table), _p(mb), _p(ms), _p(ev))
     if nm < 0:
         return None
     return table[:n].copy(), mb[:nm].copy(), ms[:nm].copy(), ev[:nm].copy()

@@ -334,6 +334,48 @@ int or_recall_plan(const int* sel, int nsel, int* slot_of_block, int* block_of_s
   return nmiss;
 }
 
+/* Plan of a layer held whole in HBM ([G] "2. IO-Adaptive Offloading Admission":
+ * the most active layers are retained in GPU HBM). Such a layer has room for
+ * every block, so a recall takes the empty slots first (ascending) and only then
+ * slots holding an unselected block (ascending): nothing is evicted while room
+ * is left. Otherwise as or_recall_plan. */
+int or_recall_plan_pinned(const int* sel, int nsel, int* slot_of_block, int* block_of_slot, int P, int* table,
+                          int* miss_block, int* miss_slot, int* evicted) {
+  int nmiss = 0, nfree = 0;
+  int* missing = (int*)malloc(sizeof(int) * (size_t)(nsel > 0 ? nsel : 1));
+  int* freel = (int*)malloc(sizeof(int) * (size_t)(P > 0 ? P : 1));
+  for (int i = 0; i < nsel; i++)
+    if (slot_of_block[sel[i]] < 0) missing[nmiss++] = sel[i];
+  for (int pass = 0; pass < 2; pass++)
+    for (int s = 0; s < P; s++) {
+      int b = block_of_slot[s];
+      if (pass == 0) {
+        if (b < 0) freel[nfree++] = s;
+        continue;
+      }
+      if (b < 0) continue;
+      int keep = 0;
+      for (int i = 0; i < nsel; i++)
+        if (sel[i] == b) { keep = 1; break; }
+      if (!keep) freel[nfree++] = s;
+    }
+  if (nmiss > nfree) { free(missing); free(freel); return -1; }
+  for (int i = 0; i < nmiss; i++) {
+    int s = freel[i];
+    int old = block_of_slot[s];
+    if (old >= 0) slot_of_block[old] = -1;
+    slot_of_block[missing[i]] = s;
+    block_of_slot[s] = missing[i];
+    if (miss_block) miss_block[i] = missing[i];
+    if (miss_slot) miss_slot[i] = s;
+    if (evicted) evicted[i] = old;
+  }
+  for (int i = 0; i < nsel; i++) table[i] = slot_of_block[sel[i]];
+  free(missing);
+  free(freel);
+  return nmiss;
+}
+
 /* Least-recently-selected variant of the plan (a pool policy option; the pages
  * leave eviction open). stamp[s] is the epoch at which slot s's block was last
  * selected (-1: never, or the slot is empty). This call is epoch `epoch`: the

@@ -71,11 +71,11 @@ class Pool:
     def __init__(self, layers: int, batch: int, hq: int, hkv: int, head_dim: int, block_tokens: int,
                  max_blocks: int, pool_slots: int, k_max: int, window: int, select_mode: int = PI_SHARED,
                  host_layers: int = 0, staging_blocks: int = 0, gather_ctas: int = 0, pool_slots_per_req=None,
-                 gather_depth: int = 0, host_alloc: int = 0, evict_policy: int = 0):
+                 gather_depth: int = 0, host_alloc: int = 0, evict_policy: int = 0, pin_layers: int = 0):
         self.lib = load()
         cfg = pi_config(layers, batch, hq, hkv, head_dim, block_tokens, max_blocks, pool_slots, k_max, window,
                         select_mode, host_layers, staging_blocks, gather_ctas, gather_depth, evict_policy, host_alloc,
-                        None)
+                        pin_layers, None)
         self._slots_arr = None
         if pool_slots_per_req is not None:
             self._slots_arr = (ctypes.c_int * batch)(*[int(x) for x in pool_slots_per_req])
@@ -98,7 +98,8 @@ class Pool:
         self.frag_bytes = v.frag_bytes
         self.region_bytes = v.host_region_bytes
         self.slots_per_req = [v.slots_per_req[r] for r in range(batch)]
-        self.slot_base = [v.slot_base[r] for r in range(batch)]
+        self.slot_base = [[v.slot_base[r * layers + l] for l in range(layers)] for r in range(batch)]
+        self.total_slots = v.total_slots
 
     # ---------------------------------------------------------------- lifetime
     def close(self):
@@ -133,11 +134,14 @@ class Pool:
 
     # ---------------------------------------------------------------- views
     def view_pool(self):
-        total = sum(self.slots_per_req) * self.L
-        return device_view(self._views.pool, (total, self.Hkv, 2, self.B, self.D), "int16")
+        return device_view(self._views.pool, (self.total_slots, self.Hkv, 2, self.B, self.D), "int16")
 
     def global_slot(self, r: int, l: int, s: int) -> int:
-        return self.slot_base[r] + l * self.slots_per_req[r] + s
+        return self.slot_base[r][l] + s
+
+    def slots(self, r: int, l: int) -> int:
+        """Slots (r, l) uses now: P_r, or every block of a pinned layer."""
+        return self._views.slots_rl[r * self.L + l]
 
     def view_kmean(self):
         return device_view(self._views.kmean, (self.R, self.L, self.max_blocks, self.Hkv, self.D), "float32")
@@ -193,6 +197,16 @@ class Pool:
     def set_schedule(self, dependent: bool, groups: int = 1):
         dep = dependent if isinstance(dependent, int) and not isinstance(dependent, bool) else int(bool(dependent))
         check(self.lib.pi_pool_set_schedule(self.h, dep, groups), "pi_pool_set_schedule")
+
+    def pin_layer(self, layer: int, pinned: bool = True):
+        check(self.lib.pi_pool_pin_layer(self.h, layer, int(bool(pinned))), "pi_pool_pin_layer")
+
+    def admission(self, link_util: float):
+        """One IO-adaptive admission decision; returns (layer changed or -1, pinned)."""
+        layer, pinned = ctypes.c_int(), ctypes.c_int()
+        check(self.lib.pi_pool_admission(self.h, float(link_util), ctypes.byref(layer), ctypes.byref(pinned)),
+              "pi_pool_admission")
+        return layer.value, bool(pinned.value)
 
     def set_consensus_lambda(self, lam: float):
         check(self.lib.pi_pool_set_consensus_lambda(self.h, float(lam)), "pi_pool_set_consensus_lambda")

@@ -27,7 +27,7 @@ class pi_config(ctypes.Structure):
                 ("block_tokens", c_int), ("max_blocks", c_int), ("pool_slots", c_int), ("k_max", c_int),
                 ("window", c_int), ("select_mode", c_int), ("host_layers", c_int), ("staging_blocks", c_int),
                 ("gather_ctas", c_int), ("gather_depth", c_int), ("evict_policy", c_int), ("host_alloc", c_int),
-                ("pool_slots_per_req", ctypes.POINTER(c_int))]
+                ("pin_layers", c_int), ("pool_slots_per_req", ctypes.POINTER(c_int))]
 
 
 class pi_recall_stats(ctypes.Structure):
@@ -47,7 +47,8 @@ class pi_pool_views(ctypes.Structure):
                 ("kmean", c_void_p), ("ntok", c_void_p), ("slot_of_block", c_void_p), ("block_of_slot", c_void_p),
                 ("p_max", c_int), ("step_sel", c_void_p), ("step_nsel", c_void_p), ("step_table", c_void_p),
                 ("block_bytes", c_size_t), ("frag_bytes", c_size_t), ("host_region_bytes", c_size_t),
-                ("slot_stamp", c_void_p)]
+                ("slot_stamp", c_void_p), ("slots_rl", ctypes.POINTER(c_int)), ("capacity_rl", ctypes.POINTER(c_int)),
+                ("total_slots", c_ll)]
 
 
 class pi_kernel_timing(ctypes.Structure):
@@ -77,6 +78,8 @@ _SIGS = {
     "pi_pool_set_attention": (c_int, [_P, c_int]),
     "pi_pool_set_attention_cluster": (c_int, [_P, c_int]),
     "pi_pool_set_schedule": (c_int, [_P, c_int, c_int]),
+    "pi_pool_pin_layer": (c_int, [_P, c_int, c_int]),
+    "pi_pool_admission": (c_int, [_P, c_double, ctypes.POINTER(c_int), ctypes.POINTER(c_int)]),
     "pi_pool_set_consensus_lambda": (c_int, [_P, ctypes.c_float]),
     "pi_pool_set_evict": (c_int, [_P, c_int]),
     "pi_sparse_decode": (c_int, [_P, c_int, _P, _P, _P, _P, _P, _P, _P, _P]),

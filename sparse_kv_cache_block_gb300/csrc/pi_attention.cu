@@ -110,8 +110,8 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
     s_slot[i] = tabu[i0 + i];
   }
   const int nt = p.ntok[(size_t)r * p.L + p.layer];
-  const int Pr = p.P[r];
-  const long long gbase = p.slot_base[r] + (long long)p.layer * Pr;
+  const int Pr = p.P[(size_t)r * p.L + p.layer];
+  const long long gbase = p.slot_base[(size_t)r * p.L + p.layer];
   const int gid = lane >> 2, tig = lane & 3;
   uint32_t qb[KS][2];  // this group's query rows as the mma's B fragments (consumer warps)
   if (warp < kConsumerWarps) {

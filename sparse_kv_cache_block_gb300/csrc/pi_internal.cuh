@@ -54,10 +54,15 @@ struct pi_pool {
   // device state
   uint8_t* pool = nullptr;       // all slots
   long long total_slots = 0;
-  std::vector<long long> slot_base_h;
-  std::vector<int> P_h;
-  long long* slot_base = nullptr; // device [R]
-  int* P = nullptr;               // device [R]
+  std::vector<long long> slot_base_h;  // [R][L] first global slot of (r, l)
+  std::vector<int> P_h;           // [R] configured slots per (request, layer)
+  std::vector<int> P_rl_h;        // [R][L] slots in use (P_r, or the room of a pinned layer)
+  std::vector<int> cap_rl_h;      // [R][L] slots reserved
+  std::vector<int> pinned_h;      // [L] 1 = held whole in HBM
+  std::vector<int> pinnable_h;    // [L] 1 = room reserved for every block
+  std::vector<int> pin_order;     // admission: layers pinned, most recent last
+  long long* slot_base = nullptr; // device [R][L]
+  int* P = nullptr;               // device [R][L] slots in use
   float* kmean = nullptr;         // [R][L][max_blocks][Hkv][D]
   float* tail_sum = nullptr;      // [R][L][Hkv][D]
   int* ntok = nullptr;            // [R][L]
@@ -135,7 +140,7 @@ struct pi_pool {
 
 // --------------------------------------------------------------- helpers
 static inline long long pi_global_slot(const pi_pool* p, int r, int l, int s) {
-  return p->slot_base_h[r] + (long long)l * p->P_h[r] + s;
+  return p->slot_base_h[(size_t)r * p->L + l] + s;
 }
 
 // kernel launchers (return cudaGetLastError of the launch)

@@ -61,6 +61,7 @@ struct UnitArgs {
   int* plan_n;           // out: number of plan entries
   long long* counts;     // [0] misses, [1] hits (accumulated)
   unsigned* status;
+  int empty_first;       // layer held whole in HBM: empty slots before stale ones (lowest-slot rule)
 };
 
 // Shared memory: bits [ceil(max_blocks/32)] + miss_pos [cap] + free_list [cap];
@@ -174,24 +175,29 @@ __device__ void plan_unit(const UnitArgs& a, unsigned* bits, int* miss_pos, int*
     }
     __syncthreads();
   }
-  for (int base = 0; base < a.P && nf < nm && !a.stamp; base += NT) {
-    const int s = base + threadIdx.x;
-    int fr = 0;
-    if (s < a.P) {
-      const int bb = a.bos[s];
-      if (bb < 0) {
-        fr = 1;
-      } else if (bb >= a.max_blocks) {
-        pi_flag(a.status, PI_DEV_BAD_INDEX);
-      } else {
-        fr = ((bits[bb >> 5] >> (bb & 31)) & 1u) ? 0 : 1;
+  // lowest free slot first; a layer held whole in HBM takes its empty slots
+  // before the slots of unselected blocks (two passes), so it evicts nothing
+  // while room is left
+  const int passes = a.empty_first ? 2 : 1;
+  for (int pass = 0; pass < passes && nf < nm && !a.stamp; pass++)
+    for (int base = 0; base < a.P && nf < nm; base += NT) {
+      const int s = base + threadIdx.x;
+      int fr = 0;
+      if (s < a.P) {
+        const int bb = a.bos[s];
+        if (bb < 0) {
+          fr = (passes == 1 || pass == 0) ? 1 : 0;
+        } else if (bb >= a.max_blocks) {
+          if (pass == passes - 1) pi_flag(a.status, PI_DEV_BAD_INDEX);
+        } else if (passes == 1 || pass == 1) {
+          fr = ((bits[bb >> 5] >> (bb & 31)) & 1u) ? 0 : 1;
+        }
       }
+      int tot;
+      const int pos = cta_excl_scan<NT>(fr, warp_sums, tot);
+      if (fr && nf + pos < nm) free_list[nf + pos] = s;
+      nf += tot;
     }
-    int tot;
-    const int pos = cta_excl_scan<NT>(fr, warp_sums, tot);
-    if (fr && nf + pos < nm) free_list[nf + pos] = s;
-    nf += tot;
-  }
   if (nf < nm) {
     if (threadIdx.x == 0) {
       pi_flag(a.status, PI_DEV_POOL_FULL);

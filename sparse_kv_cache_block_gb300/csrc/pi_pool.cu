@@ -1,3 +1,4 @@
+#include <algorithm>
 // Pool lifetime, views, residency control, device status and fault injection.
 //
 // The pool follows the architecture of "PulseInfer Guide: I/O-Centric Sparse
@@ -102,6 +103,7 @@ static bool valid_config(const pi_config& c) {
   if (c.host_alloc != 0 && c.host_alloc != 1) return false;
   if (c.evict_policy != PI_EVICT_ASCENDING && c.evict_policy != PI_EVICT_LRU) return false;
   if (c.gather_ctas < 0) return false;
+  if (c.pin_layers < 0 || c.pin_layers > c.layers) return false;
   int cap = c.k_max + c.window;
   if (c.pool_slots_per_req) {
     for (int r = 0; r < c.batch; r++)
@@ -159,15 +161,28 @@ extern "C" pi_status pi_pool_create(const pi_config* cfg, pi_pool** out) {
   const char* fault = getenv("PI_FAULT");
   if (parse_fault(p, fault) != PI_OK) { pool_free(p); return PI_ERR_INVALID; }
 
-  // per-request slot counts and global slot offsets
+  // slots per (request, layer): P_r, and room for every block in the pinnable
+  // layers (the first ceil(n/2) and the last floor(n/2)); global slot offsets
   p->P_h.resize(p->R);
-  p->slot_base_h.resize(p->R);
+  p->slot_base_h.resize((size_t)p->R * p->L);
+  p->P_rl_h.resize((size_t)p->R * p->L);
+  p->cap_rl_h.resize((size_t)p->R * p->L);
+  p->pinned_h.assign(p->L, 0);
+  p->pinnable_h.assign(p->L, 0);
+  const int pin_lo = (cfg->pin_layers + 1) / 2, pin_hi = cfg->pin_layers / 2;
   long long acc = 0;
   for (int r = 0; r < p->R; r++) {
     p->P_h[r] = cfg->pool_slots_per_req ? cfg->pool_slots_per_req[r] : cfg->pool_slots;
-    p->p_max = p->P_h[r] > p->p_max ? p->P_h[r] : p->p_max;
-    p->slot_base_h[r] = acc;
-    acc += (long long)p->L * p->P_h[r];
+    for (int l = 0; l < p->L; l++) {
+      const size_t rl = (size_t)r * p->L + l;
+      const bool pinnable = l < pin_lo || l >= p->L - pin_hi;
+      p->pinnable_h[l] = pinnable ? 1 : 0;
+      p->cap_rl_h[rl] = pinnable ? std::max(p->P_h[r], p->max_blocks) : p->P_h[r];
+      p->P_rl_h[rl] = p->P_h[r];
+      p->slot_base_h[rl] = acc;
+      acc += p->cap_rl_h[rl];
+      p->p_max = std::max(p->p_max, p->cap_rl_h[rl]);
+    }
   }
   p->total_slots = acc;
   p->lru_p2 = 1;
@@ -228,8 +243,8 @@ extern "C" pi_status pi_pool_create(const pi_config* cfg, pi_pool** out) {
     }                        \
   } while (0)
   TRY_ALLOC(dalloc(&p->pool, (size_t)p->total_slots * p->block_bytes));
-  TRY_ALLOC(dalloc(&p->slot_base, (size_t)p->R, false));
-  TRY_ALLOC(dalloc(&p->P, (size_t)p->R, false));
+  TRY_ALLOC(dalloc(&p->slot_base, (size_t)p->R * p->L, false));
+  TRY_ALLOC(dalloc(&p->P, (size_t)p->R * p->L, false));
   TRY_ALLOC(dalloc(&p->kmean, RL * p->max_blocks * p->Hkv * p->D));
   TRY_ALLOC(dalloc(&p->tail_sum, RL * p->Hkv * p->D));
   TRY_ALLOC(dalloc(&p->ntok, RL));
@@ -265,9 +280,9 @@ extern "C" pi_status pi_pool_create(const pi_config* cfg, pi_pool** out) {
   TRY_ALLOC(dalloc(&p->step_out, p->step_out_bytes, false));
 #undef TRY_ALLOC
 
-  if (cudaMemcpy(p->slot_base, p->slot_base_h.data(), sizeof(long long) * p->R, cudaMemcpyHostToDevice) !=
+  if (cudaMemcpy(p->slot_base, p->slot_base_h.data(), sizeof(long long) * p->R * p->L, cudaMemcpyHostToDevice) !=
           cudaSuccess ||
-      cudaMemcpy(p->P, p->P_h.data(), sizeof(int) * p->R, cudaMemcpyHostToDevice) != cudaSuccess) {
+      cudaMemcpy(p->P, p->P_rl_h.data(), sizeof(int) * p->R * p->L, cudaMemcpyHostToDevice) != cudaSuccess) {
     pool_free(p);
     return PI_ERR_CUDA;
   }
@@ -325,6 +340,9 @@ extern "C" pi_status pi_pool_get_views(pi_pool* p, pi_pool_views* v) {
   v->pool = p->pool;
   v->slot_base = p->slot_base_h.data();
   v->slots_per_req = p->P_h.data();
+  v->slots_rl = p->P_rl_h.data();
+  v->capacity_rl = p->cap_rl_h.data();
+  v->total_slots = p->total_slots;
   v->kmean = p->kmean;
   v->ntok = p->ntok;
   v->slot_of_block = p->slot_of;
@@ -392,7 +410,7 @@ extern "C" pi_status pi_pool_preload(pi_pool* p, int layer, int req, const int* 
   if (!p || layer < 0 || layer >= p->L || req < 0 || req >= p->R || n < 0 || (n > 0 && !blocks))
     return PI_ERR_INVALID;
   if (p->U != 1) return PI_ERR_STATE;
-  if (n > p->P_h[req]) return PI_ERR_INVALID;
+  if (n > p->P_rl_h[(size_t)req * p->L + layer]) return PI_ERR_INVALID;
   for (int i = 0; i < n; i++) {
     if (blocks[i] < 0 || blocks[i] >= p->max_blocks) return PI_ERR_INVALID;
     if (i > 0 && blocks[i] <= blocks[i - 1]) return PI_ERR_INVALID;
@@ -477,6 +495,88 @@ extern "C" pi_status pi_pool_set_gather(pi_pool* p, int ctas, int depth, int exc
 extern "C" pi_status pi_pool_set_consensus_lambda(pi_pool* p, float lambda) {
   if (!p || !(lambda >= 0.0f) || !(lambda <= 1e30f)) return PI_ERR_INVALID;
   p->consensus_lambda = lambda;
+  return PI_OK;
+}
+
+// ------------------------------------------------------------------ IO-adaptive admission
+// "PulseInfer Guide", section "Interruptible Layer-Wise Scheduling & Adaptive
+// Admission", "2. IO-Adaptive Offloading Admission": under a saturated link the
+// most active layers (the first and the last) stay whole in HBM; under a quiet
+// link they are offloaded again. A pinned layer uses the room the pool reserved
+// for every block of each request, so once its blocks have been recalled it
+// recalls nothing; releasing it drops the blocks held beyond P_r from the maps.
+static pi_status set_layer_slots(pi_pool* p, int layer, bool pinned) {
+  PI_CUDA_TRY(cudaDeviceSynchronize());
+  std::vector<int> sob(p->max_blocks), bos(p->p_max), stamp(p->p_max);
+  for (int r = 0; r < p->R; r++) {
+    const size_t rl = (size_t)r * p->L + layer;
+    const int keep = p->P_h[r];
+    if (!pinned && p->P_rl_h[rl] > keep) {
+      for (int u = 0; u < p->U; u++) {
+        const size_t rlu = rl * p->U + u;
+        int* sob_d = p->slot_of + rlu * p->max_blocks;
+        int* bos_d = p->block_of + rlu * p->p_max;
+        int* st_d = p->slot_stamp + rlu * p->p_max;
+        PI_CUDA_TRY(cudaMemcpy(sob.data(), sob_d, sizeof(int) * p->max_blocks, cudaMemcpyDeviceToHost));
+        PI_CUDA_TRY(cudaMemcpy(bos.data(), bos_d, sizeof(int) * p->p_max, cudaMemcpyDeviceToHost));
+        PI_CUDA_TRY(cudaMemcpy(stamp.data(), st_d, sizeof(int) * p->p_max, cudaMemcpyDeviceToHost));
+        for (int s = keep; s < p->P_rl_h[rl]; s++) {
+          const int b = bos[s];
+          if (b >= 0 && b < p->max_blocks) sob[b] = -1;
+          bos[s] = -1;
+          stamp[s] = -1;
+        }
+        PI_CUDA_TRY(cudaMemcpy(sob_d, sob.data(), sizeof(int) * p->max_blocks, cudaMemcpyHostToDevice));
+        PI_CUDA_TRY(cudaMemcpy(bos_d, bos.data(), sizeof(int) * p->p_max, cudaMemcpyHostToDevice));
+        PI_CUDA_TRY(cudaMemcpy(st_d, stamp.data(), sizeof(int) * p->p_max, cudaMemcpyHostToDevice));
+      }
+    }
+    p->P_rl_h[rl] = pinned ? p->cap_rl_h[rl] : keep;
+    PI_CUDA_TRY(cudaMemcpy(p->P + rl, &p->P_rl_h[rl], sizeof(int), cudaMemcpyHostToDevice));
+  }
+  p->pinned_h[layer] = pinned ? 1 : 0;
+  if (pinned) {
+    p->pin_order.push_back(layer);
+  } else {
+    for (size_t i = 0; i < p->pin_order.size(); i++)
+      if (p->pin_order[i] == layer) {
+        p->pin_order.erase(p->pin_order.begin() + (long)i);
+        break;
+      }
+  }
+  return PI_OK;
+}
+
+extern "C" pi_status pi_pool_pin_layer(pi_pool* p, int layer, int pinned) {
+  if (!p || layer < 0 || layer >= p->L || (pinned != 0 && pinned != 1)) return PI_ERR_INVALID;
+  if (!p->pinnable_h[layer]) return PI_ERR_INVALID;
+  if (p->pinned_h[layer] == pinned) return PI_OK;
+  return set_layer_slots(p, layer, pinned != 0);
+}
+
+extern "C" pi_status pi_pool_admission(pi_pool* p, double link_util, int* layer, int* pinned) {
+  if (!p || !layer || !pinned || !(link_util >= 0.0)) return PI_ERR_INVALID;
+  *layer = -1;
+  *pinned = 0;
+  if (link_util > 0.85) {
+    // the most active layers first: 0, L-1, 1, L-2, ...
+    for (int i = 0; i < p->L; i++) {
+      const int l = (i % 2 == 0) ? i / 2 : p->L - 1 - i / 2;
+      if (p->pinnable_h[l] && !p->pinned_h[l]) {
+        pi_status st = set_layer_slots(p, l, true);
+        if (st != PI_OK) return st;
+        *layer = l;
+        *pinned = 1;
+        break;
+      }
+    }
+  } else if (link_util < 0.5 && !p->pin_order.empty()) {
+    const int l = p->pin_order.back();
+    pi_status st = set_layer_slots(p, l, false);
+    if (st != PI_OK) return st;
+    *layer = l;
+    *pinned = 0;
+  }
   return PI_OK;
 }
 

@@ -37,6 +37,7 @@ struct PlanParams {
   int* slot_stamp;    // nullptr unless the least-recently-selected policy is on
   int* epoch;
   int layer, L, U, max_blocks, p_max, cap, lru_p2;
+  int empty_first;    // the layer is held whole in HBM
 };
 
 // One CTA per unit (request, or request x KV head). Writes the table and the
@@ -60,7 +61,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
   a.n = n;
   a.sob = p.slot_of + rlu * p.max_blocks;
   a.bos = p.block_of + rlu * p.p_max;
-  a.P = p.P[r];
+  a.P = p.P[(size_t)r * p.L + p.layer];
   a.max_blocks = p.max_blocks;
   a.table = p.table + (size_t)u * p.cap;
   a.plan = p.plan + (size_t)u * p.cap;
@@ -69,6 +70,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
   a.status = p.status;
   a.stamp = p.slot_stamp ? p.slot_stamp + rlu * p.p_max : nullptr;
   a.epoch = p.slot_stamp ? p.epoch + rlu : nullptr;
+  a.empty_first = p.empty_first;
   pi_plan::plan_unit<kPlanThreads>(a, reinterpret_cast<unsigned*>(sm), sm + words, sm + words + p.cap, warp_sums,
                                    keys, p.lru_p2);
 }
@@ -174,7 +176,7 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(GatherParams g) 
     const int j = (int)(e - prefix[u]);
     const int4 pe = g.plan[(size_t)u * g.cap + j];
     const int r = g.r0 + u / g.U, gu = u % g.U;
-    const int Pr = g.P[r];
+    const int Pr = g.P[(size_t)r * g.L + g.layer];
     const bool ok = pe.x >= 0 && pe.x < g.max_blocks && pe.y >= 0 && pe.y < Pr && pe.z < g.max_blocks;
     if (!ok) {
       if (threadIdx.x == 0) pi_flag(g.status, PI_DEV_BAD_INDEX);
@@ -187,7 +189,7 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(GatherParams g) 
       const uint8_t* src = g.stage_src ? g.stage_src + (size_t)(e - e0) * g.copy_bytes + off
                                        : g.host_src + (size_t)r * g.region_bytes +
                                              (size_t)pe.x * g.block_bytes + head_off + off;
-      uint8_t* blk = g.pool + (size_t)(g.slot_base[r] + (long long)g.layer * Pr + pe.y) * g.block_bytes;
+      uint8_t* blk = g.pool + (size_t)(g.slot_base[(size_t)r * g.L + g.layer] + pe.y) * g.block_bytes;
       uint8_t* dst = blk + head_off + off;
       const uint4* s4 = reinterpret_cast<const uint4*>(src);
       uint4* d4 = reinterpret_cast<uint4*>(dst);
@@ -258,6 +260,7 @@ cudaError_t pi_launch_plan(pi_pool* p, int layer, const int* sel, const int* nse
   pp.slot_stamp = lru ? p->slot_stamp : nullptr;
   pp.epoch = lru ? p->epoch : nullptr;
   pp.lru_p2 = lru ? p->lru_p2 : 0;
+  pp.empty_first = p->pinned_h.empty() ? 0 : p->pinned_h[layer];
   const size_t smem = pi_plan::plan_smem_bytes(p->max_blocks, p->cap, pp.lru_p2);
   if (smem > 48 * 1024) cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   plan_kernel<<<(unsigned)RU, kPlanThreads, smem, s>>>(pp);

@@ -109,10 +109,10 @@ __global__ void append_kernel(AppendParams a) {
     const int u = (a.U == 1) ? 0 : g;
     const int slot = a.slot_of[(rl * a.U + u) * a.max_blocks + b];
     if (slot >= 0) {
-      if (slot >= a.P[r]) {
+      if (slot >= a.P[rl]) {
         pi_flag(a.status, PI_DEV_BAD_INDEX);
       } else {
-        const long long gs = a.slot_base[r] + (long long)a.layer * a.P[r] + slot;
+        const long long gs = a.slot_base[rl] + slot;
         uint8_t* pool_blk = a.pool + (size_t)gs * block_bytes;
         *reinterpret_cast<uint4*>(pool_blk + in_block_k) = kv;
         *reinterpret_cast<uint4*>(pool_blk + in_block_v) = vv;
@@ -171,6 +171,7 @@ struct SelParams {
   int P2;                // the smallest power of two >= G
   int ring_stages;       // consensus: bulk-copy stages of 8 blocks' summaries
   int dyn_plan_off;      // bytes of dynamic shared memory before the plan scratch (consensus: ring + c_g)
+  int empty_first;       // the layer is held whole in HBM
 };
 
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -460,7 +461,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelParams p) {
   // fused plan: read this unit's slot maps now (one round of loads, held in
   // registers, then stored), so the plan runs from shared memory
   const size_t rlu_m = rl * p.U + g;
-  const int P_r = p.P[r];
+  const int P_r = p.P[rl];
   int* sob_c = nullptr;
   int* bos_c = nullptr;
   if (p.table && p.map_cache_blocks >= nb && p.map_cache_slots >= P_r) {
@@ -642,7 +643,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelParams p) {
   const size_t rlu = rl * p.U + g;
   a.sob = sob_c ? sob_c : p.slot_of + rlu * p.max_blocks;
   a.bos = bos_c ? bos_c : p.block_of + rlu * p.p_max;
-  a.P = p.P[r];
+  a.P = p.P[rl];
   a.max_blocks = p.max_blocks;
   a.table = p.table + (size_t)u * p.cap;
   a.plan = p.plan + (size_t)u * p.cap;
@@ -651,6 +652,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelParams p) {
   a.status = p.status;
   a.stamp = p.slot_stamp ? p.slot_stamp + rlu * p.p_max : nullptr;
   a.epoch = p.slot_stamp ? p.epoch + rlu : nullptr;
+  a.empty_first = p.empty_first;
   pi_plan::plan_unit<kSelThreads>(a, pl, reinterpret_cast<int*>(pl) + words, reinterpret_cast<int*>(pl) + words + p.cap,
                                   warp_sums, lkeys, p.lru_p2);
 }
@@ -757,6 +759,7 @@ cudaError_t pi_launch_select(pi_pool* p, int layer, const void* q, const int* k_
   sp.epoch = lru ? p->epoch : nullptr;
   sp.lru_p2 = lru ? p->lru_p2 : 0;
   sp.consensus = (mode == PI_CONSENSUS) ? 1 : 0;
+  sp.empty_first = p->pinned_h.empty() ? 0 : p->pinned_h[layer];
   sp.lambda = p->consensus_lambda;
   sp.P2 = 1;
   while (sp.P2 < p->G) sp.P2 <<= 1;

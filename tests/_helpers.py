@@ -107,12 +107,36 @@ class OracleModel:
         self.stamp = {(r, l, u): np.full(P[r], -1, dtype=np.int32)
                       for r in range(w.batch) for l in range(w.layers) for u in range(U)}
         self.epoch = {(r, l, u): 0 for r in range(w.batch) for l in range(w.layers) for u in range(U)}
+        self.pinned = set()  # layers held whole in HBM
 
     def preload(self, l, r, blocks):
         for s, b in enumerate(blocks):
             self.sob[(r, l, 0)][b] = s
             self.bos[(r, l, 0)][s] = b
             self.stamp[(r, l, 0)][s] = 0
+
+    def pin(self, l, capacity):
+        """Layer l held whole in HBM: every request's slot list grows to `capacity`."""
+        self.pinned.add(l)
+        for key in self.bos:
+            if key[1] == l and len(self.bos[key]) < capacity:
+                extra = capacity - len(self.bos[key])
+                self.bos[key] = np.concatenate([self.bos[key], np.full(extra, -1, dtype=np.int32)])
+                self.stamp[key] = np.concatenate([self.stamp[key], np.full(extra, -1, dtype=np.int32)])
+
+    def unpin(self, l):
+        """Layer l back to P_r slots: blocks held beyond them leave the maps."""
+        self.pinned.discard(l)
+        for key in list(self.bos):
+            if key[1] != l:
+                continue
+            P = self.P[key[0]]
+            for s in range(P, len(self.bos[key])):
+                b = self.bos[key][s]
+                if b >= 0:
+                    self.sob[key][b] = -1
+            self.bos[key] = self.bos[key][:P].copy()
+            self.stamp[key] = self.stamp[key][:P].copy()
 
     def flush(self):
         for key in self.sob:
@@ -126,7 +150,7 @@ class OracleModel:
         if self.w.evict_policy == 1:
             self.epoch[key] += 1
             return oracle.recall_plan_lru(sel, self.sob[key], self.bos[key], self.stamp[key], self.epoch[key])
-        return oracle.recall_plan(sel, self.sob[key], self.bos[key])
+        return oracle.recall_plan(sel, self.sob[key], self.bos[key], empty_first=l in self.pinned)
 
     def append(self, l, k_new, v_new):
         w = self.w

@@ -55,5 +55,5 @@ def test_struct_layouts_match_header():
     hdr = open(os.path.join(os.path.dirname(pi.build()), "..", "include", "pi.h")).read()
     for field in ("gather_ctas", "pool_slots_per_req", "cpu_gather_ms", "host_region_bytes"):
         assert field in hdr
-    assert ctypes.sizeof(_lib.pi_config) == 17 * 4 + 4 + 8
+    assert ctypes.sizeof(_lib.pi_config) == 18 * 4 + 8
     assert ctypes.sizeof(_lib.pi_recall_stats) == 5 * 8 + 2 * 8

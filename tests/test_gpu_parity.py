@@ -78,11 +78,12 @@ def check_tables_maps_bytes(pool, om, w, l, sels, tables, table_dev):
             want_t = tables[r] if U == 1 else tables[r][u]
             got = tab[r * U + u, : len(want_t)]
             assert np.array_equal(got, want_t), (r, u, got, want_t)
+            n_slots = len(om.bos[(r, l, u)])
             assert np.array_equal(sob[r, l, u], om.sob[(r, l, u)]), (r, l, u)
-            assert np.array_equal(bos[r, l, u, : om.P[r]], om.bos[(r, l, u)]), (r, l, u)
+            assert np.array_equal(bos[r, l, u, :n_slots], om.bos[(r, l, u)]), (r, l, u)
             if w.evict_policy == 1:
                 st = pool.view_slot_stamp().cpu().numpy()
-                assert np.array_equal(st[r, l, u, : om.P[r]], om.stamp[(r, l, u)]), (r, l, u)
+                assert np.array_equal(st[r, l, u, :n_slots], om.stamp[(r, l, u)]), (r, l, u)
             s_list = sels[r] if U == 1 else sels[r][u]
             reg = om.reg[(w.host_layer(l), r)]
             for i, b in enumerate(s_list):
@@ -645,3 +646,95 @@ def test_schedule_arguments():
                              method=pi.PI_RECALL_MEMCPY)
         assert ei.value.status == pi.PI_ERR_INVALID
         pool.set_schedule(False, 1)
+
+
+@pytest.mark.parametrize("evict", [0, 1])
+def test_headwise_pool_through_the_decode_step(evict):
+    """The per-KV-head arm through pi_decode_step: per-head selections, fragment
+    recall into per-head sub-slots and per-head attention, 3 pipelined steps with
+    appends, checked against the oracle every layer and step."""
+    w = Workload(layers=2, batch=2, hq=16, hkv=4, head_dim=128, block_tokens=32, ntok=[2000, 1500], k=6, window=2,
+                 pool_slots=10, steps=3, seed=67, select_mode=1, evict_policy=evict, heavy_frac=0.05)
+    L, R = w.layers, w.batch
+    with make_pool(w) as pool:
+        prefill(pool, w)
+        om = OracleModel(w)
+        qs = queries(w)
+        for step in range(w.steps):
+            kn, vn = new_tokens(w, step)
+            kbud = np.full((L, R), w.k, dtype=np.int32)
+            out = torch.empty((L, R, w.hq, w.head_dim), dtype=torch.int16, device="cuda")
+            lse = torch.empty((L, R, w.hq), dtype=torch.float32, device="cuda")
+            pool.decode_step(dev(qs[step]), dev(kn), dev(vn), dev(kbud), out, lse)
+            torch.cuda.synchronize()
+            assert pool.device_status() == pi.PI_OK
+            sel_v, nsel_v, tab_v = pool.view_step()
+            for l in range(L):
+                om.append(l, kn[l], vn[l])
+                ref_sel = om.select(l, qs[step][l], kbud[l])
+                check_selection(sel_v[l], nsel_v[l], ref_sel, om.U)
+                ref_tab = om.recall(l, ref_sel)
+                check_tables_maps_bytes(pool, om, w, l, ref_sel, ref_tab, tab_v[l])
+                ref_out, ref_lse, _ = om.attention(l, qs[step][l], ref_sel)
+                check_attention(out[l], lse[l], ref_out, ref_lse)
+
+
+@pytest.mark.parametrize("evict", [0, 1])
+def test_pinned_layers_and_admission(evict):
+    """IO-adaptive admission (guide, "2. IO-Adaptive Offloading Admission"): a
+    pinned layer keeps room for every block, so blocks once recalled stay; a
+    released layer drops what it held beyond P_r; every step matches the oracle
+    run with the same residency changes. Then the controller's decisions: pin in
+    the order 0, L-1, ... above 0.85 utilisation, release the last pinned below
+    0.5, nothing in between; layers without reserved room cannot be pinned."""
+    w = Workload(layers=3, batch=2, hq=32, hkv=8, head_dim=128, block_tokens=64, ntok=[3000, 2000], k=8, window=2,
+                 pool_slots=12, steps=4, rho=0.5, heavy_frac=0.05, seed=71, evict_policy=evict)
+    L, R = w.layers, w.batch
+    cap = max(w.pool_slots, w.max_blocks)
+    with make_pool(w, pin_layers=2) as pool:
+        prefill(pool, w)
+        om = OracleModel(w)
+        with pytest.raises(pi.PiError) as ei:
+            pool.pin_layer(1, True)
+        assert ei.value.status == pi.PI_ERR_INVALID
+        pool.pin_layer(0, True)
+        om.pin(0, cap)
+        assert pool.slots(0, 0) == cap and pool.slots(0, 1) == w.pool_slots
+        qs = queries(w)
+        held = [set() for _ in range(R)]
+        for step in range(w.steps):
+            if step == 2:
+                pool.pin_layer(0, False)
+                om.unpin(0)
+                pool.pin_layer(2, True)
+                om.pin(2, cap)
+            kn, vn = new_tokens(w, step)
+            kbud = np.full((L, R), w.k, dtype=np.int32)
+            out = torch.empty((L, R, w.hq, w.head_dim), dtype=torch.int16, device="cuda")
+            lse = torch.empty((L, R, w.hq), dtype=torch.float32, device="cuda")
+            pool.decode_step(dev(qs[step]), dev(kn), dev(vn), dev(kbud), out, lse)
+            torch.cuda.synchronize()
+            assert pool.device_status() == pi.PI_OK
+            sel_v, nsel_v, tab_v = pool.view_step()
+            for l in range(L):
+                om.append(l, kn[l], vn[l])
+                ref_sel = om.select(l, qs[step][l], kbud[l])
+                check_selection(sel_v[l], nsel_v[l], ref_sel, 1)
+                ref_tab = om.recall(l, ref_sel)
+                check_tables_maps_bytes(pool, om, w, l, ref_sel, ref_tab, tab_v[l])
+                ref_out, ref_lse, _ = om.attention(l, qs[step][l], ref_sel)
+                check_attention(out[l], lse[l], ref_out, ref_lse)
+            if step < 2:  # while pinned, layer 0 never lets a block go
+                sob = pool.view_slot_of_block().cpu().numpy()
+                for r in range(R):
+                    now = set(np.nonzero(sob[r, 0, 0] >= 0)[0].tolist())
+                    assert held[r] <= now
+                    held[r] = now
+        # controller decisions (layer 2 pinned, layer 0 released at this point)
+        assert pool.admission(0.90) == (0, True)
+        assert pool.admission(0.95) == (-1, False)   # 0 and 2 pinned, 1 has no room
+        assert pool.admission(0.70) == (-1, False)
+        assert pool.admission(0.30) == (0, False)    # the last pinned goes first
+        assert pool.admission(0.30) == (2, False)
+        assert pool.admission(0.10) == (-1, False)
+        assert pool.slots(1, 2) == w.pool_slots

@@ -562,3 +562,44 @@ def test_consensus_score_close_to_fp64_formula_on_gaussian_inputs():
             tot += s_h.max() + 0.5 * s_h.mean()
         got = oracle.consensus_score(q, km[b], 0.5)
         assert abs(got - tot) <= 1e-4 * (1.0 + np.abs(qf).sum() * 0.1)
+
+
+# ------------------------------------------------------------------ pinned-layer plan
+def test_pinned_plan_takes_empty_slots_first_hand_example():
+    """Slots [7, -, 3, -, 9], selection {3, 4, 5}: the lowest-free-slot rule puts 4
+    in slot 0 (evicting 7) and 5 in slot 1; a layer held whole in HBM puts them in
+    the empty slots 1 and 3 and evicts nothing."""
+    def maps():
+        bos = np.array([7, -1, 3, -1, 9], dtype=np.int32)
+        sob = np.full(12, -1, dtype=np.int32)
+        for s, b in enumerate(bos):
+            if b >= 0:
+                sob[b] = s
+        return sob, bos
+    sel = np.array([3, 4, 5], dtype=np.int32)
+    sob, bos = maps()
+    t, mb, ms, ev = oracle.recall_plan(sel, sob, bos)
+    assert list(mb) == [4, 5] and list(ms) == [0, 1] and list(ev) == [7, -1] and list(t) == [2, 0, 1]
+    sob, bos = maps()
+    t, mb, ms, ev = oracle.recall_plan(sel, sob, bos, empty_first=True)
+    assert list(mb) == [4, 5] and list(ms) == [1, 3] and list(ev) == [-1, -1] and list(t) == [2, 1, 3]
+    assert list(bos) == [7, 4, 3, 5, 9] and sob[7] == 0 and sob[9] == 4
+
+
+def test_pinned_plan_never_evicts_while_room_is_left():
+    """Random selections over a layer with room for every block: a block, once
+    placed, stays; the table maps every selected block to its slot."""
+    rng = np.random.default_rng(3)
+    nb, P = 60, 60
+    sob = np.full(nb, -1, dtype=np.int32)
+    bos = np.full(P, -1, dtype=np.int32)
+    placed = {}
+    for _ in range(40):
+        sel = np.sort(rng.choice(nb, size=9, replace=False)).astype(np.int32)
+        t, mb, ms, ev = oracle.recall_plan(sel, sob, bos, empty_first=True)
+        assert np.all(ev == -1)
+        for b, s in zip(mb, ms):
+            placed[int(b)] = int(s)
+        for b, s in placed.items():
+            assert sob[b] == s and bos[s] == b
+        assert np.array_equal(t, sob[sel])
