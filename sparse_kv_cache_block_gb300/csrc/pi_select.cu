@@ -168,7 +168,6 @@ struct SelParams {
   int u0;                // first unit of this launch (grid.y covers u0 ..)
   int consensus;         // rank blocks by the consensus score (shared selection only)
   float lambda;          // its weight on the group mean
-  int P2;                // the smallest power of two >= G
   int ring_stages;       // consensus: bulk-copy stages of 8 blocks' summaries
   int dyn_plan_off;      // bytes of dynamic shared memory before the plan scratch (consensus: ring + c_g)
   int empty_first;       // the layer is held whole in HBM
@@ -310,7 +309,8 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelParams p) {
   const int ncand = max(0, nb - p.W);
 
   // qsum[e] = sum over the group's query heads (ascending) of q[h][d], fp32
-  for (int e = threadIdx.x; e < E; e += kSelThreads) {
+  // (the mean-key score; the consensus ranking reads the heads one by one)
+  for (int e = threadIdx.x; e < E && !p.consensus; e += kSelThreads) {
     const int gg = (p.U == 1) ? e / p.D : g;
     const int d = e % p.D;
     const uint16_t* qh = p.q + ((size_t)r * p.Hq + (size_t)gg * p.G) * p.D + d;
@@ -761,8 +761,6 @@ cudaError_t pi_launch_select(pi_pool* p, int layer, const void* q, const int* k_
   sp.consensus = (mode == PI_CONSENSUS) ? 1 : 0;
   sp.empty_first = p->pinned_h.empty() ? 0 : p->pinned_h[layer];
   sp.lambda = p->consensus_lambda;
-  sp.P2 = 1;
-  while (sp.P2 < p->G) sp.P2 <<= 1;
   sp.ring_stages = 0;
   sp.dyn_plan_off = 0;
   if (sp.consensus) {
