@@ -1,14 +1,18 @@
-// Layer-wise two-stream decode step.
+// Layer-wise decode step.
 //
 // "PulseInfer Guide: I/O-Centric Sparse KV Cache Offloading", section
 // "Interruptible Layer-Wise Scheduling", and the PulseInfer abstract: recall of
 // one layer's blocks runs while the GPU computes another layer, so variable
-// recall latency hides behind compute. Here the compute stream runs append,
-// selection and attention, the copy stream runs the recall (plan + gather), and
-// events order them: recall(l) waits for select(l); attention(l) waits for
-// recall(l). Selections are issued ahead of attention (one layer, or all layers
-// first), so recall(l+1) overlaps attention(l). With the UVA gather arm no step
-// needs the host.
+// recall latency hides behind compute. Three shapes, all ordered by events only:
+//  - default: the compute stream runs append and selection (+ plan) of every
+//    layer in turn, the copy stream the gathers, a pool-owned stream the
+//    attention; recall(l) waits for select(l), attention(l) for recall(l);
+//  - two streams: attention on the compute stream, selection select_ahead
+//    layers in front of it;
+//  - dependent queries: per request group, append, selection, recall and
+//    attention of layer after layer on the group's stream, the groups' recalls
+//    taking turns on the copy stream.
+// With the UVA gather arm no step needs the host.
 #include <cstring>
 #include <vector>
 
