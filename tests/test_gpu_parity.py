@@ -738,3 +738,17 @@ def test_pinned_layers_and_admission(evict):
         assert pool.admission(0.30) == (2, False)
         assert pool.admission(0.10) == (-1, False)
         assert pool.slots(1, 2) == w.pool_slots
+
+
+@pytest.mark.parametrize("mode", [pi.PI_SHARED, pi.PI_CONSENSUS], ids=["shared", "consensus"])
+def test_large_selection_sizes(mode):
+    """Beyond the register-resident fast paths: 4 375 candidate blocks (more than
+    the 4 096 a selection CTA keeps in registers, so keys are read from the score
+    buffer), a budget of 1 100 blocks (more than the 512 one attention CTA takes,
+    so at least three splits), a second request with a budget of 300."""
+    w = Workload(layers=1, batch=2, hq=8, hkv=2, head_dim=64, block_tokens=16, ntok=[70000, 33000], k=1100, window=4,
+                 pool_slots=1104, steps=1, seed=73, select_mode=mode)
+    with make_pool(w) as pool:
+        prefill(pool, w)
+        om = OracleModel(w)
+        run_layer(pool, om, w, 0, queries(w)[0][0], [1100, 300], pi.PI_RECALL_UVA, logits=False)
