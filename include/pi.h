@@ -369,6 +369,14 @@ pi_status pi_pool_set_pipeline(pi_pool* p, int select_ahead, int attention_strea
  * PI_ERR_INVALID unless dependent is 0 or 1 and 1 <= groups <= min(8, batch). */
 pi_status pi_pool_set_schedule(pi_pool* p, int dependent, int groups);
 
+/* Copy streams of the UVA recall in pi_decode_step (default schedules): n = 2
+ * (the default) runs odd layers' gathers on a second stream the pool owns, so a
+ * gather's start overlaps the previous gather's tail (each still follows its
+ * layer's selection and precedes its attention; measured 6-8 % more tokens/s);
+ * n = 1 runs every gather on the caller's copy stream. Results are identical.
+ * Synchronizes the device. PI_ERR_INVALID unless n is 1 or 2. */
+pi_status pi_pool_set_copy_streams(pi_pool* p, int n);
+
 /* Split count of the attention kernel (CTAs per request and KV head; 0 = the
  * default: one wave at the kernel's occupancy). Clamped to what the pool's
  * scratch holds. Results change only by floating-point summation order. */
@@ -397,6 +405,8 @@ enum { PI_K_APPEND = 0, PI_K_SELECT = 1, PI_K_PLAN = 2, PI_K_GATHER = 3, PI_K_AT
 typedef struct pi_kernel_timing {
   long long launches;        /* kernels of this kind timed */
   double total_ms;           /* sum of their CUDA-event durations */
+  double busy_ms;            /* length of the union of their [start, end] intervals
+                                (less than total_ms when launches overlap) */
 } pi_kernel_timing;
 
 /* Enable per-kernel CUDA-event timing inside pi_decode_step for the next

@@ -198,6 +198,9 @@ class Pool:
         dep = dependent if isinstance(dependent, int) and not isinstance(dependent, bool) else int(bool(dependent))
         check(self.lib.pi_pool_set_schedule(self.h, dep, groups), "pi_pool_set_schedule")
 
+    def set_copy_streams(self, n: int):
+        check(self.lib.pi_pool_set_copy_streams(self.h, n), "pi_pool_set_copy_streams")
+
     def pin_layer(self, layer: int, pinned: bool = True):
         check(self.lib.pi_pool_pin_layer(self.h, layer, int(bool(pinned))), "pi_pool_pin_layer")
 
@@ -255,7 +258,7 @@ class Pool:
     def get_timing(self) -> dict:
         arr = (_lib.pi_kernel_timing * _lib.PI_K_KINDS)()
         check(self.lib.pi_pool_get_timing(self.h, arr), "pi_pool_get_timing")
-        return {name: {"launches": arr[i].launches, "total_ms": arr[i].total_ms}
+        return {name: {"launches": arr[i].launches, "total_ms": arr[i].total_ms, "busy_ms": arr[i].busy_ms}
                 for i, name in enumerate(_lib.KERNEL_KINDS)}
 
     def device_status(self) -> int:

@@ -52,7 +52,7 @@ class pi_pool_views(ctypes.Structure):
 
 
 class pi_kernel_timing(ctypes.Structure):
-    _fields_ = [("launches", c_ll), ("total_ms", c_double)]
+    _fields_ = [("launches", c_ll), ("total_ms", c_double), ("busy_ms", c_double)]
 
 
 PI_K_KINDS = 5
@@ -78,6 +78,7 @@ _SIGS = {
     "pi_pool_set_attention": (c_int, [_P, c_int]),
     "pi_pool_set_attention_cluster": (c_int, [_P, c_int]),
     "pi_pool_set_schedule": (c_int, [_P, c_int, c_int]),
+    "pi_pool_set_copy_streams": (c_int, [_P, c_int]),
     "pi_pool_pin_layer": (c_int, [_P, c_int, c_int]),
     "pi_pool_admission": (c_int, [_P, c_double, ctypes.POINTER(c_int), ctypes.POINTER(c_int)]),
     "pi_pool_set_consensus_lambda": (c_int, [_P, ctypes.c_float]),

@@ -122,6 +122,8 @@ struct pi_pool {
   // interruptible layer-wise scheduling: with dependent queries a request
   // group's selection of layer l+1 follows its attention of layer l; groups
   // interleave on the copy stream (group 0 on the caller's compute stream)
+  bool copy2_on = true;           // UVA gathers of odd layers on a second, pool-owned copy stream
+  cudaStream_t copy2 = nullptr;
   int sched_dependent = 0;
   int sched_groups = 1;
   cudaStream_t grp_stream[8] = {};

@@ -47,6 +47,7 @@ static void pool_free(pi_pool* p) {
   if (p->ev_start) cudaEventDestroy(p->ev_start);
   for (auto e : p->ev_att) cudaEventDestroy(e);
   if (p->attn_stream) cudaStreamDestroy(p->attn_stream);
+  if (p->copy2) cudaStreamDestroy(p->copy2);
   for (auto st : p->grp_stream)
     if (st) cudaStreamDestroy(st);
   for (auto e : p->grp_ev)
@@ -297,7 +298,8 @@ extern "C" pi_status pi_pool_create(const pi_config* cfg, pi_pool** out) {
       pool_free(p);
       return PI_ERR_CUDA;
     }
-  if (cudaStreamCreateWithFlags(&p->attn_stream, cudaStreamNonBlocking) != cudaSuccess) {
+  if (cudaStreamCreateWithFlags(&p->attn_stream, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaStreamCreateWithFlags(&p->copy2, cudaStreamNonBlocking) != cudaSuccess) {
     pool_free(p);
     return PI_ERR_CUDA;
   }

@@ -13,7 +13,9 @@
 //    attention of layer after layer on the group's stream, the groups' recalls
 //    taking turns on the copy stream.
 // With the UVA gather arm no step needs the host.
+#include <algorithm>
 #include <cstring>
+#include <utility>
 #include <vector>
 
 #include "pi_internal.cuh"
@@ -77,19 +79,24 @@ static pi_status step_impl(pi_pool* p, const uint8_t* q_all, const uint8_t* k_ne
     return PI_OK;
   };
 
+  // with two copy streams the UVA gathers of odd layers run on the pool's second
+  // one, so a gather's start overlaps the previous gather's tail
+  const bool two_copies = uva && p->copy2_on;
+  if (two_copies) PI_CUDA_TRY(cudaStreamWaitEvent(p->copy2, p->ev_start, 0));
   auto recall_layer = [&](int l) -> pi_status {
-    PI_CUDA_TRY(cudaStreamWaitEvent(ys, p->ev_sel[l], 0));
+    cudaStream_t rs = (two_copies && (l & 1)) ? p->copy2 : ys;
+    PI_CUDA_TRY(cudaStreamWaitEvent(rs, p->ev_sel[l], 0));
     if (uva) {
       p->recall_calls++;
       if (p->fault_recall_at > 0 && p->recall_calls == p->fault_recall_at) return PI_ERR_FAULT_INJECTED;
-      PI_TIMED(l, PI_K_GATHER, ys,
-               pi_launch_gather(p, l, nullptr, true, true, ys, append ? k_new_all + (size_t)l * kv_bytes : nullptr,
+      PI_TIMED(l, PI_K_GATHER, rs,
+               pi_launch_gather(p, l, nullptr, true, true, rs, append ? k_new_all + (size_t)l * kv_bytes : nullptr,
                                 append ? v_new_all + (size_t)l * kv_bytes : nullptr));
     } else {
-      pi_status s2 = pi_recall_impl(p, l, sel_of(l), nsel_of(l), method, tab_of(l), nullptr, ys);
+      pi_status s2 = pi_recall_impl(p, l, sel_of(l), nsel_of(l), method, tab_of(l), nullptr, rs);
       if (s2 != PI_OK) return s2;
     }
-    PI_CUDA_TRY(cudaEventRecord(p->ev_rec[l], ys));
+    PI_CUDA_TRY(cudaEventRecord(p->ev_rec[l], rs));
     return PI_OK;
   };
   auto attend_layer = [&](int l, cudaStream_t as) -> pi_status {
@@ -204,6 +211,7 @@ static pi_status step_impl(pi_pool* p, const uint8_t* q_all, const uint8_t* k_ne
     PI_CUDA_TRY(cudaStreamSynchronize(p->attn_stream));
     for (int g = 1; g < 8; g++)
       if (p->grp_stream[g]) PI_CUDA_TRY(cudaStreamSynchronize(p->grp_stream[g]));
+    if (p->copy2) PI_CUDA_TRY(cudaStreamSynchronize(p->copy2));
     PI_CUDA_TRY(cudaMemcpy(c.data(), p->recall_counts, sizeof(long long) * 4 * p->L, cudaMemcpyDeviceToHost));
     std::vector<int> ns((size_t)p->L * RU);
     PI_CUDA_TRY(cudaMemcpy(ns.data(), p->step_nsel, sizeof(int) * ns.size(), cudaMemcpyDeviceToHost));
@@ -282,18 +290,32 @@ extern "C" pi_status pi_pool_set_timing(pi_pool* p, int max_steps) {
 extern "C" pi_status pi_pool_get_timing(pi_pool* p, pi_kernel_timing* out) {
   if (!p || !out) return PI_ERR_INVALID;
   PI_CUDA_TRY(cudaDeviceSynchronize());
-  for (int k = 0; k < PI_K_KINDS; k++) out[k] = pi_kernel_timing{0, 0.0};
+  for (int k = 0; k < PI_K_KINDS; k++) out[k] = pi_kernel_timing{0, 0.0, 0.0};
+  std::vector<std::pair<double, double>> iv[PI_K_KINDS];
+  cudaEvent_t ref = nullptr;  // the first recorded start: the origin of every interval
   for (int s = 0; s < p->timing_used; s++)
     for (int lg = 0; lg < p->L * p->timing_groups; lg++)
       for (int k = 0; k < PI_K_KINDS; k++) {
         cudaEvent_t* ev = &p->tev[(((size_t)s * p->L * p->timing_groups + lg) * PI_K_KINDS + k) * 2];
-        float ms = 0.0f;
+        float ms = 0.0f, t0 = 0.0f;
         // a kind that did not run in this step leaves its pair unrecorded
         if (cudaEventQuery(ev[1]) != cudaSuccess) { cudaGetLastError(); continue; }
         if (cudaEventElapsedTime(&ms, ev[0], ev[1]) != cudaSuccess) { cudaGetLastError(); continue; }
+        if (!ref) ref = ev[0];
+        if (cudaEventElapsedTime(&t0, ref, ev[0]) != cudaSuccess) { cudaGetLastError(); continue; }
         out[k].launches++;
         out[k].total_ms += ms;
+        iv[k].push_back({(double)t0, (double)t0 + ms});
       }
+  for (int k = 0; k < PI_K_KINDS; k++) {
+    std::sort(iv[k].begin(), iv[k].end());
+    double end = -1e300;
+    for (const auto& x : iv[k]) {
+      const double a = std::max(x.first, end);
+      if (x.second > a) out[k].busy_ms += x.second - a;
+      end = std::max(end, x.second);
+    }
+  }
   p->timing_used = 0;
   return PI_OK;
 }
@@ -303,6 +325,14 @@ extern "C" pi_status pi_pool_set_pipeline(pi_pool* p, int select_ahead, int atte
   PI_CUDA_TRY(cudaDeviceSynchronize());  // no step of the old mode may still run
   p->select_ahead = select_ahead;
   p->attn_stream_on = attention_stream != 0;
+  return PI_OK;
+}
+
+extern "C" pi_status pi_pool_set_copy_streams(pi_pool* p, int n) {
+  if (!p || (n != 1 && n != 2)) return PI_ERR_INVALID;
+  PI_CUDA_TRY(cudaDeviceSynchronize());
+  if (n == 2 && !p->copy2) PI_CUDA_TRY(cudaStreamCreateWithFlags(&p->copy2, cudaStreamNonBlocking));
+  p->copy2_on = (n == 2);
   return PI_OK;
 }
 

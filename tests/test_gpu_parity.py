@@ -174,7 +174,8 @@ def test_small_config_layer_calls(method):
                           (pi.PI_RECALL_UVA, 0, 0, "default"), (pi.PI_RECALL_UVA, 1, 0, "default"),
                           (pi.PI_RECALL_UVA, 0, 1, "few"), (pi.PI_RECALL_UVA, 1, 1, "shared"),
                           (pi.PI_RECALL_UVA, 0, 1, "shared"), (pi.PI_RECALL_UVA, 0, -1, "default"),
-                          (pi.PI_RECALL_UVA, 1, -1, "default"), (pi.PI_RECALL_MEMCPY, 0, -1, "default")])
+                          (pi.PI_RECALL_UVA, 1, -1, "default"), (pi.PI_RECALL_MEMCPY, 0, -1, "default"),
+                          (pi.PI_RECALL_UVA, 0, -1, "one_copy"), (pi.PI_RECALL_UVA, 1, 1, "one_copy")])
 def test_multistep_pipeline_8b_shape(method, evict, ahead, placement):
     """Llama-3-8B-shaped heads (32 q / 8 KV, d 128, blocks of 64), 2 layers, 2
     requests with ragged tails, heavy-hitter blocks, AR(1) queries, 4 pipelined
@@ -189,6 +190,8 @@ def test_multistep_pipeline_8b_shape(method, evict, ahead, placement):
             pool.set_gather(5, 8, True)  # few exclusive CTAs: every CTA loops over many chunks
         elif placement == "shared":
             pool.set_gather(0, 8, False)  # one 256-thread CTA per SM beside other kernels
+        elif placement == "one_copy":
+            pool.set_copy_streams(1)  # every gather on the caller's copy stream (the default uses two)
         prefill(pool, w)
         om = OracleModel(w)
         qs = queries(w)
