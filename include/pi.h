@@ -426,7 +426,7 @@ pi_status pi_clear_device_status(pi_pool* p);
 /* Self-test of the bounded device wait every kernel uses: one thread waits on an
  * mbarrier phase that nothing completes, gives up after limit_cycles (clock64;
  * 1..2e9), records PI_ERR_TIMEOUT in the status word and exits. The context
- * stays usable. Synchronous; returns the status word's verdict. */
+ * stays usable. Synchronous; returns the status word it read. */
 pi_status pi_selftest_bounded_wait(pi_pool* p, long long limit_cycles);
 
 /* Host-side fault injection for tests: "recall_fail@N" or "" (off). The
