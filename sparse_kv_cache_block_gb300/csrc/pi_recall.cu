@@ -337,10 +337,13 @@ static cudaError_t launch_gather_d(int depth, int ctas, size_t smem, const Gathe
 // long-latency host-link reads stay on a few SMs and the other SMs' memory
 // requests never queue behind them (measured: attention in the decode step drops
 // from ~110 us to ~40-55 us per layer; the step runs 12 % faster).
-// Shared: 256-thread CTAs, one per SM, beside whatever else runs.
+// Shared: 256-thread CTAs, one per SM, beside whatever else runs. Copy units
+// under 32 KiB (one KV head's fragment of small blocks in the head-wise arm)
+// always take the shared shape: a 1024-thread CTA would leave most threads idle
+// on each unit (measured: 8 KiB fragments move 120 GB/s exclusive, 184 shared).
 static cudaError_t launch_gather(pi_pool* p, const GatherParams& g, cudaStream_t s) {
   size_t smem = sizeof(long long) * ((size_t)g.units + 1);
-  if (p->gather_exclusive) {
+  if (p->gather_exclusive && g.copy_bytes >= 32768) {
     const int ctas = p->cfg.gather_ctas > 0 ? p->cfg.gather_ctas : max(1, p->num_sms / 4);
     const size_t attn = (size_t)pi_attention_smem(p->D, p->B);
     const size_t sm_bytes = 228 * 1024, reserve = 1024;
