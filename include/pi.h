@@ -276,10 +276,12 @@ pi_status pi_pool_set_consensus_lambda(pi_pool* p, float lambda);
 
 /* Retune the UVA gather: grid size (CTAs; 0 = default), 16-byte loads in flight
  * per thread (2, 4, 8 or 16) and placement: exclusive = 1 (the default) runs
- * 1024-thread CTAs (default: a quarter of the SMs) that reserve enough shared
+ * 1024-thread CTAs (default: a quarter of the SMs, an eighth per gather when
+ * the decode step pairs gathers on two copy streams) that reserve enough shared
  * memory to keep attention CTAs off their SMs, so host-link reads stay on a few
  * SMs; exclusive = 0 runs 256-thread CTAs, one per SM, beside other kernels.
- * Applies to calls issued afterwards. */
+ * Copy units under 32 KiB always take the 256-thread shape. Applies to calls
+ * issued afterwards. */
 pi_status pi_pool_set_gather(pi_pool* p, int ctas, int depth, int exclusive);
 
 /* Forget residency of `layer` (-1 = all layers): every slot empty. Bytes stay. */

@@ -159,7 +159,7 @@ cudaError_t pi_launch_select(pi_pool* p, int layer, const void* q, const int* k_
 cudaError_t pi_launch_plan(pi_pool* p, int layer, const int* sel, const int* nsel, int* table, cudaStream_t s);
 cudaError_t pi_launch_gather(pi_pool* p, int layer, const uint8_t* stage_src, bool copy, bool commit,
                              cudaStream_t s, const void* k_new = nullptr, const void* v_new = nullptr, int r0 = 0,
-                             int nr = -1);
+                             int nr = -1, bool paired = false);
 cudaError_t pi_launch_attention(pi_pool* p, int layer, const void* q, const int* sel, const int* table,
                                 const int* nsel, void* out, float* lse, float* logits, cudaStream_t s, int r0 = 0,
                                 int nr = -1);

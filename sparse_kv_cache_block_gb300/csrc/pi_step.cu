@@ -91,7 +91,7 @@ static pi_status step_impl(pi_pool* p, const uint8_t* q_all, const uint8_t* k_ne
       if (p->fault_recall_at > 0 && p->recall_calls == p->fault_recall_at) return PI_ERR_FAULT_INJECTED;
       PI_TIMED(l, PI_K_GATHER, rs,
                pi_launch_gather(p, l, nullptr, true, true, rs, append ? k_new_all + (size_t)l * kv_bytes : nullptr,
-                                append ? v_new_all + (size_t)l * kv_bytes : nullptr));
+                                append ? v_new_all + (size_t)l * kv_bytes : nullptr, 0, -1, two_copies));
     } else {
       pi_status s2 = pi_recall_impl(p, l, sel_of(l), nsel_of(l), method, tab_of(l), nullptr, rs);
       if (s2 != PI_OK) return s2;
