@@ -755,3 +755,39 @@ def test_large_selection_sizes(mode):
         prefill(pool, w)
         om = OracleModel(w)
         run_layer(pool, om, w, 0, queries(w)[0][0], [1100, 300], pi.PI_RECALL_UVA, logits=False)
+
+
+@pytest.mark.parametrize("mode", [pi.PI_SHARED, pi.PI_CONSENSUS, pi.PI_HEADWISE], ids=["shared", "consensus", "headwise"])
+def test_features_together(mode):
+    """Dependent-query schedule with two request groups, a pinned layer, the
+    least-recently-selected rule and each ranking, three pipelined steps: every
+    layer and step against the oracle run with the same residency."""
+    w = Workload(layers=3, batch=3, hq=16, hkv=4, head_dim=128, block_tokens=32, ntok=[2500, 1800, 900], k=6,
+                 window=2, pool_slots=9, steps=3, rho=0.7, heavy_frac=0.05, seed=79, evict_policy=1,
+                 select_mode=mode)
+    L, R = w.layers, w.batch
+    cap = max(w.pool_slots, w.max_blocks)
+    with make_pool(w, pin_layers=1) as pool:
+        pool.set_schedule(True, 2)
+        prefill(pool, w)
+        om = OracleModel(w)
+        pool.pin_layer(0, True)
+        om.pin(0, cap)
+        qs = queries(w)
+        for step in range(w.steps):
+            kn, vn = new_tokens(w, step)
+            kbud = np.full((L, R), w.k, dtype=np.int32)
+            out = torch.empty((L, R, w.hq, w.head_dim), dtype=torch.int16, device="cuda")
+            lse = torch.empty((L, R, w.hq), dtype=torch.float32, device="cuda")
+            pool.decode_step(dev(qs[step]), dev(kn), dev(vn), dev(kbud), out, lse)
+            torch.cuda.synchronize()
+            assert pool.device_status() == pi.PI_OK
+            sel_v, nsel_v, tab_v = pool.view_step()
+            for l in range(L):
+                om.append(l, kn[l], vn[l])
+                ref_sel = om.select(l, qs[step][l], kbud[l])
+                check_selection(sel_v[l], nsel_v[l], ref_sel, om.U)
+                ref_tab = om.recall(l, ref_sel)
+                check_tables_maps_bytes(pool, om, w, l, ref_sel, ref_tab, tab_v[l])
+                ref_out, ref_lse, _ = om.attention(l, qs[step][l], ref_sel)
+                check_attention(out[l], lse[l], ref_out, ref_lse)
