@@ -665,7 +665,9 @@ def run_ours(args, cfg, rank, world, local_rank):
         "cpu_baseline": cpu,
         "cpu_baseline_all_cores": cpu_all,
         "e2e": e2e,
-        "gpu_launches": K * L * 5,
+        # kernels of the library per step, counted by the per-kernel timing of pass B
+        # (same steps: append, selection with the fused plan, gather, attention per layer)
+        "gpu_launches": int(round(sum(timing[k_]["launches"] for k_ in KINDS) / max(K, 1))) * K,
         "clocks": clocks.summary(),
         "kernel_timing": "per-kernel CUDA events over a second run of K pipelined steps (pass B)",
         "pass_b_tok_s": world * R * K / pass_b_s,
