@@ -740,8 +740,10 @@ cudaError_t pi_launch_select(pi_pool* p, int layer, const void* q, const int* k_
   }
   const int ncand_max = max(0, nb_max - p->W);
   // enough CTAs to cover every SM twice, at least 8 blocks (one per warp) each
+  // (rounded down: one more chunk per unit would spill into a second wave)
   long long target = 2LL * p->num_sms;
-  int chunks = (int)max(1LL, (target + (long long)RU - 1) / (long long)RU);
+  const long long units_launch = (long long)nr * p->U;
+  int chunks = (int)max(1LL, target / units_launch);
   int bpc = (ncand_max + chunks - 1) / chunks;
   bpc = ((max(bpc, 8) + 7) / 8) * 8;
   chunks = max(1, (ncand_max + bpc - 1) / bpc);
