@@ -768,6 +768,98 @@ def run_fragmentation_sweep(args):
     return rows
 
 
+def run_mass_diagnostic(args):
+    """Attention mass each query head keeps under the shared, the consensus and
+    the per-KV-head selection at one budget (guide, "SoloHead Sparse Selection",
+    "2. High Attention Mass Preservation"), with the blocks each selection moves
+    and the mass kernel's host-link rate. Llama-3-8B shape at 32768 tokens
+    (batch 8, top-32 + 2 recent, 5 % heavy-hitter blocks shifted by 2 u_g), AR(1)
+    queries over a few steps, two query recipes: "random" (the benchmark's own
+    queries: attention close to uniform) and "aligned" (each head's query plus
+    1.5 sqrt(D) u_g, its group's heavy-hitter direction, so that every head
+    attends to the heavy blocks: the premise the guide states for SoloHead).
+    Synthetic keys: the comparison between the rankings is the result, not the
+    absolute mass. One JSON line."""
+    import torch
+
+    import synth
+    import sparse_kv_cache_block_gb300 as pi
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    pi.build()
+    pi.load()
+    L = args.layers or 2
+    R = args.batch or 8
+    Hq, Hkv, D, B, N, k, W, steps = 32, 8, 128, 64, 32768, 32, 2, 4
+    G, nb, cap = Hq // Hkv, N // B, k + W
+    qs = synth.q_ar1(args.seed, L, R, Hq, D, steps, 0.9)
+    qa = synth.bf16_to_f32(qs).astype(np.float64)
+    for l in range(L):
+        for r in range(R):
+            for g in range(Hkv):
+                qa[:, l, r, g * G:(g + 1) * G] += 1.5 * math.sqrt(D) * synth.direction(args.seed, l, r, g, D)
+    recipes = {"random": qs, "aligned": synth.f32_to_bf16(qa.astype(np.float32))}
+    kb = torch.full((R,), k, dtype=torch.int32, device=dev)
+    pools = {}
+    for name, mode in (("one_set", pi.PI_SHARED), ("headwise", pi.PI_HEADWISE)):
+        pool = pi.Pool(L, R, Hq, Hkv, D, B, nb + 1, cap, k, W, select_mode=mode)
+        for l in range(L):
+            for r in range(R):
+                synth.fill_kv(pool.host_kv_ptr(l, r), args.seed, l, r, N, nb + 1, Hkv, B, D, 0.05, 2.0)
+            pool.update_summaries(l, [N] * R)
+        pools[name] = pool
+    torch.cuda.synchronize()
+    rankings = (("shared", "one_set", pi.PI_SHARED, 1), ("consensus", "one_set", pi.PI_CONSENSUS, 1),
+                ("headwise", "headwise", pi.PI_HEADWISE, Hkv))
+    mass_ms = []
+    out = {}
+    for recipe, qbits in recipes.items():
+        q_d = torch.from_numpy(np.ascontiguousarray(qbits).view(np.int16)).to(dev)
+        masses = {name: [] for name, *_ in rankings}
+        union_blocks = []
+        for st in range(steps):
+            for l in range(L):
+                for name, pname, mode, U in rankings:
+                    pool = pools[pname]
+                    sel = torch.empty((R * U, cap), dtype=torch.int32, device=dev)
+                    nsel = torch.empty((R * U,), dtype=torch.int32, device=dev)
+                    mass = torch.empty((R, Hq), dtype=torch.float32, device=dev)
+                    pool.select_topk(l, q_d[st, l], kb, sel, nsel, mode=mode)
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record()
+                    pool.attention_mass(l, q_d[st, l], sel, nsel, mass, per_head=U > 1)
+                    e1.record()
+                    e1.synchronize()
+                    mass_ms.append(e0.elapsed_time(e1))
+                    masses[name].append(mass.cpu().numpy())
+                    if U > 1:
+                        sh, nh = sel.cpu().numpy().reshape(R, U, cap), nsel.cpu().numpy().reshape(R, U)
+                        for r in range(R):
+                            union_blocks.append(len(set(int(b) for g in range(U) for b in sh[r, g, :nh[r, g]])))
+        stats = {}
+        for name in masses:
+            m = np.stack(masses[name])
+            stats[name] = {"mean": float(m.mean()), "min": float(m.min()), "p01": float(np.quantile(m, 0.01))}
+        out[recipe] = {"mass": stats,
+                       "shared_over_headwise": stats["shared"]["mean"] / stats["headwise"]["mean"],
+                       "consensus_over_headwise": stats["consensus"]["mean"] / stats["headwise"]["mean"],
+                       "headwise_union_blocks": float(np.mean(union_blocks)),
+                       "whole_block_volume_saved_vs_headwise_union": 1.0 - cap / float(np.mean(union_blocks))}
+    for pool in pools.values():
+        assert pool.device_status() == pi.PI_OK
+        pool.close()
+    mass_bytes = R * Hkv * N * D * 2
+    warm = mass_ms[len(rankings):]  # the first calls allocate scratch and warm the mapping
+    row = {"diagnostic": "attention_mass", "workload": "llama3-8b-shape", "layers": L, "batch": R, "context": N,
+           "block_tokens": B, "k": k, "window": W, "steps": steps, "heavy_frac": 0.05, "data": "synthetic",
+           "uniform_share": cap / nb, "shared_blocks": cap, "headwise_fragments": cap * Hkv, "recipes": out,
+           "mass_kernel": {"bytes_per_call": mass_bytes, "ms_per_call": float(np.median(warm)),
+                           "host_link_gbs": mass_bytes / (float(np.median(warm)) / 1e3) / 1e9}}
+    print(json.dumps(row), flush=True)
+    return row
+
+
 def run_reference(args, cfg):
     """The CPU oracle as it stands, on a bounded sample of the workload per step."""
     import synth
@@ -848,8 +940,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (small profiling cases)")
     ap.add_argument("--batch", type=int, default=0, help="override the batch (small profiling cases)")
-    ap.add_argument("--sweep", default="", choices=["", "fragmentation"],
-                    help="fragmentation: block-size sweep of shared vs head-wise recall (not the headline line)")
+    ap.add_argument("--sweep", default="", choices=["", "fragmentation", "mass"],
+                    help="fragmentation: block-size sweep of shared vs head-wise recall; mass: attention mass "
+                         "kept by each ranking (neither is the headline line)")
     ap.add_argument("--sweep-blocks", default="16,32,64,128")
     ap.add_argument("--sweep-methods", default="uva,memcpy,staged")
     ap.add_argument("--sweep-host-layers", type=int, default=2)
@@ -870,6 +963,9 @@ def main():
     if args.sweep == "fragmentation":
         rows = run_fragmentation_sweep(args)
         print(json.dumps({"sweep": "fragmentation", "rows": len(rows)}), flush=True)
+        return
+    if args.sweep == "mass":
+        run_mass_diagnostic(args)
         return
     if args.impl == "reference":
         if rank == 0:

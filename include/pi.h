@@ -327,6 +327,28 @@ pi_status pi_sparse_decode_noalloc(const void* kv_slots, long long n_slots, int 
                                    const int* slot_table, const int* nsel, const int* ntok, void* out, float* lse,
                                    pi_stream s);
 
+/* Attention mass a block selection keeps: a diagnostic, off the decode path.
+ * For request r and query head h (group g = h / G), with z_t = q_h . K_t /
+ * sqrt(D) over all ntok tokens t of (r, layer):
+ *   mass[r][h] = sum over t in a selected block of exp(z_t) / sum over all t of exp(z_t),
+ * the share of h's full softmax attention that the selection keeps. per_head = 0:
+ * sel [R][cap], nsel [R] (one set per request: PI_SHARED / PI_CONSENSUS);
+ * per_head = 1: sel [R][Hkv][cap], nsel [R][Hkv] (head h uses its group's set).
+ * Independent of the pool's select_mode, so selections from pools of either kind
+ * over the same tokens can be compared. A block listed twice counts once.
+ * K is read from the host store through the mapping, so the whole context of
+ * the layer crosses the host link (Hkv*ntok*D*2 bytes per request). Logits and
+ * sums in fp32, combined per chunk of tokens by a log-sum-exp merge in a fixed
+ * order (deterministic). mass = 0 where ntok = 0. q, sel, nsel, mass: device.
+ * A selected index outside [0, nb) is skipped and flags PI_ERR_DEVICE. The first
+ * call allocates the pool's scratch for it (a synchronizing cudaMalloc).
+ * Source: PulseInfer Guide, "SoloHead Sparse Selection", "2. High Attention Mass
+ * Preservation" (the shared set keeps nearly the attention mass that independent
+ * per-head sets keep while moving fewer bytes).
+ * Errors: PI_ERR_INVALID, PI_ERR_OOM, PI_ERR_CUDA. */
+pi_status pi_attention_mass(pi_pool* p, int layer, const void* q, const int* sel, const int* nsel, int per_head,
+                            float* mass, pi_stream s);
+
 /* ------------------------------------------------------------------ a-6 pipeline */
 /* One decode step over all layers with the recall of layer l+1 overlapped with
  * attention of layer l: compute stream runs append, select and attention; the

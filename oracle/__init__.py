@@ -21,6 +21,9 @@ What each function follows (page title, section):
 * attention: textbook scaled dot-product attention restricted to the tokens of
   the selected blocks, in fp64 (the guide's "PulseInfer Architectural
   Foundations": attention runs over the recalled pool blocks).
+* attention mass kept by a selection (a diagnostic): same guide, "SoloHead
+  Sparse Selection", "2. High Attention Mass Preservation"; fp64 dense softmax
+  over the whole context, summed over the selected blocks' tokens.
 
 Parity pins (tests/test_oracle_pins.py) tie every function to something other
 than itself: brute force, closed forms, invariants and the worked example of
@@ -313,6 +316,38 @@ def dense_attention_fp64(q: np.ndarray, K: np.ndarray, V: np.ndarray) -> tuple[n
         out[h] = (p @ V[g]) / p.sum()
         lse[h] = m + math.log(p.sum())
     return out, lse
+
+
+def attention_mass(q: np.ndarray, region: np.ndarray, sel, ntok: int, hkv: int) -> np.ndarray:
+    """Share of each query head's full attention that a block selection keeps, fp64.
+
+    Guide, "SoloHead Sparse Selection", "2. High Attention Mass Preservation": a
+    selection is judged by the softmax weight its blocks hold. Definition written
+    out: for head h (KV group g = h // G), z_t = q_h . K_t / sqrt(D) over every
+    valid token t of the context, p = softmax(z), mass[h] = sum of p_t over the
+    tokens of the selected blocks. q [Hq][D] bf16 bits; region [max_blocks][Hkv][2][B][D]
+    bf16 bits; sel one array of block ids (shared by all heads) or a list of Hkv
+    arrays (head h uses sel[h // G]); a repeated id counts once. No tokens: 0."""
+    qf = bf16_to_f64(_c(q, np.uint16))
+    region = _c(region, np.uint16)
+    hq, D = qf.shape
+    B = region.shape[3]
+    G = hq // hkv
+    mass = np.zeros(hq)
+    if ntok <= 0:
+        return mass
+    nb = -(-ntok // B)
+    per_head = isinstance(sel, (list, tuple))
+    for h in range(hq):
+        g = h // G
+        K = bf16_to_f64(region[:nb, g, 0]).reshape(nb * B, D)[:ntok]
+        z = K @ qf[h] / math.sqrt(D)
+        p = np.exp(z - z.max())
+        member = np.zeros(ntok, dtype=bool)
+        for b in set(int(x) for x in (sel[g] if per_head else sel)):
+            member[b * B:min(ntok, (b + 1) * B)] = True
+        mass[h] = p[member].sum() / p.sum()
+    return mass
 
 
 def union_fragments(per_head_sets) -> int:

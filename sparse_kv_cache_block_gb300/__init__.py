@@ -233,6 +233,11 @@ class Pool:
         check(self.lib.pi_sparse_decode(self.h, layer, _ptr(q), _ptr(sel), _ptr(table), _ptr(nsel), _ptr(out),
                                         _ptr(lse), _ptr(logits), _stream(stream)), "pi_sparse_decode")
 
+    def attention_mass(self, layer: int, q, sel, nsel, mass, per_head: bool = False, stream=None):
+        """Share of each head's full attention that the selection keeps: mass [R][Hq] fp32."""
+        check(self.lib.pi_attention_mass(self.h, layer, _ptr(q), _ptr(sel), _ptr(nsel), int(bool(per_head)),
+                                         _ptr(mass), _stream(stream)), "pi_attention_mass")
+
     def decode_step(self, q_all, k_new_all, v_new_all, k_budget, out_all, lse_all=None, method: int = PI_RECALL_UVA,
                     compute=None, copy=None, stats: bool = False):
         st = pi_step_stats() if stats else None

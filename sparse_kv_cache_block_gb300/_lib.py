@@ -84,6 +84,7 @@ _SIGS = {
     "pi_pool_set_consensus_lambda": (c_int, [_P, ctypes.c_float]),
     "pi_pool_set_evict": (c_int, [_P, c_int]),
     "pi_sparse_decode": (c_int, [_P, c_int, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "pi_attention_mass": (c_int, [_P, c_int, _P, _P, _P, c_int, _P, _P]),
     "pi_sparse_decode_noalloc": (c_int, [_P, c_ll, c_int, c_int, c_int, c_int, c_int, c_int, _P, _P, _P, _P, _P,
                                          _P, _P, _P]),
     "pi_decode_step": (c_int, [_P, _P, _P, _P, _P, c_int, _P, _P, _P, _P, ctypes.POINTER(pi_step_stats)]),

@@ -15,7 +15,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OBJDIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpi.so")
-SOURCES = ["pi_pool.cu", "pi_select.cu", "pi_recall.cu", "pi_attention.cu", "pi_step.cu"]
+SOURCES = ["pi_pool.cu", "pi_select.cu", "pi_recall.cu", "pi_attention.cu", "pi_step.cu", "pi_mass.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fopenmp", "-I" + os.path.join(ROOT, "include")]
 

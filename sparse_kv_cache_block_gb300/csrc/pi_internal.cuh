@@ -135,6 +135,9 @@ struct pi_pool {
   bool attn_cluster = true;       // splits 2..8 of a unit merge through DSMEM in a cluster
   int attn_splits = 0;            // attention split count override (0 = one wave at full occupancy)
 
+  // attention-mass diagnostic: per-chunk partials [L][R][Hq][kMassChunksMax], allocated on first use
+  float4* mass_part = nullptr;
+
   // fault injection
   long long fault_recall_at = 0;
   long long recall_calls = 0;

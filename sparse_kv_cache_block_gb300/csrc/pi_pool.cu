@@ -59,7 +59,7 @@ static void pool_free(pi_pool* p) {
                       p->slot_of,    p->block_of,   p->dev_status, p->sel_scores,  p->sel_counter, p->plan_n,
                       p->plan,       p->recall_counts, p->attn_o,  p->attn_ml,     p->attn_counter, p->step_sel,
                       p->step_nsel,  p->step_table, p->step_in,    p->step_out,    p->stage_dev,
-                      p->ntok_stage, p->slot_stamp, p->epoch};
+                      p->ntok_stage, p->slot_stamp, p->epoch,      p->mass_part};
   for (void* d : dev_ptrs)
     if (d) cudaFree(d);
   if (p->host) {

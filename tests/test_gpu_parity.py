@@ -791,3 +791,82 @@ def test_features_together(mode):
                 check_tables_maps_bytes(pool, om, w, l, ref_sel, ref_tab, tab_v[l])
                 ref_out, ref_lse, _ = om.attention(l, qs[step][l], ref_sel)
                 check_attention(out[l], lse[l], ref_out, ref_lse)
+
+
+MASS_ATOL = 1e-4   # fp32 logits (128 fused products) and fp32 sums over <= 32768 tokens per head
+
+
+def _mass_case(w, l, kreq, sel=None, nsel=None, expect_status=pi.PI_OK):
+    """Select (or take the given selection), then the attention mass of every head
+    on the GPU against the fp64 oracle."""
+    R, U, cap = w.batch, (w.hkv if w.select_mode == pi.PI_HEADWISE else 1), w.k + w.window
+    with make_pool(w) as pool:
+        prefill(pool, w)
+        om = OracleModel(w)
+        q = queries(w)[0][l]
+        if sel is None:
+            sel_d = torch.full((R * U, cap), -7, dtype=torch.int32, device="cuda")
+            nsel_d = torch.full((R * U,), -7, dtype=torch.int32, device="cuda")
+            pool.select_topk(l, dev(q), dev(np.asarray(kreq, dtype=np.int32)), sel_d, nsel_d)
+            ref_sel = om.select(l, q, kreq)
+            check_selection(sel_d, nsel_d, ref_sel, U)
+        else:
+            sel_d, nsel_d = dev(sel), dev(nsel)
+            ref_sel = [[sel[r * U + g, :nsel[r * U + g]] for g in range(U)] if U > 1 else sel[r, :nsel[r]]
+                       for r in range(R)]
+        mass = torch.full((R, w.hq), float("nan"), dtype=torch.float32, device="cuda")
+        pool.attention_mass(l, dev(q), sel_d, nsel_d, mass, per_head=U > 1)
+        torch.cuda.synchronize()
+        assert pool.device_status() == expect_status
+        got = mass.cpu().numpy()
+        for r in range(R):
+            want = oracle.attention_mass(q[r], om.reg[(w.host_layer(l), r)], ref_sel[r], w.ntok[r], w.hkv)
+            assert np.max(np.abs(got[r] - want)) <= MASS_ATOL, (r, got[r], want)
+        return got
+
+
+@pytest.mark.parametrize("mode", [pi.PI_SHARED, pi.PI_CONSENSUS, pi.PI_HEADWISE], ids=["shared", "consensus", "headwise"])
+@pytest.mark.parametrize("hq,hkv,D,B", [(32, 8, 128, 64), (8, 2, 64, 16), (64, 8, 128, 64), (12, 3, 64, 32)],
+                         ids=["8B", "C1_shape", "70B_G8", "G4_odd_hkv"])
+def test_attention_mass_matches_oracle(mode, hq, hkv, D, B):
+    """Attention mass each head keeps under the library's own selection (guide,
+    "SoloHead Sparse Selection", "2. High Attention Mass Preservation"): GPU fp32
+    against the fp64 oracle within MASS_ATOL; ragged tails, a one-block request,
+    the second layer of an aliased host store."""
+    w = Workload(layers=2, batch=3, hq=hq, hkv=hkv, head_dim=D, block_tokens=B, ntok=[5000, 2500, 40], k=12,
+                 window=2, pool_slots=16, seed=61 + hq + D, heavy_frac=0.05, select_mode=mode, host_layers=1)
+    _mass_case(w, 1, [w.k, 5, 3])
+
+
+def test_attention_mass_degenerate_selections():
+    """Every block -> 1; nothing -> 0; a repeated id counts once; one id past the
+    context is skipped and flagged in the status word, not read."""
+    w = Workload(layers=1, batch=3, hq=8, hkv=2, head_dim=64, block_tokens=16, ntok=[1000, 300, 37], k=70,
+                 window=0, pool_slots=70, seed=62)
+    cap = w.k
+    sel = np.full((3, cap), -1, dtype=np.int32)
+    nsel = np.array([63, 0, 4], dtype=np.int32)
+    sel[0, :63] = np.arange(63)
+    sel[2, :4] = [1, 1, 2, 0]
+    got = _mass_case(w, 0, None, sel, nsel)
+    assert np.all(np.abs(got[0] - 1.0) <= MASS_ATOL) and np.all(got[1] == 0.0)
+    sel[2, :4] = [1, 1, 2, 9]     # request 2 holds 3 blocks: block 9 is past its context
+    with make_pool(w) as pool:
+        prefill(pool, w)
+        q = queries(w)[0][0]
+        mass = torch.empty((3, w.hq), dtype=torch.float32, device="cuda")
+        pool.attention_mass(0, dev(q), dev(sel), dev(nsel), mass)
+        torch.cuda.synchronize()
+        assert pool.device_status() == pi.PI_ERR_DEVICE
+        want = oracle.attention_mass(q[2], synth.kv_region(w.seed, 0, 2, 37, w.max_blocks, 2, 16, 64),
+                                     np.array([1, 2]),
+                                     37, w.hkv)
+        assert np.max(np.abs(mass[2].cpu().numpy() - want)) <= MASS_ATOL
+
+
+def test_attention_mass_full_context_8b_shape():
+    """Two requests of the Llama-3-8B shape at 32768 tokens (512 blocks, top-32 +
+    2): every head against the oracle, shared selection."""
+    w = Workload(layers=1, batch=2, hq=32, hkv=8, head_dim=128, block_tokens=64, ntok=[32768, 32768], k=32,
+                 window=2, pool_slots=128, seed=63, heavy_frac=0.05)
+    _mass_case(w, 0, [32, 32])

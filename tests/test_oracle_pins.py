@@ -603,3 +603,82 @@ def test_pinned_plan_never_evicts_while_room_is_left():
         for b, s in placed.items():
             assert sob[b] == s and bos[s] == b
         assert np.array_equal(t, sob[sel])
+
+
+# ------------------------------------------------------------------ attention mass kept by a selection
+# Guide, "SoloHead Sparse Selection", "2. High Attention Mass Preservation".
+
+def test_mass_every_block_is_one_and_none_is_zero():
+    hq, hkv, B, D, ntok = 8, 2, 16, 64, 1000      # ragged tail: 63 blocks, 8 tokens in the last
+    reg = synth.kv_region(21, 0, 0, ntok, 64, hkv, B, D, 0.05, 2.0)
+    q = synth.normal_bf16(21, synth.KIND_MISC, 0, 0, hq * D).reshape(hq, D)
+    nb = -(-ntok // B)
+    m = oracle.attention_mass(q, reg, np.arange(nb), ntok, hkv)
+    assert np.all(np.abs(m - 1.0) < 1e-12)
+    assert np.all(oracle.attention_mass(q, reg, np.zeros(0, dtype=np.int32), ntok, hkv) == 0.0)
+    assert np.all(oracle.attention_mass(q, reg, np.arange(nb), 0, hkv) == 0.0)
+
+
+def test_mass_zero_query_is_the_token_share():
+    """q = 0: every logit is 0, the softmax is uniform, and a selection keeps
+    exactly its share of the valid tokens (the tail block counts its valid ones)."""
+    hq, hkv, B, D, ntok = 4, 2, 16, 64, 200      # 13 blocks; the tail (block 12) holds 8 tokens
+    reg = synth.kv_region(22, 0, 0, ntok, 13, hkv, B, D)
+    q = np.zeros((hq, D), dtype=np.uint16)
+    for sel, tokens in (([0, 5], 32), ([12], 8), ([3, 12, 3], 24), ([0, 1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11], 192)):
+        m = oracle.attention_mass(q, reg, np.array(sel, dtype=np.int32), ntok, hkv)
+        assert np.all(np.abs(m - tokens / ntok) < 1e-15), (sel, m)
+
+
+def test_mass_two_token_closed_form_and_gqa_mapping():
+    """Two tokens of one block each, head_dim 4, two KV groups of two heads.
+    Group 0 holds (c e0, 0), group 1 (0, c e0); every q_h = 2 e0, so the logits
+    are (c, 0) for heads 0, 1 and (0, c) for heads 2, 3 (scale 1/sqrt(4)). Block 0
+    keeps sigmoid(c) of heads 0, 1 and sigmoid(-c) of heads 2, 3: a wrong scale,
+    sign or head-to-group map changes one of the four values."""
+    hq, hkv, B, D, ntok = 4, 2, 1, 4, 2
+    reg = np.zeros((2, hkv, 2, B, D), dtype=np.uint16)
+    c = 1.5
+    reg[0, 0, 0, 0, 0] = bf16_bits([c])[0]
+    reg[1, 1, 0, 0, 0] = bf16_bits([c])[0]
+    q = np.zeros((hq, D), dtype=np.uint16)
+    q[:, 0] = bf16_bits([2.0])[0]
+    sig = 1.0 / (1.0 + math.exp(-c))
+    m = oracle.attention_mass(q, reg, np.array([0], dtype=np.int32), ntok, hkv)
+    assert np.allclose(m, [sig, sig, 1 - sig, 1 - sig], rtol=0, atol=1e-15)
+    # per-head sets: group 0 keeps block 1, group 1 keeps block 1
+    m = oracle.attention_mass(q, reg, [np.array([1]), np.array([1])], ntok, hkv)
+    assert np.allclose(m, [1 - sig, 1 - sig, sig, sig], rtol=0, atol=1e-15)
+
+
+def test_mass_is_additive_over_disjoint_selections():
+    hq, hkv, B, D, ntok = 8, 2, 16, 64, 700
+    reg = synth.kv_region(23, 0, 0, ntok, 44, hkv, B, D, 0.1, 2.0)
+    q = synth.normal_bf16(23, synth.KIND_MISC, 0, 0, hq * D).reshape(hq, D)
+    nb = -(-ntok // B)
+    rs = np.random.default_rng(23)
+    for _ in range(5):
+        perm = rs.permutation(nb)
+        s1, s2 = np.sort(perm[:10]), np.sort(perm[10:25])
+        m1 = oracle.attention_mass(q, reg, s1, ntok, hkv)
+        m2 = oracle.attention_mass(q, reg, s2, ntok, hkv)
+        m12 = oracle.attention_mass(q, reg, np.sort(np.concatenate([s1, s2])), ntok, hkv)
+        assert np.all(np.abs(m1 + m2 - m12) < 1e-12)
+        assert np.all((m1 > 0) & (m1 < 1) & (m12 >= m1))
+
+
+@pytest.mark.parametrize("ntok", [1000, 33])
+def test_mass_equals_sparse_over_dense_softmax_normaliser(ntok):
+    """log(mass) = lse over the selected tokens - lse over all tokens: the sparse
+    attention oracle (C, over the selection) against the independent numpy fp64
+    dense attention (over the whole context)."""
+    hq, hkv, B, D = 8, 2, 16, 64
+    nb = -(-ntok // B)
+    reg = synth.kv_region(24, 0, 0, ntok, nb + 1, hkv, B, D, 0.05, 2.0)
+    q = synth.normal_bf16(24, synth.KIND_MISC, 0, 0, hq * D).reshape(hq, D)
+    sel = np.array(sorted({0, nb - 1, nb // 2}), dtype=np.int32)
+    _, lse_sel, _ = oracle.attention(q, reg, sel, ntok, hkv)
+    K, V = _dense_inputs(reg, ntok, hkv, np.arange(nb))
+    _, lse_all = oracle.dense_attention_fp64(oracle.bf16_to_f64(q), K, V)
+    m = oracle.attention_mass(q, reg, sel, ntok, hkv)
+    assert np.allclose(np.log(m), lse_sel - lse_all, rtol=0, atol=1e-10)
