@@ -344,6 +344,8 @@ def run_ours(args, cfg, rank, world, local_rank):
     if args.schedule == "dependent":
         pool.set_schedule(True, args.groups)
     pool.set_copy_streams(args.copy_streams)
+    if args.fused:
+        pool.set_fused(True, args.fused_ctas)
     if args.select_ahead >= 0 or args.two_streams:
         pool.set_pipeline(max(args.select_ahead, 0) if args.select_ahead >= 0 else 1, not args.two_streams)
     if args.gather_placement == "shared" or args.gather_ctas or args.gather_depth:
@@ -647,6 +649,8 @@ def run_ours(args, cfg, rank, world, local_rank):
                    "streams": 2 if args.two_streams else 3,
                    "admission": admission,
                    "copy_streams": args.copy_streams,
+                   "select_gather": ((f"fused, {args.fused_ctas or 'a quarter of the SMs'} CTAs per launch")
+                                     if args.fused else "separate launches"),
                    "schedule": ("queries known up front, selections run ahead" if args.schedule == "ahead" else
                                 f"dependent queries, {args.groups} interleaved request group(s)"),
                    "gather_ctas": args.gather_ctas or "default",
@@ -922,6 +926,9 @@ def main():
     ap.add_argument("--schedule", default="ahead", choices=["ahead", "dependent"],
                     help="dependent: a request's selection of layer l+1 waits for its attention of layer l")
     ap.add_argument("--groups", type=int, default=2, help="request groups interleaved under --schedule dependent")
+    ap.add_argument("--fused", action="store_true",
+                    help="selection, plan and gather of a layer as one launch on the copy stream")
+    ap.add_argument("--fused-ctas", type=int, default=0, help="CTAs of a fused launch (0: a quarter of the SMs)")
     ap.add_argument("--copy-streams", type=int, default=2, choices=[1, 2],
                     help="2 (default): odd layers' gathers on a second copy stream; 1: one copy stream")
     ap.add_argument("--admission", action="store_true",

@@ -401,6 +401,26 @@ pi_status pi_pool_set_schedule(pi_pool* p, int dependent, int groups);
  * Synchronizes the device. PI_ERR_INVALID unless n is 1 or 2. */
 pi_status pi_pool_set_copy_streams(pi_pool* p, int n);
 
+/* Fused selection + recall (on = 1): in pi_decode_step with PI_RECALL_UVA, the
+ * selection, recall plan and gather of a layer (of a request group, under the
+ * dependent schedule) run as one launch of `ctas` CTAs on the copy stream (0 =
+ * a quarter of the SMs) instead of a selection on the compute stream and a
+ * gather on the copy stream. Its CTAs first claim selection items (a chunk of a
+ * unit's candidates) from a counter; the CTA that completes a unit's last chunk
+ * runs the unit's top-k and plan and publishes them through a flag; then every
+ * CTA copies its share of each unit's missing blocks once the unit's flag is
+ * set (bounded wait: PI_ERR_TIMEOUT in the status word, the unit skipped). A CTA
+ * waits only after every item has been taken by a running CTA, so the launch
+ * completes whatever the CTAs' residency. Results are identical to the unfused
+ * step. Under the dependent schedule each request group's launch runs on the
+ * group's stream (groups share the link instead of taking turns on the copy
+ * stream); launches over the same requests of one layer stay stream-ordered.
+ * Source: the guide's "The Gather-Scatter I/O Engine" (selected blocks gathered
+ * straight into pool slots); running the three steps as one launch is this
+ * library's design.
+ * Synchronizes the device. Errors: PI_ERR_INVALID. */
+pi_status pi_pool_set_fused(pi_pool* p, int on, int ctas);
+
 /* Split count of the attention kernel (CTAs per request and KV head; 0 = the
  * default: one wave at the kernel's occupancy). Clamped to what the pool's
  * scratch holds. Results change only by floating-point summation order. */

@@ -198,6 +198,10 @@ class Pool:
         dep = dependent if isinstance(dependent, int) and not isinstance(dependent, bool) else int(bool(dependent))
         check(self.lib.pi_pool_set_schedule(self.h, dep, groups), "pi_pool_set_schedule")
 
+    def set_fused(self, on: bool, ctas: int = 0):
+        """Selection, plan and gather of a layer as one launch in the decode step."""
+        check(self.lib.pi_pool_set_fused(self.h, int(bool(on)), ctas), "pi_pool_set_fused")
+
     def set_copy_streams(self, n: int):
         check(self.lib.pi_pool_set_copy_streams(self.h, n), "pi_pool_set_copy_streams")
 

@@ -135,6 +135,19 @@ struct pi_pool {
   bool attn_cluster = true;       // splits 2..8 of a unit merge through DSMEM in a cluster
   int attn_splits = 0;            // attention split count override (0 = one wave at full occupancy)
 
+  // fused selection + gather (UVA arm of the decode step): one launch per layer (or
+  // request group) on a few SMs; its CTAs claim selection items from a counter that
+  // only grows, one per (layer, first unit of the launch) so that request groups'
+  // launches of one layer may overlap (fused_base = its value when the next launch
+  // starts), and a unit's plan is published to the launch's other CTAs by
+  // fused_ready = epoch
+  bool fused_on = false;
+  int fused_ctas = 0;                    // 0 = a quarter of the SMs
+  unsigned long long* fused_claim = nullptr;  // [L][R*U]
+  unsigned* fused_ready = nullptr;       // [L][R*U]
+  std::vector<unsigned long long> fused_base;  // [L][R*U]
+  std::vector<unsigned> fused_epoch;     // [L]
+
   // attention-mass diagnostic: per-chunk partials [L][R][Hq][kMassChunksMax], allocated on first use
   float4* mass_part = nullptr;
 
@@ -160,6 +173,10 @@ cudaError_t pi_launch_append(pi_pool* p, int layer, const void* k_new, const voi
 cudaError_t pi_launch_select(pi_pool* p, int layer, const void* q, const int* k_per_req, int* sel, int* nsel,
                              cudaStream_t s, int* fused_table = nullptr, int mode = -1, int r0 = 0, int nr = -1);
 cudaError_t pi_launch_plan(pi_pool* p, int layer, const int* sel, const int* nsel, int* table, cudaStream_t s);
+// selection + plan + UVA gather of requests r0 .. r0+nr-1 in one launch (decode step)
+cudaError_t pi_launch_select_gather(pi_pool* p, int layer, const void* q, const int* k_per_req, int* sel, int* nsel,
+                                    int* table, const void* k_new, const void* v_new, cudaStream_t s, int r0 = 0,
+                                    int nr = -1);
 cudaError_t pi_launch_gather(pi_pool* p, int layer, const uint8_t* stage_src, bool copy, bool commit,
                              cudaStream_t s, const void* k_new = nullptr, const void* v_new = nullptr, int r0 = 0,
                              int nr = -1, bool paired = false);
@@ -223,6 +240,37 @@ __device__ __forceinline__ bool pi_mbar_wait_bounded(uint64_t* bar, unsigned par
 
 __device__ __forceinline__ void pi_fence_barrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void pi_mbar_inval(uint64_t* bar) {
+  asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(pi_smem_addr(bar)) : "memory");
+}
+
+// Flags one CTA publishes to the other CTAs of the same launch.
+__device__ __forceinline__ void pi_st_release(unsigned* addr, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned pi_ld_acquire(const unsigned* addr) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
+  return v;
+}
+
+// Wait until *flag == want; gives up after `limit` cycles (about a second at the
+// default), records PI_DEV_TIMEOUT and returns false.
+__device__ __forceinline__ bool pi_wait_flag_bounded(const unsigned* flag, unsigned want, unsigned* status,
+                                                     long long limit = 2000000000LL) {
+  if (pi_ld_acquire(flag) == want) return true;
+  const long long t0 = clock64();
+  while (pi_ld_acquire(flag) != want) {
+    if (clock64() - t0 > limit) {
+      pi_flag(status, PI_DEV_TIMEOUT);
+      return false;
+    }
+    __nanosleep(200);
+  }
+  return true;
 }
 
 // 2D tiled TMA load global -> shared, completion on an mbarrier.

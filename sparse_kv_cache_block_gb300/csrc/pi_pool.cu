@@ -59,7 +59,8 @@ static void pool_free(pi_pool* p) {
                       p->slot_of,    p->block_of,   p->dev_status, p->sel_scores,  p->sel_counter, p->plan_n,
                       p->plan,       p->recall_counts, p->attn_o,  p->attn_ml,     p->attn_counter, p->step_sel,
                       p->step_nsel,  p->step_table, p->step_in,    p->step_out,    p->stage_dev,
-                      p->ntok_stage, p->slot_stamp, p->epoch,      p->mass_part};
+                      p->ntok_stage, p->slot_stamp, p->epoch,      p->mass_part,
+                      p->fused_claim, p->fused_ready};
   for (void* d : dev_ptrs)
     if (d) cudaFree(d);
   if (p->host) {
@@ -257,6 +258,10 @@ extern "C" pi_status pi_pool_create(const pi_config* cfg, pi_pool** out) {
   TRY_ALLOC(dalloc(&p->dev_status, 1));
   TRY_ALLOC(dalloc(&p->sel_scores, (size_t)p->L * RU * p->max_blocks));
   TRY_ALLOC(dalloc(&p->sel_counter, (size_t)p->L * RU));
+  TRY_ALLOC(dalloc(&p->fused_claim, (size_t)p->L * RU));
+  TRY_ALLOC(dalloc(&p->fused_ready, (size_t)p->L * RU));
+  p->fused_base.assign((size_t)p->L * RU, 0ULL);
+  p->fused_epoch.assign(p->L, 0u);
   TRY_ALLOC(dalloc(&p->plan_n, (size_t)p->L * RU));
   TRY_ALLOC(dalloc(&p->plan, (size_t)p->L * RU * p->cap));
   TRY_ALLOC(dalloc(&p->recall_counts, (size_t)p->L * 4));
@@ -389,6 +394,8 @@ extern "C" pi_status pi_clear_device_status(pi_pool* p) {
   // a kernel that gave up on a wait may have left its completion counters behind
   PI_CUDA_TRY(cudaMemset(p->sel_counter, 0, sizeof(unsigned) * p->L * p->R * p->U));
   PI_CUDA_TRY(cudaMemset(p->attn_counter, 0, sizeof(unsigned) * p->L * p->R * p->Hkv));
+  PI_CUDA_TRY(cudaMemset(p->fused_claim, 0, sizeof(unsigned long long) * p->L * p->R * p->U));
+  p->fused_base.assign((size_t)p->L * p->R * p->U, 0ULL);
   return PI_OK;
 }
 

@@ -15,6 +15,7 @@
 #include <chrono>
 #include <cstring>
 
+#include "pi_gather.cuh"
 #include "pi_internal.cuh"
 #include "pi_plan.cuh"
 
@@ -75,36 +76,6 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
                                    keys, p.lru_p2);
 }
 
-struct GatherParams {
-  const int* plan_n;
-  const int4* plan;
-  int* slot_of;
-  int* block_of;
-  int* slot_stamp;           // stamped at commit under the least-recently-selected policy
-  const uint8_t* host_src;   // device address of this layer's host store (request 0)
-  uint8_t* host_dst;         // same memory, writable (write-through of new tokens)
-  const uint8_t* stage_src;  // staged arm: device staging buffer (entries e_begin..)
-  uint8_t* pool;
-  const long long* slot_base;
-  const int* P;
-  const int* ntok;           // [R][L] (after this step's append)
-  const uint8_t* k_new;      // optional [R][Hkv][D]: this step's token of this layer
-  const uint8_t* v_new;
-  unsigned* status;
-  long long region_bytes;
-  long long e_begin, e_end;  // entry range to process (global plan order)
-  int layer, L, R, U, Hkv, B, D, max_blocks, p_max, cap, units, copy_bytes, block_bytes, do_copy, do_commit;
-  int r0, nr;                // requests of this launch: r0 .. r0+nr-1 (units r0*U ..; plan pointers offset)
-};
-
-__device__ __forceinline__ uint4 ld_stream(const uint4* ptr) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(ptr));
-  return v;
-}
-
 // Grid-stride over (plan entry, chunk of 256 x 16 x DEPTH bytes). Each thread
 // keeps DEPTH 16-byte loads in flight (DEPTH = 8: 32 KiB outstanding per CTA).
 // With k_new set (decode-step pipeline), CTA 0 also writes this step's token of
@@ -116,23 +87,7 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(GatherParams g) 
   constexpr int kChunkBytes = kGatherThreads * 16 * kGatherDepth;
   extern __shared__ long long prefix[];  // [units + 1]
   __shared__ int warp_sums[kGatherThreads / 32];
-  const int row_bytes = g.D * 2;
-  const int row_words = row_bytes / 16;
-  // write-through of the new tokens (host store), one request per pass
-  if (g.k_new && blockIdx.x == 0) {
-    const int per_req = g.Hkv * 2 * row_words;  // 16-byte words of K and V rows
-    for (int w = threadIdx.x; w < g.nr * per_req; w += kGatherThreads) {
-      const int r = g.r0 + w / per_req, rem = w % per_req;
-      const int g_ = rem / (2 * row_words), kv = (rem / row_words) & 1, x = rem % row_words;
-      const int t = g.ntok[(size_t)r * g.L + g.layer] - 1;
-      if (t < 0 || t / g.B >= g.max_blocks) continue;
-      const int b = t / g.B, tp = t % g.B;
-      const uint8_t* src = (kv ? g.v_new : g.k_new) + (((size_t)r * g.Hkv + g_) * g.D) * 2 + (size_t)x * 16;
-      uint8_t* dst = g.host_dst + (size_t)r * g.region_bytes + (size_t)b * g.block_bytes +
-                     (((size_t)g_ * 2 + kv) * g.B + tp) * row_bytes + (size_t)x * 16;
-      *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
-    }
-  }
+  if (g.k_new && blockIdx.x == 0) pi_gather_write_through<kGatherThreads>(g);
   // prefix sums of the per-unit plan counts (every CTA computes its own copy)
   long long run = 0;
   for (int base = 0; base < g.units; base += kGatherThreads) {
@@ -172,66 +127,7 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(GatherParams g) 
       const int mid = (lo + hi + 1) >> 1;
       if (prefix[mid] <= e) lo = mid; else hi = mid - 1;
     }
-    const int u = lo;
-    const int j = (int)(e - prefix[u]);
-    const int4 pe = g.plan[(size_t)u * g.cap + j];
-    const int r = g.r0 + u / g.U, gu = u % g.U;
-    const int Pr = g.P[(size_t)r * g.L + g.layer];
-    const bool ok = pe.x >= 0 && pe.x < g.max_blocks && pe.y >= 0 && pe.y < Pr && pe.z < g.max_blocks;
-    if (!ok) {
-      if (threadIdx.x == 0) pi_flag(g.status, PI_DEV_BAD_INDEX);
-      continue;
-    }
-    const size_t head_off = (g.U > 1) ? (size_t)gu * g.copy_bytes : 0;
-    if (g.do_copy) {
-      const size_t off = (size_t)c * chunk;
-      const int len = min(chunk, g.copy_bytes - c * chunk);
-      const uint8_t* src = g.stage_src ? g.stage_src + (size_t)(e - e0) * g.copy_bytes + off
-                                       : g.host_src + (size_t)r * g.region_bytes +
-                                             (size_t)pe.x * g.block_bytes + head_off + off;
-      uint8_t* blk = g.pool + (size_t)(g.slot_base[(size_t)r * g.L + g.layer] + pe.y) * g.block_bytes;
-      uint8_t* dst = blk + head_off + off;
-      const uint4* s4 = reinterpret_cast<const uint4*>(src);
-      uint4* d4 = reinterpret_cast<uint4*>(dst);
-      const int words = len >> 4;
-      for (int w = threadIdx.x; w < words; w += kGatherThreads * kGatherDepth) {
-        uint4 v[kGatherDepth];
-#pragma unroll
-        for (int k = 0; k < kGatherDepth; k++)
-          if (w + k * kGatherThreads < words) v[k] = ld_stream(s4 + w + k * kGatherThreads);
-#pragma unroll
-        for (int k = 0; k < kGatherDepth; k++)
-          if (w + k * kGatherThreads < words) d4[w + k * kGatherThreads] = v[k];
-      }
-      if (g.k_new) {
-        const int t = g.ntok[(size_t)r * g.L + g.layer] - 1;
-        if (t >= 0 && t / g.B == pe.x) {
-          // this block holds the new token: rewrite its rows that fall in this chunk
-          __syncthreads();
-          const int tp = t % g.B;
-          const int heads = (g.U > 1) ? 1 : g.Hkv;
-          for (int w = threadIdx.x; w < heads * 2 * row_words; w += kGatherThreads) {
-            const int hh = w / (2 * row_words), kv = (w / row_words) & 1, x = w % row_words;
-            const int g_ = (g.U > 1) ? gu : hh;
-            const size_t rel = (((size_t)g_ * 2 + kv) * g.B + tp) * row_bytes + (size_t)x * 16;  // in the block
-            const size_t lo_b = head_off + off, hi_b = head_off + off + len;
-            if (rel >= lo_b && rel < hi_b) {
-              const uint8_t* tsrc = (kv ? g.v_new : g.k_new) + (((size_t)r * g.Hkv + g_) * g.D) * 2 + (size_t)x * 16;
-              *reinterpret_cast<uint4*>(blk + rel) = *reinterpret_cast<const uint4*>(tsrc);
-            }
-          }
-        }
-      }
-    }
-    if (g.do_commit && c == 0 && threadIdx.x == 0) {
-      const size_t rlu = ((size_t)r * g.L + g.layer) * g.U + gu;
-      int* sob = g.slot_of + rlu * g.max_blocks;
-      int* bos = g.block_of + rlu * g.p_max;
-      if (pe.z >= 0) sob[pe.z] = -1;
-      sob[pe.x] = pe.y;
-      bos[pe.y] = pe.x;
-      if (g.slot_stamp) g.slot_stamp[rlu * g.p_max + pe.y] = pe.w;
-    }
+    pi_gather_item<kGatherDepth, kGatherThreads>(g, lo, (int)(e - prefix[lo]), c, chunk, e - e0);
   }
 }
 
@@ -267,7 +163,7 @@ cudaError_t pi_launch_plan(pi_pool* p, int layer, const int* sel, const int* nse
   return cudaGetLastError();
 }
 
-static GatherParams gather_params(pi_pool* p, int layer) {
+GatherParams pi_gather_params(pi_pool* p, int layer) {
   GatherParams g;
   const size_t RU = (size_t)p->R * p->U;
   g.plan_n = p->plan_n + (size_t)layer * RU;
@@ -361,7 +257,7 @@ static cudaError_t launch_gather(pi_pool* p, const GatherParams& g, cudaStream_t
 
 cudaError_t pi_launch_gather(pi_pool* p, int layer, const uint8_t* stage_src, bool copy, bool commit,
                              cudaStream_t s, const void* k_new, const void* v_new, int r0, int nr, bool paired) {
-  GatherParams g = gather_params(p, layer);
+  GatherParams g = pi_gather_params(p, layer);
   if (nr >= 0) {
     // requests r0 .. r0+nr-1 only: their units' plans (the staged arm always takes every request)
     g.plan_n += (size_t)r0 * p->U;
@@ -515,7 +411,7 @@ pi_status pi_recall_impl(pi_pool* p, int layer, const int* sel, const int* nsel,
         local.cpu_gather_ms += std::chrono::duration<double, std::milli>(t1 - t0).count();
         PI_CUDA_TRY(cudaMemcpyAsync(p->stage_dev, p->stage_host, (size_t)(e1 - e0) * cb, cudaMemcpyHostToDevice, st));
         local.api_calls++;
-        GatherParams g = gather_params(p, layer);
+        GatherParams g = pi_gather_params(p, layer);
         g.stage_src = p->stage_dev;
         g.e_begin = e0;
         g.e_end = e1;

@@ -12,6 +12,7 @@
 // token order divided by the token count (IEEE division); the score uses one
 // fixed fp32 order (per-lane fused multiply-add over elements 128c+4*lane+j,
 // then a xor butterfly); ties go to the lower block index.
+#include "pi_gather.cuh"
 #include "pi_internal.cuh"
 #include "pi_plan.cuh"
 
@@ -291,13 +292,16 @@ __device__ __forceinline__ void stage_ints(int* dst, const int* src, int n) {
   }
 }
 
-__global__ void __launch_bounds__(kSelThreads) select_kernel(SelParams p) {
+// One work item of a selection: the scores of chunk `chunk` (of nchunks) of unit
+// u's candidates; the CTA that finishes the unit's last chunk then runs its
+// top-k (and, with a table, its recall plan) and returns true. Every branch is
+// uniform across the CTA; a CTA may run several items one after another.
+__device__ __forceinline__ bool select_item(const SelParams& p, const int u, const int chunk, const int nchunks) {
   __shared__ __align__(16) float qs[1024];
   __shared__ int hist[512];
   __shared__ int warp_sums[kSelThreads / 32];
   __shared__ int bcast[4];
   extern __shared__ __align__(16) uint32_t dyn[];  // plan scratch, then the slot-map cache
-  const int u = p.u0 + blockIdx.y;
   const int r = u / p.U;
   const int g = (p.U == 1) ? 0 : u % p.U;
   const int E = (p.U == 1) ? p.Hkv * p.D : p.D;
@@ -322,7 +326,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelParams p) {
 
   // scores of this CTA's candidates: one warp per block, canonical lane order,
   // two blocks per pass so sixteen 16-byte loads per lane are in flight
-  const int b_begin = blockIdx.x * p.bpc;
+  const int b_begin = chunk * p.bpc;
   const int b_end = min(ncand, b_begin + p.bpc);
   float* sc = p.scores + (size_t)u * p.max_blocks;
   const int chunks = (E + 127) / 128;
@@ -393,6 +397,9 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelParams p) {
     if (!ok && threadIdx.x == 0)
       for (int it = 0; it < nst; it++) pi_mbar_wait_bounded(&full[it % NS], (it / NS) & 1, p.status);
     __syncthreads();
+    // the ring's barriers are done with (a later item of the same CTA sets them up again)
+    if (threadIdx.x == 0)
+      for (int s = 0; s < NS; s++) pi_mbar_inval(&full[s]);
     for (int bl = threadIdx.x; bl < nblk; bl += kSelThreads) {
       float total = 0.0f;
       for (int g2 = 0; g2 < p.Hkv; g2++) total = __fadd_rn(total, cg_s[(size_t)bl * p.Hkv + g2]);
@@ -447,10 +454,10 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelParams p) {
   __syncthreads();
   if (threadIdx.x == 0) {
     const unsigned done = atomicAdd(p.counter + u, 1u);
-    bcast[0] = (done == gridDim.x - 1) ? 1 : 0;
+    bcast[0] = (done == (unsigned)nchunks - 1) ? 1 : 0;
   }
   __syncthreads();
-  if (!bcast[0]) return;
+  if (!bcast[0]) return false;
   if (threadIdx.x == 0) p.counter[u] = 0;  // ready for the next call
   __threadfence();
 
@@ -628,7 +635,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelParams p) {
     if (out_n != kk) pi_flag(p.status, PI_DEV_BAD_INDEX);
     p.nsel[u] = kk + nrecent;
   }
-  if (p.table == nullptr) return;
+  if (p.table == nullptr) return true;
 
   // fused recall plan of this unit (the selection is in global memory, written
   // by this CTA; the barrier makes it visible to every thread of the CTA)
@@ -655,6 +662,63 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelParams p) {
   a.empty_first = p.empty_first;
   pi_plan::plan_unit<kSelThreads>(a, pl, reinterpret_cast<int*>(pl) + words, reinterpret_cast<int*>(pl) + words + p.cap,
                                   warp_sums, lkeys, p.lru_p2);
+  return true;
+}
+
+__global__ void __launch_bounds__(kSelThreads) select_kernel(SelParams p) {
+  select_item(p, p.u0 + blockIdx.y, blockIdx.x, gridDim.x);
+}
+
+struct FusedArgs {
+  unsigned long long* claim;      // this layer's item counter (only grows)
+  unsigned long long claim_base;  // its value when this launch starts
+  unsigned* ready;                // [R*U] of this layer: epoch once a unit's plan is written
+  unsigned epoch;
+  int units, chunks, items;       // units p.u0 .. p.u0+units-1; items = units x chunks
+};
+
+// Selection, recall plan and UVA gather of one layer in one launch on a few SMs
+// (the decode step's fused form). Phase 1: each CTA claims selection items
+// (unit-major, so the first units' plans come out first) from a counter until
+// none are left; the CTA that completes a unit's last item runs its top-k and
+// plan and publishes them with a release store of the launch's epoch. Phase 2:
+// every CTA walks the units in order, waits (bounded) for each unit's flag, and
+// copies its share of the unit's missing blocks in 32 KiB items. A CTA only
+// waits once every item has been claimed by a running CTA, and items never
+// wait, so the launch finishes whatever the CTAs' residency.
+__global__ void __launch_bounds__(kSelThreads) select_gather_kernel(SelParams p, GatherParams g, FusedArgs f) {
+  __shared__ int claim_s;
+  if (g.k_new && blockIdx.x == 0) pi_gather_write_through<kSelThreads>(g);
+  for (;;) {
+    __syncthreads();  // the previous item is done with shared memory and claim_s
+    if (threadIdx.x == 0) claim_s = (int)min(atomicAdd(f.claim, 1ULL) - f.claim_base, (unsigned long long)f.items);
+    __syncthreads();
+    const int it = claim_s;
+    if (it >= f.items) break;
+    const int v = it / f.chunks;
+    if (select_item(p, p.u0 + v, it - v * f.chunks, f.chunks)) {
+      __threadfence();
+      __syncthreads();
+      if (threadIdx.x == 0) pi_st_release(f.ready + p.u0 + v, f.epoch);
+    }
+  }
+  constexpr int kDepth = 8;
+  constexpr int kChunk = kSelThreads * 16 * kDepth;
+  const int chunk = min(g.copy_bytes, kChunk);
+  const int cpe = (g.copy_bytes + chunk - 1) / chunk;
+  const int F = gridDim.x;
+  long long rot = 0;  // items of the earlier units: the next unit's first item goes to CTA rot % F
+  for (int v = 0; v < f.units; v++) {
+    __syncthreads();
+    if (threadIdx.x == 0) claim_s = pi_wait_flag_bounded(f.ready + p.u0 + v, f.epoch, p.status) ? 1 : 0;
+    __syncthreads();
+    if (!claim_s) continue;  // timed out: recorded in the status word, the unit is skipped
+    const long long items = (long long)__ldcg(g.plan_n + v) * cpe;
+    const long long first = ((long long)blockIdx.x - rot % F + F) % F;
+    for (long long i = first; i < items; i += F)
+      pi_gather_item<kDepth, kSelThreads>(g, v, (int)(i / cpe), (int)(i % cpe), chunk, 0);
+    rot += items;
+  }
 }
 
 }  // namespace
@@ -704,12 +768,11 @@ cudaError_t pi_launch_append(pi_pool* p, int layer, const void* k_new, const voi
   return cudaGetLastError();
 }
 
-cudaError_t pi_launch_select(pi_pool* p, int layer, const void* q, const int* k_per_req, int* sel, int* nsel,
-                             cudaStream_t s, int* fused_table, int mode, int r0, int nr) {
-  if (mode < 0) mode = p->mode;
-  if (nr < 0) nr = p->R;
-  if (nr == 0) return cudaSuccess;
-  SelParams sp;
+// Parameters, chunk count and dynamic shared memory of a selection launch over
+// requests r0 .. r0+nr-1 whose grid should hold about `target` CTAs.
+static void prepare_select(pi_pool* p, int layer, const void* q, const int* k_per_req, int* sel, int* nsel,
+                           int* fused_table, int mode, int r0, int nr, long long target, SelParams& sp, int& chunks,
+                           size_t& smem) {
   sp.q = (const uint16_t*)q;
   sp.k_per_req = k_per_req;
   sp.sel = sel;
@@ -739,11 +802,10 @@ cudaError_t pi_launch_select(pi_pool* p, int layer, const void* q, const int* k_
     nb_max = max(nb_max, (nt + p->B - 1) / p->B);
   }
   const int ncand_max = max(0, nb_max - p->W);
-  // enough CTAs to cover every SM twice, at least 8 blocks (one per warp) each
-  // (rounded down: one more chunk per unit would spill into a second wave)
-  long long target = 2LL * p->num_sms;
+  // about `target` CTAs, at least 8 blocks (one per warp) each (rounded down:
+  // one more chunk per unit would spill into a second wave)
   const long long units_launch = (long long)nr * p->U;
-  int chunks = (int)max(1LL, target / units_launch);
+  chunks = (int)max(1LL, target / units_launch);
   int bpc = (ncand_max + chunks - 1) / chunks;
   bpc = ((max(bpc, 8) + 7) / 8) * 8;
   chunks = max(1, (ncand_max + bpc - 1) / bpc);
@@ -772,7 +834,7 @@ cudaError_t pi_launch_select(pi_pool* p, int layer, const void* q, const int* k_
     sp.ring_stages = max(2, min(8, 65536 / stage_bytes));
     sp.dyn_plan_off = sp.ring_stages * stage_bytes + sp.ring_stages * 8 + ((bpc * p->Hkv * 4 + 15) & ~15);
   }
-  size_t smem = sp.dyn_plan_off;
+  smem = sp.dyn_plan_off;
   if (fused_table) smem += pi_plan::plan_smem_bytes(p->max_blocks, p->cap, sp.lru_p2);
   // slot maps cached for the fused plan when they are small (cached only up to
   // the largest block count of this layer; nothing beyond it is ever looked up)
@@ -783,14 +845,64 @@ cudaError_t pi_launch_select(pi_pool* p, int layer, const void* q, const int* k_
     sp.map_cache_slots = (p->p_max + 3) & ~3;
     smem += sizeof(int) * (size_t)(sp.map_cache_blocks + sp.map_cache_slots);
   }
+  sp.u0 = r0 * p->U;
+}
+
+cudaError_t pi_launch_select(pi_pool* p, int layer, const void* q, const int* k_per_req, int* sel, int* nsel,
+                             cudaStream_t s, int* fused_table, int mode, int r0, int nr) {
+  if (mode < 0) mode = p->mode;
+  if (nr < 0) nr = p->R;
+  if (nr == 0) return cudaSuccess;
+  SelParams sp;
+  int chunks = 1;
+  size_t smem = 0;
+  // enough CTAs to cover every SM twice
+  prepare_select(p, layer, q, k_per_req, sel, nsel, fused_table, mode, r0, nr, 2LL * p->num_sms, sp, chunks, smem);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  sp.u0 = r0 * p->U;
   dim3 grid(chunks, (unsigned)(nr * p->U));
   select_kernel<<<grid, kSelThreads, smem, s>>>(sp);
   return cudaGetLastError();
+}
+
+cudaError_t pi_launch_select_gather(pi_pool* p, int layer, const void* q, const int* k_per_req, int* sel, int* nsel,
+                                    int* table, const void* k_new, const void* v_new, cudaStream_t s, int r0,
+                                    int nr) {
+  if (nr < 0) nr = p->R;
+  if (nr == 0) return cudaSuccess;
+  const int ctas = p->fused_ctas > 0 ? p->fused_ctas : max(1, p->num_sms / 4);
+  FusedArgs f;
+  SelParams sp;
+  size_t smem = 0;
+  // two selection items per CTA: a CTA that finishes early takes another
+  prepare_select(p, layer, q, k_per_req, sel, nsel, table, p->mode, r0, nr, 2LL * ctas, sp, f.chunks, smem);
+  GatherParams g = pi_gather_params(p, layer);
+  g.plan_n += (size_t)r0 * p->U;
+  g.plan += (size_t)r0 * p->U * p->cap;
+  g.r0 = r0;
+  g.nr = nr;
+  g.units = nr * p->U;
+  g.k_new = (const uint8_t*)k_new;
+  g.v_new = (const uint8_t*)v_new;
+  f.units = nr * p->U;
+  f.items = f.units * f.chunks;
+  const size_t ci = (size_t)layer * p->R * p->U + (size_t)r0 * p->U;  // counter of (layer, first unit)
+  f.claim = p->fused_claim + ci;
+  f.claim_base = p->fused_base[ci];
+  f.ready = p->fused_ready + (size_t)layer * p->R * p->U;
+  f.epoch = ++p->fused_epoch[layer];
+  if (smem > 48 * 1024) {
+    cudaError_t e =
+        cudaFuncSetAttribute(select_gather_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  select_gather_kernel<<<ctas, kSelThreads, smem, s>>>(sp, g, f);
+  cudaError_t e = cudaGetLastError();
+  // every CTA claims until a claim fails: the counter grows by the items plus one per CTA
+  if (e == cudaSuccess) p->fused_base[ci] += (unsigned long long)f.items + (unsigned long long)ctas;
+  return e;
 }
 
 // ---------------------------------------------------------------------- API

@@ -12,6 +12,8 @@
 //  - dependent queries: per request group, append, selection, recall and
 //    attention of layer after layer on the group's stream, the groups' recalls
 //    taking turns on the copy stream.
+// With the fused form (pi_pool_set_fused) the selection, plan and gather of a
+// layer (or a request group's share of it) are one launch on the copy stream.
 // With the UVA gather arm no step needs the host.
 #include <algorithm>
 #include <cstring>
@@ -66,15 +68,19 @@ static pi_status step_impl(pi_pool* p, const uint8_t* q_all, const uint8_t* k_ne
   // writes the new tokens through to the host store, so the copy stream carries
   // only the gather and the compute stream never waits on host-memory writes.
   const bool uva = (method == PI_RECALL_UVA);
+  // fused: selection, plan and gather of a layer run as one launch on the copy
+  // stream (the compute stream keeps only the append)
+  const bool fused = uva && p->fused_on;
   auto select = [&](int l) -> pi_status {
     if (append) {
       PI_TIMED(l, PI_K_APPEND, cs,
                pi_launch_append(p, l, k_new_all + (size_t)l * kv_bytes, v_new_all + (size_t)l * kv_bytes, cs, !uva));
       for (int r = 0; r < p->R; r++) p->ntok_h[(size_t)r * p->L + l] += 1;
     }
-    PI_TIMED(l, PI_K_SELECT, cs,
-             pi_launch_select(p, l, q_all + (size_t)l * q_bytes, k_budget + (size_t)l * p->R, sel_of(l), nsel_of(l), cs,
-                              uva ? tab_of(l) : nullptr));
+    if (!fused)
+      PI_TIMED(l, PI_K_SELECT, cs,
+               pi_launch_select(p, l, q_all + (size_t)l * q_bytes, k_budget + (size_t)l * p->R, sel_of(l), nsel_of(l),
+                                cs, uva ? tab_of(l) : nullptr));
     PI_CUDA_TRY(cudaEventRecord(p->ev_sel[l], cs));
     return PI_OK;
   };
@@ -89,9 +95,14 @@ static pi_status step_impl(pi_pool* p, const uint8_t* q_all, const uint8_t* k_ne
     if (uva) {
       p->recall_calls++;
       if (p->fault_recall_at > 0 && p->recall_calls == p->fault_recall_at) return PI_ERR_FAULT_INJECTED;
-      PI_TIMED(l, PI_K_GATHER, rs,
-               pi_launch_gather(p, l, nullptr, true, true, rs, append ? k_new_all + (size_t)l * kv_bytes : nullptr,
-                                append ? v_new_all + (size_t)l * kv_bytes : nullptr, 0, -1, two_copies));
+      const uint8_t* kn = append ? k_new_all + (size_t)l * kv_bytes : nullptr;
+      const uint8_t* vn = append ? v_new_all + (size_t)l * kv_bytes : nullptr;
+      if (fused)
+        PI_TIMED(l, PI_K_GATHER, rs,
+                 pi_launch_select_gather(p, l, q_all + (size_t)l * q_bytes, k_budget + (size_t)l * p->R, sel_of(l),
+                                         nsel_of(l), tab_of(l), kn, vn, rs));
+      else
+        PI_TIMED(l, PI_K_GATHER, rs, pi_launch_gather(p, l, nullptr, true, true, rs, kn, vn, 0, -1, two_copies));
     } else {
       pi_status s2 = pi_recall_impl(p, l, sel_of(l), nsel_of(l), method, tab_of(l), nullptr, rs);
       if (s2 != PI_OK) return s2;
@@ -135,18 +146,26 @@ static pi_status step_impl(pi_pool* p, const uint8_t* q_all, const uint8_t* k_ne
                                       false, r0[g], nr[g]));
           for (int r = r0[g]; r < r0[g] + nr[g]; r++) p->ntok_h[(size_t)r * p->L + l] += 1;
         }
-        PI_TIMED_G(l, g, PI_K_SELECT, s,
-                   pi_launch_select(p, l, q_all + (size_t)l * q_bytes, k_budget + (size_t)l * p->R, sel_of(l),
-                                    nsel_of(l), s, tab_of(l), -1, r0[g], nr[g]));
-        PI_CUDA_TRY(cudaEventRecord(ev[0], s));
-        PI_CUDA_TRY(cudaStreamWaitEvent(ys, ev[0], 0));
         p->recall_calls++;
         if (p->fault_recall_at > 0 && p->recall_calls == p->fault_recall_at) return PI_ERR_FAULT_INJECTED;
-        PI_TIMED_G(l, g, PI_K_GATHER, ys,
-                   pi_launch_gather(p, l, nullptr, true, true, ys, append ? k_new_all + (size_t)l * kv_bytes : nullptr,
-                                    append ? v_new_all + (size_t)l * kv_bytes : nullptr, r0[g], nr[g]));
-        PI_CUDA_TRY(cudaEventRecord(ev[1], ys));
-        PI_CUDA_TRY(cudaStreamWaitEvent(s, ev[1], 0));
+        const uint8_t* kn = append ? k_new_all + (size_t)l * kv_bytes : nullptr;
+        const uint8_t* vn = append ? v_new_all + (size_t)l * kv_bytes : nullptr;
+        if (fused) {
+          // the fused launch stays on the group's stream: the groups' launches
+          // share the link instead of taking turns on the copy stream
+          PI_TIMED_G(l, g, PI_K_GATHER, s,
+                     pi_launch_select_gather(p, l, q_all + (size_t)l * q_bytes, k_budget + (size_t)l * p->R,
+                                             sel_of(l), nsel_of(l), tab_of(l), kn, vn, s, r0[g], nr[g]));
+        } else {
+          PI_TIMED_G(l, g, PI_K_SELECT, s,
+                     pi_launch_select(p, l, q_all + (size_t)l * q_bytes, k_budget + (size_t)l * p->R, sel_of(l),
+                                      nsel_of(l), s, tab_of(l), -1, r0[g], nr[g]));
+          PI_CUDA_TRY(cudaEventRecord(ev[0], s));
+          PI_CUDA_TRY(cudaStreamWaitEvent(ys, ev[0], 0));
+          PI_TIMED_G(l, g, PI_K_GATHER, ys, pi_launch_gather(p, l, nullptr, true, true, ys, kn, vn, r0[g], nr[g]));
+          PI_CUDA_TRY(cudaEventRecord(ev[1], ys));
+          PI_CUDA_TRY(cudaStreamWaitEvent(s, ev[1], 0));
+        }
         PI_TIMED_G(l, g, PI_K_ATTENTION, s,
                    pi_launch_attention(p, l, q_all + (size_t)l * q_bytes, sel_of(l), tab_of(l), nsel_of(l),
                                        out_all + (size_t)l * q_bytes,
@@ -325,6 +344,16 @@ extern "C" pi_status pi_pool_set_pipeline(pi_pool* p, int select_ahead, int atte
   PI_CUDA_TRY(cudaDeviceSynchronize());  // no step of the old mode may still run
   p->select_ahead = select_ahead;
   p->attn_stream_on = attention_stream != 0;
+  return PI_OK;
+}
+
+extern "C" pi_status pi_pool_set_fused(pi_pool* p, int on, int ctas) {
+  if (!p || (on != 0 && on != 1) || ctas < 0) return PI_ERR_INVALID;
+  PI_CUDA_TRY(cudaDeviceSynchronize());
+  p->fused_on = (on == 1);
+  p->fused_ctas = ctas;
+  // fresh timing events: a kind the new form no longer launches keeps no old times
+  if (p->timing_steps > 0) return pi_pool_set_timing(p, p->timing_steps);
   return PI_OK;
 }
 

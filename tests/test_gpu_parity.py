@@ -175,7 +175,10 @@ def test_small_config_layer_calls(method):
                           (pi.PI_RECALL_UVA, 0, 1, "few"), (pi.PI_RECALL_UVA, 1, 1, "shared"),
                           (pi.PI_RECALL_UVA, 0, 1, "shared"), (pi.PI_RECALL_UVA, 0, -1, "default"),
                           (pi.PI_RECALL_UVA, 1, -1, "default"), (pi.PI_RECALL_MEMCPY, 0, -1, "default"),
-                          (pi.PI_RECALL_UVA, 0, -1, "one_copy"), (pi.PI_RECALL_UVA, 1, 1, "one_copy")])
+                          (pi.PI_RECALL_UVA, 0, -1, "one_copy"), (pi.PI_RECALL_UVA, 1, 1, "one_copy"),
+                          (pi.PI_RECALL_UVA, 0, -1, "fused"), (pi.PI_RECALL_UVA, 1, -1, "fused"),
+                          (pi.PI_RECALL_UVA, 0, -1, "fused_few"), (pi.PI_RECALL_UVA, 1, 1, "fused"),
+                          (pi.PI_RECALL_UVA, 0, -1, "fused_one_copy")])
 def test_multistep_pipeline_8b_shape(method, evict, ahead, placement):
     """Llama-3-8B-shaped heads (32 q / 8 KV, d 128, blocks of 64), 2 layers, 2
     requests with ragged tails, heavy-hitter blocks, AR(1) queries, 4 pipelined
@@ -192,6 +195,11 @@ def test_multistep_pipeline_8b_shape(method, evict, ahead, placement):
             pool.set_gather(0, 8, False)  # one 256-thread CTA per SM beside other kernels
         elif placement == "one_copy":
             pool.set_copy_streams(1)  # every gather on the caller's copy stream (the default uses two)
+        elif placement.startswith("fused"):
+            # selection, plan and gather of a layer in one launch; "few": 3 CTAs, many items each
+            pool.set_fused(True, 3 if placement == "fused_few" else 0)
+            if placement == "fused_one_copy":
+                pool.set_copy_streams(1)
         prefill(pool, w)
         om = OracleModel(w)
         qs = queries(w)
@@ -629,6 +637,39 @@ def test_dependent_schedule_gives_identical_results(mode, evict):
             assert err <= OUT_ATOL, (groups, s, err)
             rel = np.abs(got[s]["lse"] - base[s]["lse"]) / np.maximum(np.abs(base[s]["lse"]), 1.0)
             assert rel.max() <= LSE_RTOL, (groups, s)
+
+
+@pytest.mark.parametrize("mode,evict", [(pi.PI_SHARED, 0), (pi.PI_SHARED, 1), (pi.PI_CONSENSUS, 0),
+                                        (pi.PI_HEADWISE, 0)], ids=["shared", "shared_lru", "consensus", "headwise"])
+def test_fused_select_gather_gives_identical_results(mode, evict):
+    """Selection, recall plan and gather of a layer as one launch: selections,
+    tables, slot maps and pool bytes bit for bit equal to the unfused decode step,
+    and the outputs too (the attention launches are the same), with the default
+    grid, with 3 CTAs (every CTA takes many items), on one copy stream; under the
+    dependent schedule with 2 or 3 request groups (their launches of a layer run
+    at the same time on the groups' streams) the outputs are within the
+    tolerances (launches over fewer requests split differently)."""
+    w = Workload(layers=3, batch=5, hq=32, hkv=8, head_dim=128, block_tokens=64, ntok=[4000, 2500, 3100, 700, 5000],
+                 k=8, window=2, pool_slots=12, steps=3, rho=0.9, heavy_frac=0.05, seed=67, evict_policy=evict,
+                 select_mode=mode)
+    base = _run_steps(w, lambda pool: None)
+    setups = {"fused": lambda pool: pool.set_fused(True),
+              "fused_3_ctas": lambda pool: pool.set_fused(True, 3),
+              "fused_one_copy": lambda pool: (pool.set_fused(True), pool.set_copy_streams(1)),
+              "fused_dependent_2": lambda pool: (pool.set_fused(True), pool.set_schedule(True, 2)),
+              "fused_dependent_3": lambda pool: (pool.set_fused(True, 2), pool.set_schedule(True, 3))}
+    for name, setup in setups.items():
+        got = _run_steps(w, setup)
+        for s in range(w.steps):
+            for key in ("sel", "nsel", "tab", "sob", "bos", "pool"):
+                assert np.array_equal(got[s][key], base[s][key]), (name, s, key)
+            if not name.startswith("fused_dependent"):
+                assert np.array_equal(got[s]["out"], base[s]["out"]), (name, s)
+                assert np.array_equal(got[s]["lse"], base[s]["lse"]), (name, s)
+            else:
+                err = np.max(np.abs(bf16_to_f32(got[s]["out"].view(np.uint16)) -
+                                    bf16_to_f32(base[s]["out"].view(np.uint16))))
+                assert err <= OUT_ATOL, (name, s, err)
 
 
 def test_schedule_arguments():
