@@ -42,6 +42,21 @@ def test_host_only_calls(lib):
     assert lib.pi_pool_create(None, None) == pi.PI_ERR_INVALID
     assert lib.pi_pool_destroy(None) == pi.PI_ERR_INVALID
     assert lib.pi_host_kv(None, 0, 0) is None
+    # every entry point checks its pool before touching the device
+    null_calls = {
+        "pi_select_topk": (None, 0, None, None, 0, None, None, None),
+        "pi_recall": (None, 0, None, None, 0, None, None, None),
+        "pi_sparse_decode": (None, 0, None, None, None, None, None, None, None, None),
+        "pi_attention_mass": (None, 0, None, None, None, 0, None, None),
+        "pi_pool_set_fused": (None, 1, 0),
+        "pi_pool_set_schedule": (None, 1, 2),
+        "pi_pool_set_copy_streams": (None, 2),
+        "pi_pool_pin_layer": (None, 0, 1),
+        "pi_pool_set_consensus_lambda": (None, 0.5),
+        "pi_pool_set_attention_cluster": (None, 1),
+    }
+    for name, args in null_calls.items():
+        assert getattr(lib, name)(*args) == pi.PI_ERR_INVALID, name
 
 
 def test_library_is_built_for_sm103a_only():
