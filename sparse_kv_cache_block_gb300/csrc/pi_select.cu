@@ -12,6 +12,10 @@
 // token order divided by the token count (IEEE division); the score uses one
 // fixed fp32 order (per-lane fused multiply-add over elements 128c+4*lane+j,
 // then a xor butterfly); ties go to the lower block index.
+//
+// A selection is a set of work items (a chunk of one unit's candidates); the
+// stand-alone kernel runs one item per CTA, the fused select + gather kernel
+// lets a few CTAs claim the items one after another and then copy the recalls.
 #include "pi_gather.cuh"
 #include "pi_internal.cuh"
 #include "pi_plan.cuh"
