@@ -798,10 +798,12 @@ def test_large_selection_sizes(mode):
         run_layer(pool, om, w, 0, queries(w)[0][0], [1100, 300], pi.PI_RECALL_UVA, logits=False)
 
 
+@pytest.mark.parametrize("fused", [False, True], ids=["separate", "fused"])
 @pytest.mark.parametrize("mode", [pi.PI_SHARED, pi.PI_CONSENSUS, pi.PI_HEADWISE], ids=["shared", "consensus", "headwise"])
-def test_features_together(mode):
+def test_features_together(mode, fused):
     """Dependent-query schedule with two request groups, a pinned layer, the
-    least-recently-selected rule and each ranking, three pipelined steps: every
+    least-recently-selected rule and each ranking, three pipelined steps, with
+    selection and gather as separate launches or fused (2 CTAs per launch): every
     layer and step against the oracle run with the same residency."""
     w = Workload(layers=3, batch=3, hq=16, hkv=4, head_dim=128, block_tokens=32, ntok=[2500, 1800, 900], k=6,
                  window=2, pool_slots=9, steps=3, rho=0.7, heavy_frac=0.05, seed=79, evict_policy=1,
@@ -810,6 +812,8 @@ def test_features_together(mode):
     cap = max(w.pool_slots, w.max_blocks)
     with make_pool(w, pin_layers=1) as pool:
         pool.set_schedule(True, 2)
+        if fused:
+            pool.set_fused(True, 2)
         prefill(pool, w)
         om = OracleModel(w)
         pool.pin_layer(0, True)
