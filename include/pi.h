@@ -10,8 +10,8 @@
  * Method (page title, section):
  *  - "PulseInfer: I/O-Centric Sparse KV Cache Offloading for Efficient
  *    Long-Context LLM Decoding", Abstract: KV blocks stay in CPU DRAM, selected
- *    blocks are recalled on demand; SoloHead selection and a gather-scatter I/O
- *    engine turn many small head-wise transfers into one coalesced recall;
+ *    blocks are recalled on demand; one block set shared by the heads (SoloHead)
+ *    and a gathering recall path replace many small per-head copies by one;
  *    recall is overlapped with decode layer by layer.
  *  - "PulseInfer Guide: I/O-Centric Sparse KV Cache Offloading":
  *    "SoloHead Sparse Selection" (one block set shared by all heads of a layer),

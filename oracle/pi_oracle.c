@@ -7,8 +7,8 @@
  * Sources (page title, section):
  *  [A] "PulseInfer: I/O-Centric Sparse KV Cache Offloading for Efficient
  *      Long-Context LLM Decoding", Abstract: most KV blocks live in CPU DRAM and
- *      only selected blocks are recalled; SoloHead selection and a gather-scatter
- *      I/O engine coalesce the recall.
+ *      only selected blocks are recalled; one shared block set (SoloHead) and
+ *      a gathering recall path turn the recall into few large copies.
  *  [G] "PulseInfer Guide: I/O-Centric Sparse KV Cache Offloading":
  *      "SoloHead Sparse Selection" (one block set shared by all heads),
  *      "The Gather-Scatter I/O Engine" (recalled blocks land in pool page slots),
