@@ -9,11 +9,13 @@
 // store (the pool holds only the recalled blocks), so one call moves
 // Hkv*ntok*D*2 bytes per request over the host link and is bound by it.
 //
-// Kernel 1, one CTA per (chunk of tokens, request, KV head): the group's G
-// queries sit in shared memory (fp32), the selected blocks in a bitmap; each
-// thread takes one token at a time, forms the G logits in fp32 and keeps an
-// online (max, sum over all tokens, sum over selected tokens) per head, merged
-// across the CTA by a fixed tree. Kernel 2 merges the chunks in chunk order.
+// Kernel 1, one CTA per (chunk of tokens, request, KV head): the selected
+// blocks sit in a shared-memory bitmap; a warp reads whole key rows (D/8 lanes
+// of 16 bytes per token), each lane dots its 8 elements with the group's G
+// queries (fp32, in registers) and a xor tree over the row's lanes completes the
+// logits; every row keeps an online (max, sum over all tokens, sum over
+// selected tokens) per head, merged across the warp and the CTA by fixed trees.
+// Kernel 2 merges the chunks in chunk order.
 #include <math.h>
 
 #include "pi_internal.cuh"
@@ -88,6 +90,20 @@ __global__ void __launch_bounds__(kMassThreads) mass_part_kernel(MassParams a) {
   }
   __syncthreads();
 
+  // a token's key row is D/8 lanes x 16 bytes: a warp reads 32/(D/8) whole rows
+  // per load instruction (full 128-byte lines over the host link); each lane
+  // keeps its 8 elements of the group's queries in registers
+  constexpr int LPT = D / 8;      // lanes per token
+  constexpr int TPW = 32 / LPT;   // tokens per warp pass
+  constexpr int kPass = 4;        // passes whose loads are in flight together
+  const int lane = tid & 31, warp = tid >> 5;
+  const int sub = lane / LPT, part = lane % LPT;
+  float qr[8][8];
+#pragma unroll
+  for (int j = 0; j < 8; j++)
+#pragma unroll
+    for (int e = 0; e < 8; e++) qr[j][e] = (j < G) ? qf[j * D + part * 8 + e] : 0.f;
+
   MassAcc acc[8];
 #pragma unroll
   for (int j = 0; j < 8; j++) acc[j] = {-INFINITY, 0.f, 0.f};
@@ -96,66 +112,71 @@ __global__ void __launch_bounds__(kMassThreads) mass_part_kernel(MassParams a) {
   const int t0 = c * per, t1 = min(n_tok, t0 + per);
   const uint8_t* region = a.host + ((size_t)a.hl * a.R + r) * a.region_bytes;
   const size_t half = (size_t)a.B * D * 2;  // one head's K (or V) of a block, bytes
-  for (int t = t0 + tid; t < t1; t += kMassThreads) {
-    const int b = t / a.B, i = t - b * a.B;
-    const uint4* kp = reinterpret_cast<const uint4*>(region + (size_t)(b * a.Hkv + g) * 2 * half + (size_t)i * D * 2);
-    uint4 kv[D / 8];
+  constexpr int kWarps = kMassThreads / 32;
+  for (int tb = t0 + warp * kPass * TPW; tb < t1; tb += kWarps * kPass * TPW) {
+    uint4 kv[kPass];
 #pragma unroll
-    for (int d8 = 0; d8 < D / 8; d8++) kv[d8] = kp[d8];
-    float z[8];
+    for (int u = 0; u < kPass; u++) {
+      const int t = tb + u * TPW + sub;
+      kv[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (t < t1) {
+        const int b = t / a.B, i = t - b * a.B;
+        kv[u] = *reinterpret_cast<const uint4*>(region + (size_t)(b * a.Hkv + g) * 2 * half + (size_t)i * D * 2 +
+                                                (size_t)part * 16);
+      }
+    }
 #pragma unroll
-    for (int j = 0; j < 8; j++) z[j] = 0.f;
-#pragma unroll
-    for (int d8 = 0; d8 < D / 8; d8++) {
-      const uint32_t w[4] = {kv[d8].x, kv[d8].y, kv[d8].z, kv[d8].w};
+    for (int u = 0; u < kPass; u++) {
+      const int t = tb + u * TPW + sub;
+      const uint32_t w[4] = {kv[u].x, kv[u].y, kv[u].z, kv[u].w};
       float k[8];
 #pragma unroll
       for (int e = 0; e < 4; e++) {
         k[2 * e] = pi_bf16_lo(w[e]);
         k[2 * e + 1] = pi_bf16_hi(w[e]);
       }
+      float z[8];
 #pragma unroll
       for (int j = 0; j < 8; j++) {
+        z[j] = 0.f;
         if (j < G) {
-          const float4* qv = reinterpret_cast<const float4*>(qf + j * D + d8 * 8);
-          const float4 q0 = qv[0], q1 = qv[1];
-          z[j] = fmaf(q0.x, k[0], z[j]);
-          z[j] = fmaf(q0.y, k[1], z[j]);
-          z[j] = fmaf(q0.z, k[2], z[j]);
-          z[j] = fmaf(q0.w, k[3], z[j]);
-          z[j] = fmaf(q1.x, k[4], z[j]);
-          z[j] = fmaf(q1.y, k[5], z[j]);
-          z[j] = fmaf(q1.z, k[6], z[j]);
-          z[j] = fmaf(q1.w, k[7], z[j]);
+#pragma unroll
+          for (int e = 0; e < 8; e++) z[j] = fmaf(qr[j][e], k[e], z[j]);
+          // the row's LPT lanes: xor tree, every lane ends with the full dot
+#pragma unroll
+          for (int off = LPT / 2; off > 0; off >>= 1) z[j] += __shfl_xor_sync(0xffffffffu, z[j], off);
         }
       }
-    }
-    const float in = (bits[b >> 5] >> (b & 31)) & 1u ? 1.f : 0.f;
+      if (t < t1) {
+        const int b = t / a.B;
+        const float in = (bits[b >> 5] >> (b & 31)) & 1u ? 1.f : 0.f;
 #pragma unroll
-    for (int j = 0; j < 8; j++) {
-      if (j < G) {
-        const float zj = z[j] * a.scale;
-        if (zj > acc[j].m) {
-          const float cm = acc[j].m == -INFINITY ? 0.f : expf(acc[j].m - zj);
-          acc[j].la = acc[j].la * cm + 1.f;
-          acc[j].ls = acc[j].ls * cm + in;
-          acc[j].m = zj;
-        } else {
-          const float e = expf(zj - acc[j].m);
-          acc[j].la += e;
-          acc[j].ls += in * e;
+        for (int j = 0; j < 8; j++) {
+          if (j < G) {
+            const float zj = z[j] * a.scale;
+            if (zj > acc[j].m) {
+              const float cm = acc[j].m == -INFINITY ? 0.f : expf(acc[j].m - zj);
+              acc[j].la = acc[j].la * cm + 1.f;
+              acc[j].ls = acc[j].ls * cm + in;
+              acc[j].m = zj;
+            } else {
+              const float e = expf(zj - acc[j].m);
+              acc[j].la += e;
+              acc[j].ls += in * e;
+            }
+          }
         }
       }
     }
   }
 
-  // merge across the CTA: xor tree in each warp, then warps in order
-  const int lane = tid & 31, warp = tid >> 5;
+  // merge across the CTA: the lanes of one row hold the same sums, so the warp
+  // merges its rows (xor offsets >= LPT), then the warps in order
 #pragma unroll
   for (int j = 0; j < 8; j++) {
     if (j < G) {
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
+      for (int off = 16; off >= LPT; off >>= 1) {
         const float m2 = __shfl_xor_sync(0xffffffffu, acc[j].m, off);
         const float la2 = __shfl_xor_sync(0xffffffffu, acc[j].la, off);
         const float ls2 = __shfl_xor_sync(0xffffffffu, acc[j].ls, off);
