@@ -72,3 +72,23 @@ def test_struct_layouts_match_header():
         assert field in hdr
     assert ctypes.sizeof(_lib.pi_config) == 18 * 4 + 8
     assert ctypes.sizeof(_lib.pi_recall_stats) == 5 * 8 + 2 * 8
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    """No fallback: loading a library that is not there raises."""
+    monkeypatch.setattr(_lib, "_lib", None)
+    with pytest.raises(FileNotFoundError):
+        _lib.load(str(tmp_path / "libpi.so"))
+
+
+def test_product_path_never_touches_the_oracle():
+    """The package and the bench's GPU leg stay independent of oracle/: no
+    source file of the package names it."""
+    pkg = os.path.dirname(_lib.__file__)
+    for root, _, files in os.walk(pkg):
+        if "_build" in root or "__pycache__" in root:
+            continue
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                src = open(os.path.join(root, f)).read()
+                assert "import oracle" not in src and "from oracle" not in src and "pi_oracle" not in src, f
