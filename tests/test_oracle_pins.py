@@ -682,3 +682,21 @@ def test_mass_equals_sparse_over_dense_softmax_normaliser(ntok):
     _, lse_all = oracle.dense_attention_fp64(oracle.bf16_to_f64(q), K, V)
     m = oracle.attention_mass(q, reg, sel, ntok, hkv)
     assert np.allclose(np.log(m), lse_sel - lse_all, rtol=0, atol=1e-10)
+
+
+def test_mass_per_head_sets_equal_sparse_over_dense_softmax_normaliser():
+    """Per-KV-head sets: each head's log(mass) is the lse over its group's set
+    (C sparse-attention oracle, head-wise selection) minus the dense lse."""
+    hq, hkv, B, D, ntok = 8, 2, 16, 64, 500
+    nb = -(-ntok // B)
+    reg = synth.kv_region(25, 0, 0, ntok, nb + 1, hkv, B, D, 0.05, 2.0)
+    q = synth.normal_bf16(25, synth.KIND_MISC, 0, 0, hq * D).reshape(hq, D)
+    sets = [np.array([0, 4, nb - 1], dtype=np.int32), np.array([2, 3, 9, 17], dtype=np.int32)]
+    _, lse_sel, _ = oracle.attention(q, reg, sets, ntok, hkv)
+    K, V = _dense_inputs(reg, ntok, hkv, np.arange(nb))
+    _, lse_all = oracle.dense_attention_fp64(oracle.bf16_to_f64(q), K, V)
+    m = oracle.attention_mass(q, reg, sets, ntok, hkv)
+    assert np.allclose(np.log(m), lse_sel - lse_all, rtol=0, atol=1e-10)
+    # a head of group 0 does not see group 1's set
+    m_swapped = oracle.attention_mass(q, reg, sets[::-1], ntok, hkv)
+    assert not np.allclose(m, m_swapped)
