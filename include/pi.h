@@ -269,6 +269,18 @@ pi_status pi_pool_pin_layer(pi_pool* p, int layer, int pinned);
  * when it changes a layer. */
 pi_status pi_pool_admission(pi_pool* p, double link_util, int* layer, int* pinned);
 
+/* The admission rule of pi_pool_admission alone, on host arrays (no pool, no
+ * device): pinnable[l], pinned[l] (0/1, host [layers]) and last_pinned (the layer
+ * pinned most recently and still pinned, -1: none). Writes the decision to
+ * *layer (-1: none) and *pin (1 pin, 0 release) without changing anything.
+ * Source: PulseInfer Guide, "Interruptible Layer-Wise Scheduling & Adaptive
+ * Admission", "2. IO-Adaptive Offloading Admission" (the two utilisation
+ * thresholds).
+ * Errors: PI_ERR_INVALID (layers <= 0, a null array or output, link_util
+ * negative or NaN). */
+pi_status pi_admission_decide(int layers, const int* pinnable, const int* pinned, int last_pinned, double link_util,
+                              int* layer, int* pin);
+
 /* Weight lambda of the group mean in the consensus score (default 0.5, the
  * guide's "typical" value; its worked example uses 1). Applies to later
  * PI_CONSENSUS selections. PI_ERR_INVALID unless 0 <= lambda <= 1e30. */

@@ -563,29 +563,40 @@ extern "C" pi_status pi_pool_pin_layer(pi_pool* p, int layer, int pinned) {
   return set_layer_slots(p, layer, pinned != 0);
 }
 
-extern "C" pi_status pi_pool_admission(pi_pool* p, double link_util, int* layer, int* pinned) {
-  if (!p || !layer || !pinned || !(link_util >= 0.0)) return PI_ERR_INVALID;
+extern "C" pi_status pi_admission_decide(int layers, const int* pinnable, const int* pinned, int last_pinned,
+                                         double link_util, int* layer, int* pin) {
+  if (layers <= 0 || !pinnable || !pinned || !layer || !pin || !(link_util >= 0.0)) return PI_ERR_INVALID;
   *layer = -1;
-  *pinned = 0;
+  *pin = 0;
   if (link_util > 0.85) {
     // the most active layers first: 0, L-1, 1, L-2, ...
-    for (int i = 0; i < p->L; i++) {
-      const int l = (i % 2 == 0) ? i / 2 : p->L - 1 - i / 2;
-      if (p->pinnable_h[l] && !p->pinned_h[l]) {
-        pi_status st = set_layer_slots(p, l, true);
-        if (st != PI_OK) return st;
+    for (int i = 0; i < layers; i++) {
+      const int l = (i % 2 == 0) ? i / 2 : layers - 1 - i / 2;
+      if (pinnable[l] && !pinned[l]) {
         *layer = l;
-        *pinned = 1;
+        *pin = 1;
         break;
       }
     }
-  } else if (link_util < 0.5 && !p->pin_order.empty()) {
-    const int l = p->pin_order.back();
-    pi_status st = set_layer_slots(p, l, false);
-    if (st != PI_OK) return st;
-    *layer = l;
-    *pinned = 0;
+  } else if (link_util < 0.5 && last_pinned >= 0 && last_pinned < layers) {
+    *layer = last_pinned;
+    *pin = 0;
   }
+  return PI_OK;
+}
+
+extern "C" pi_status pi_pool_admission(pi_pool* p, double link_util, int* layer, int* pinned) {
+  if (!p || !layer || !pinned || !(link_util >= 0.0)) return PI_ERR_INVALID;
+  int l = -1, pin = 0;
+  pi_status st = pi_admission_decide(p->L, p->pinnable_h.data(), p->pinned_h.data(),
+                                     p->pin_order.empty() ? -1 : p->pin_order.back(), link_util, &l, &pin);
+  if (st != PI_OK) return st;
+  if (l >= 0) {
+    st = set_layer_slots(p, l, pin == 1);
+    if (st != PI_OK) return st;
+  }
+  *layer = l;
+  *pinned = pin;
   return PI_OK;
 }
 
