@@ -798,6 +798,52 @@ def test_large_selection_sizes(mode):
         run_layer(pool, om, w, 0, queries(w)[0][0], [1100, 300], pi.PI_RECALL_UVA, logits=False)
 
 
+@pytest.mark.parametrize("mode", [pi.PI_SHARED, pi.PI_CONSENSUS], ids=["shared", "consensus"])
+@pytest.mark.parametrize("hq", [32, 64], ids=["G4_llama8b", "G8_llama70b"])
+def test_gpu_selection_matches_exact_arithmetic(mode, hq):
+    """The GPU's selection against the formula evaluated exactly, not only
+    against the oracle's fp32 order: for every request whose exact ranking no
+    rounding within the bound can change, the GPU's top-k is the exact top-k
+    (mean-key score: sum over heads of q_h . kmean; consensus: per group the
+    largest head score plus lambda x the mean, summed over groups). 12 requests of
+    256 blocks of 16 tokens, 8 KV heads, d 128, 5 % heavy-hitter blocks."""
+    import test_oracle_pins as pins
+    hkv, B, D, nb, k, W, lam = 8, 16, 128, 256, 32, 2, 0.5
+    w = Workload(layers=1, batch=12, hq=hq, hkv=hkv, head_dim=D, block_tokens=B, ntok=[nb * B] * 12, k=k, window=W,
+                 pool_slots=k + W, steps=1, seed=37, heavy_frac=0.05, select_mode=mode, lam=lam)
+    with make_pool(w) as pool:
+        if mode == pi.PI_CONSENSUS:
+            pool.set_consensus_lambda(lam)
+        prefill(pool, w)
+        om = OracleModel(w)
+        q = queries(w)[0][0]
+        sel = torch.full((w.batch, k + W), -7, dtype=torch.int32, device="cuda")
+        nsel = torch.full((w.batch,), -7, dtype=torch.int32, device="cuda")
+        pool.select_topk(0, dev(q), dev(np.full(w.batch, k, dtype=np.int32)), sel, nsel, mode=mode)
+        torch.cuda.synchronize()
+        assert pool.device_status() == pi.PI_OK
+        check_selection(sel, nsel, om.select(0, q, [k] * w.batch), 1)
+        got = sel.cpu().numpy()
+        ncand = nb - W
+        decided = 0
+        for r in range(w.batch):
+            km = om.kmean[(r, 0)][:ncand]
+            if mode == pi.PI_CONSENSUS:
+                exact, bound = pins.exact_consensus(q[r], km, lam)
+            else:
+                s64, a64 = pins._exact_scores(q[r], km)
+                G = hq // hkv
+                bound = ((G - 1) + hkv * D // 32 + 5 + 1) * 2.0 ** -24 * a64 * 1.01
+                exact = s64
+            top, ok = pins._decided_by_exact_arithmetic(exact, bound, k)
+            if ok:
+                # the W recent blocks are the highest ids; the top-k are the rest
+                assert sorted(top) == sorted(int(b) for b in got[r] if 0 <= b < ncand), r
+                decided += 1
+        assert decided >= w.batch // 2
+        print(f"{decided}/{w.batch} requests decided by exact arithmetic")
+
+
 @pytest.mark.parametrize("fused", [False, True], ids=["separate", "fused"])
 @pytest.mark.parametrize("mode", [pi.PI_SHARED, pi.PI_CONSENSUS, pi.PI_HEADWISE], ids=["shared", "consensus", "headwise"])
 def test_features_together(mode, fused):

@@ -716,15 +716,30 @@ def _exact_scores(q, km):
     return s, a
 
 
+def _decided_by_exact_arithmetic(exact, bound, k):
+    """The exact top-k (score desc, index asc) and whether rounding within `bound`
+    cannot change it: every member's lowest possible fp32 score stays above every
+    other candidate's highest possible one."""
+    n = len(exact)
+    order = sorted(range(n), key=lambda b: (-exact[b], b))
+    top, rest = order[:k], order[k:]
+    if not rest or not top:
+        return top, True
+    lo = min(exact[b] - bound[b] for b in top)
+    hi = max(exact[b] + bound[b] for b in rest)
+    return top, lo > hi
+
+
 def test_selection_matches_exact_arithmetic_outside_the_rounding_margin():
     """The fp32 score of every candidate lies within its rounding bound of the
     exact score (query-group sums: G - 1 roundings; the canonical dot: E/32
     sequential fused multiply-adds per lane, then a 5-level tree), and wherever
-    the exact k-th and (k+1)-th scores are further apart than their bounds the
-    fp32 top-k is the exact top-k. Llama-3-8B heads (32 q / 8 KV, d 128: E = 1024),
-    256 blocks of 16 tokens, 5 % heavy-hitter blocks, 12 (request, layer) units.
-    Also reports the margin diagnostic: the fraction of units whose k-th/(k+1)-th
-    gap is below 1e-6 relative (where fp32 and exact arithmetic may disagree)."""
+    no candidate's bound interval can cross the exact k-th/(k+1)-th boundary the
+    fp32 top-k is the exact top-k. Llama-3-8B heads (32 q / 8 KV, d 128: E =
+    1024), 256 blocks of 16 tokens, 5 % heavy-hitter blocks, 12 (request, layer)
+    units. Also reports the margin diagnostic: the fraction of units whose
+    k-th/(k+1)-th gap is below 1e-6 relative (where fp32 and exact arithmetic may
+    disagree)."""
     hq, hkv, B, D, nb, k, W = 32, 8, 16, 128, 256, 32, 2
     ntok = nb * B
     G, E = hq // hkv, hkv * D
@@ -740,14 +755,124 @@ def test_selection_matches_exact_arithmetic_outside_the_rounding_margin():
         ncand = nb - W
         bound = ((G - 1) + E // 32 + 5 + 1) * u * a64[:ncand] * 1.01
         assert np.all(np.abs(s32.astype(np.float64) - s64[:ncand]) <= bound)
-        order = sorted(range(ncand), key=lambda b: (-s64[b], b))
-        kth, nxt = order[k - 1], order[k]
-        gap = s64[kth] - s64[nxt]
-        if gap > bound[kth] + bound[nxt]:
-            assert sorted(order[:k]) == sorted(int(b) for b in sel[:k])
+        top, ok = _decided_by_exact_arithmetic(s64[:ncand], bound, k)
+        if ok:
+            assert sorted(top) == sorted(int(b) for b in sel[:k])
             decided += 1
-        if gap <= 1e-6 * max(abs(s64[kth]), 1e-30):
+        order = sorted(range(ncand), key=lambda b: (-s64[b], b))
+        gap = s64[order[k - 1]] - s64[order[k]]
+        if gap <= 1e-6 * max(abs(s64[order[k - 1]]), 1e-30):
             close += 1
     assert decided >= units // 2  # the comparison is not vacuous
     print(f"margin diagnostic: {close}/{units} units with a k-th/(k+1)-th gap below 1e-6 relative; "
           f"{decided}/{units} decided by exact arithmetic")
+
+
+# ------------------------------------------------------------------ consensus against exact arithmetic
+def exact_consensus(q, km, lam):
+    """The consensus score of the guide ("SoloHead Sparse Selection", "1. Consensus
+    Scoring Mechanism"), evaluated exactly, and a bound on any fp32 evaluation
+    that follows the fixed operation count of this library's reading.
+
+    Exact: S(h, b) = q_h . kmean[b, h // G] (bf16 x fp32 products are exact in
+    fp64; the fp64 sum of 128 of them is within 2^-46 of exact, far below the
+    fp32 bounds), c_g = max_h S + lam x (sum_h S) / G per group, score = sum_g c_g,
+    with lam taken as the fp32 value the library uses.
+
+    Bound: one standard rounding bound per operation, |fl(x op y) - (x op y)| <=
+    u |x op y| with u = 2^-24, carried through in order:
+      head score  4 fused multiply-adds per partial, then log2(D/4) additions:
+                  e_S <= (4 + log2(D/4)) u A_h, A_h = sum_d |q_hd| |kmean_gd|;
+      max         no rounding: e_M <= max_h e_S;
+      head sum    log2(P) pairwise levels (P = pow2(G)):
+                  e_sum <= sum_h e_S + log2(P) u sum_h (|S| + e_S);
+      mean        exact for a power-of-two G, else one division;
+      lam x mean, max + that: one rounding each;
+      groups      Hkv - 1 sequential additions.
+    Returns (exact [nb], bound [nb]) in fp64."""
+    qf = oracle.bf16_to_f64(q)
+    hq, D = qf.shape
+    nb, hkv, _ = km.shape
+    G = hq // hkv
+    P = 1 << (G - 1).bit_length()
+    lam = float(np.float32(lam))
+    u = 2.0 ** -24
+    slack = 1.01
+    kmf = np.repeat(km.astype(np.float64), G, axis=1)           # [nb][Hq][D]
+    S = np.einsum("hd,bhd->bh", qf, kmf).reshape(nb, hkv, G)
+    A = np.einsum("hd,bhd->bh", np.abs(qf), np.abs(kmf)).reshape(nb, hkv, G)
+    eS = (4 + int(math.log2(D // 4))) * u * A * slack
+    M = S.max(axis=2)
+    eM = eS.max(axis=2)
+    Ssum = S.sum(axis=2)
+    esum = eS.sum(axis=2) + int(math.log2(P)) * u * (np.abs(S) + eS).sum(axis=2) * slack
+    mean = Ssum / G
+    emean = esum / G
+    if P != G:
+        emean = emean + u * (np.abs(mean) + emean) * slack
+    t = lam * mean
+    et = lam * emean + u * (np.abs(t) + lam * emean) * slack
+    c = M + t
+    ec = eM + et + u * (np.abs(c) + eM + et) * slack
+    exact = c.sum(axis=1)
+    bound = ec.sum(axis=1) + (hkv - 1) * u * (np.abs(c) + ec).sum(axis=1) * slack
+    return exact, bound
+
+
+def test_exact_consensus_equals_rational_arithmetic_on_integers():
+    """The exact reference itself, on inputs whose fp64 evaluation is exact: the
+    same value as the formula in rational arithmetic (so the reference is the
+    guide's formula and not a restatement of the fp32 order)."""
+    rng_ = np.random.default_rng(77)
+    for hq, hkv, D in ((32, 8, 128), (64, 8, 128), (12, 3, 64)):
+        G = hq // hkv
+        nb = 9
+        qi = rng_.integers(-3, 4, size=(hq, D))
+        ki = rng_.integers(-8, 9, size=(nb, hkv, D))
+        q = synth.f32_to_bf16(qi.astype(np.float32))
+        km = (ki / 4.0).astype(np.float32)
+        exact, bound = exact_consensus(q, km, 0.5)
+        for b in range(nb):
+            tot = Fraction(0)
+            for g in range(hkv):
+                s_h = [Fraction(int(np.dot(qi[g * G + j], ki[b, g])), 4) for j in range(G)]
+                tot += max(s_h) + Fraction(1, 2) * sum(s_h) / G
+            assert Fraction(exact[b]) == tot
+            assert bound[b] > 0.0
+
+
+@pytest.mark.parametrize("hq", [32, 64], ids=["G4_llama8b", "G8_llama70b"])
+def test_consensus_selection_matches_exact_arithmetic_outside_the_rounding_margin(hq):
+    """The consensus ranking pinned to the formula rather than to its own fp32
+    order: every fp32 consensus score lies within its rounding bound of the exact
+    score, and wherever no candidate's bound interval can cross the exact
+    k-th/(k+1)-th boundary the fp32 top-k is the exact top-k. Llama-3-8B (G = 4)
+    and 70B (G = 8) heads, 8 KV heads, d 128, 256 blocks of 16 tokens, 5 %
+    heavy-hitter blocks, lambda 0.5, 12 (request, layer) units each. Reports the
+    margin diagnostic and how many units exact arithmetic decides."""
+    hkv, B, D, nb, k, W, lam = 8, 16, 128, 256, 32, 2, 0.5
+    ntok = nb * B
+    close = decided = 0
+    units = 12
+    worst = 0.0
+    for unit in range(units):
+        reg = synth.kv_region(37, unit % 3, unit, ntok, nb, hkv, B, D, 0.05, 2.0)
+        km = oracle.region_summaries(reg, ntok)
+        q = synth.normal_bf16(37, synth.KIND_MISC, unit, hq, hq * D).reshape(hq, D)
+        sel, s32 = oracle.select_consensus(q, km, k, W, lam, return_scores=True)
+        ncand = nb - W
+        exact, bound = exact_consensus(q, km[:ncand], lam)
+        err = np.abs(s32.astype(np.float64) - exact)
+        assert np.all(err <= bound), (unit, float((err / bound).max()))
+        worst = max(worst, float((err / bound).max()))
+        top, ok = _decided_by_exact_arithmetic(exact, bound, k)
+        if ok:
+            assert sorted(top) == sorted(int(b) for b in sel[:k])
+            decided += 1
+        order = sorted(range(ncand), key=lambda b: (-exact[b], b))
+        gap = exact[order[k - 1]] - exact[order[k]]
+        if gap <= 1e-6 * max(abs(exact[order[k - 1]]), 1e-30):
+            close += 1
+    assert decided >= units // 2  # the comparison is not vacuous
+    print(f"consensus G={hq // hkv}: margin diagnostic {close}/{units} units with a k-th/(k+1)-th gap below 1e-6 "
+          f"relative; {decided}/{units} decided by exact arithmetic; largest error / bound {worst:.3f}")
