@@ -131,11 +131,14 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def measure_h2d_peak(torch, dev) -> float:
-    """Pinned host -> device cudaMemcpyAsync of 1 GiB, best of 10 (GB/s)."""
+def measure_h2d_peak(torch, dev, numa_out=None) -> float:
+    """Pinned host -> device cudaMemcpyAsync of 1 GiB, best of 10 (GB/s). numa_out
+    (a dict) receives the NUMA placement of the pinned buffer's pages."""
     n = 1 << 30
     h = torch.empty(n, dtype=torch.uint8, pin_memory=True)
     h.fill_(1)
+    if numa_out is not None:
+        numa_out.update(numa_pages({"h2d_probe_buffer": (h.data_ptr(), n)}))
     d = torch.empty(n, dtype=torch.uint8, device=dev)
     s = torch.cuda.Stream()
     best = 0.0
@@ -149,6 +152,52 @@ def measure_h2d_peak(torch, dev) -> float:
             best = max(best, n / (e0.elapsed_time(e1) * 1e-3) / 1e9)
     del h, d
     return best
+
+
+def numa_pages(ranges):
+    """NUMA nodes holding the pages of each named host range {name: (address,
+    bytes)}: page counts per node from /proc/self/numa_maps over the mappings
+    that overlap the range (read-only queries). {name: {"N0": pages, ...}}."""
+    out = {}
+    try:
+        maps = []
+        for line in open("/proc/self/maps"):
+            a, b = line.split()[0].split("-")
+            maps.append((int(a, 16), int(b, 16)))
+        nodes_of = {}
+        for line in open("/proc/self/numa_maps"):
+            f = line.split()
+            nodes_of[int(f[0], 16)] = {kv.split("=")[0]: int(kv.split("=")[1]) for kv in f[1:]
+                                       if kv.startswith("N") and "=" in kv and kv[1:].split("=")[0].isdigit()}
+        for name, (addr, nbytes) in ranges.items():
+            tot = {}
+            for a, b in maps:
+                if a < addr + nbytes and b > addr:
+                    for k_, v_ in nodes_of.get(a, {}).items():
+                        tot[k_] = tot.get(k_, 0) + v_
+            out[name] = tot
+    except (OSError, ValueError, IndexError):
+        pass
+    return out
+
+
+def gpu_numa_affinity(gpu_index: int):
+    """The GPU's NUMA affinity column of `nvidia-smi topo -m` (a query), or None."""
+    try:
+        txt = subprocess.run(["nvidia-smi", "topo", "-m"], capture_output=True, text=True, timeout=20).stdout
+    except (OSError, subprocess.TimeoutExpired):
+        return None
+    lines = [l_ for l_ in txt.splitlines() if l_.strip()]
+    head = next((l_ for l_ in lines if "NUMA Affinity" in l_), None)
+    row = next((l_ for l_ in lines if l_.split() and l_.split()[0] == f"GPU{gpu_index}"), None)
+    if head is None or row is None:
+        return None
+    cols = [c.strip() for c in head.replace("\x1b[4m", "").replace("\x1b[0m", "").split("\t") if c.strip()]
+    vals = [c.strip() for c in row.split("\t") if c.strip()]
+    try:
+        return vals[1:][cols.index("NUMA Affinity")]
+    except (ValueError, IndexError):
+        return None
 
 
 def reduce_max(value: float, world: int, device=None) -> float:
@@ -201,20 +250,39 @@ class OracleSample:
         self.units = units
         self.B, self.hkv = cfg["block_tokens"], cfg["hkv"]
         self.state = {}
-        P_unit = cfg["pool_slots"] or (cfg["k"] + cfg["window"])
+        nb0 = -(-cfg["ntok"] // cfg["block_tokens"])
         for (r, l) in units:
             if region_source is not None:
                 reg = np.array(region_source(l, r))
             else:
                 reg = synth.kv_region(seed, l, r, cfg["ntok"], max_blocks, cfg["hkv"], cfg["block_tokens"],
                                       cfg["head_dim"], cfg["heavy"], 2.0)
-            nb0 = -(-cfg["ntok"] // cfg["block_tokens"])
             km = np.zeros((max_blocks, cfg["hkv"], cfg["head_dim"]), dtype=np.float32)
             km[:nb0] = orc.region_summaries(reg, cfg["ntok"])
-            self.state[(r, l)] = dict(region=reg, kmean=km, ntok=cfg["ntok"],
-                                      sob=np.full(max_blocks, -1, dtype=np.int32),
-                                      bos=np.full(P_unit, -1, dtype=np.int32),
-                                      pool=np.zeros((P_unit,) + reg.shape[1:], dtype=np.uint16))
+            P_unit = cfg["pool_slots"] or (cfg["k"] + cfg["window"])
+            sob = np.full(max_blocks, -1, dtype=np.int32)
+            resident = []
+            if "frac_range" in cfg:
+                # the variable-recall workload: per-request pool size and preloaded
+                # residency drawn exactly as the GPU run draws them
+                lo, hi = cfg["frac_range"]
+                f = synth.uniform_real(seed, synth.KIND_FRAC, r, 0, 0, lo, hi)
+                P_unit = max(int(math.ceil(f * nb0)), cfg["k"] + cfg["window"])
+                resident = synth.sample_sorted(seed, synth.KIND_RESIDENT, l, r, nb0, int(round(f * nb0)))
+            bos = np.full(P_unit, -1, dtype=np.int32)
+            pool = np.zeros((P_unit,) + reg.shape[1:], dtype=np.uint16)
+            for s_, b_ in enumerate(resident):
+                sob[b_], bos[s_] = s_, b_
+                pool[s_] = reg[b_]
+            self.state[(r, l)] = dict(region=reg, kmean=km, ntok=cfg["ntok"], sob=sob, bos=bos, pool=pool)
+
+    def budget(self, step_idx, l):
+        """Top-k of layer l at decode step step_idx (drawn per (layer, step) in the
+        variable-recall workload, as the GPU run draws it)."""
+        if "k_range" in self.cfg:
+            lo, hi = self.cfg["k_range"]
+            return self.synth.uniform_int(self.seed, self.synth.KIND_BUDGET, step_idx, l, 0, lo, hi)
+        return self.cfg["k"]
 
     def step(self, qs_step, step_idx, budget_s=None):
         """Run every unit (or until budget_s elapses). Returns (units done, seconds)."""
@@ -223,7 +291,8 @@ class OracleSample:
         for (r, l) in self.units:
             st = self.state[(r, l)]
             kn, vn = self.synth.token_kv(self.seed, l, r, self.cfg["ntok"] + step_idx, self.hkv, self.cfg["head_dim"])
-            st["ntok"] = oracle_unit_step(self.orc, st["region"], st["kmean"], st["ntok"], qs_step[l, r], self.cfg["k"],
+            st["ntok"] = oracle_unit_step(self.orc, st["region"], st["kmean"], st["ntok"], qs_step[l, r],
+                                          self.budget(step_idx, l),
                                           self.cfg["window"], st["sob"], st["bos"], st["pool"], kn, vn, self.hkv,
                                           self.B)
             done += 1
@@ -296,8 +365,44 @@ def cpu_baseline_all_cores(cfg, seed, max_blocks, budget_s=10.0, units_per_proc=
                       f"start-up and input generation); tokens/s = unit-steps / s / {L} layers"}
 
 
+# ------------------------------------------------------------------ measured traffic
+# Host-link and DRAM bytes per recalled block of the UVA gather, from one ncu
+# capture (counters syslts__t_sectors_srcunit_tex_aperture_sysmem_op_read_lookup_miss.sum
+# x 32 B and dram__bytes_read.sum + dram__bytes_write.sum, divided by the blocks
+# the captured launches recalled), valid only for the kernel sources whose hash
+# is recorded with it: a changed kernel reports null until it is captured again.
+GATHER_SOURCES = ["pi_gather.cuh", "pi_recall.cu", "pi_internal.cuh"]
+GATHER_TRAFFIC = None  # filled from a capture: {"sha": ..., "host_link_bytes_per_block": ..., ...}
+
+
+def sources_sha(names):
+    import hashlib
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "sparse_kv_cache_block_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def gather_traffic(blocks_per_launch: float, block_bytes: int):
+    """traffic of one gather launch scaled from the capture by the blocks it
+    recalls (the kernel reads each missing block once), or None with the reason."""
+    sha = sources_sha(GATHER_SOURCES)
+    rec = GATHER_TRAFFIC
+    if not rec or rec.get("block_bytes") != block_bytes:
+        return None, {"reason": "no capture of this kernel at this block size", "sources_sha": sha}
+    if rec["sha"] != sha:
+        return None, {"reason": "kernel changed since the capture", "sources_sha": sha, "captured_sha": rec["sha"]}
+    return rec["host_link_bytes_per_block"] * blocks_per_launch, {
+        "counter": "host-link read sectors x 32 B (syslts sysmem read misses), per launch, scaled from the capture by "
+                   "recalled blocks", "dram_bytes_per_launch": rec["dram_bytes_per_block"] * blocks_per_launch,
+        "capture": rec["capture"], "sources_sha": sha}
+
+
 # ------------------------------------------------------------------ main arm
-def run_ours(args, cfg, rank, world, local_rank):
+def run_ours(args, cfg, rank, world, local_rank, extra=False):
+    """One configuration end to end. extra = True (the additional configurations
+    of the same line): no e2e pass, no CPU legs, no eviction variant."""
     import torch
 
     import synth
@@ -316,7 +421,8 @@ def run_ours(args, cfg, rank, world, local_rank):
     seed = rank_seed(args.seed, rank)
     method = {"uva": pi.PI_RECALL_UVA, "memcpy": pi.PI_RECALL_MEMCPY, "staged": pi.PI_RECALL_STAGED}[args.method]
 
-    h2d_peak = measure_h2d_peak(torch, dev)
+    numa = {}
+    h2d_peak = measure_h2d_peak(torch, dev, numa)
     log(f"rank {rank}: pinned H2D peak {h2d_peak:.1f} GB/s")
 
     region_bytes = max_blocks * 2 * Hkv * B * D * 2
@@ -366,6 +472,20 @@ def run_ours(args, cfg, rank, world, local_rank):
                 n_res = int(round(fracs[r] * nb0))
                 pool.preload(l, r, synth.sample_sorted(seed, synth.KIND_RESIDENT, l, r, nb0, n_res))
     torch.cuda.synchronize()
+    # prefill summaries (row a-1) of layer 0 again, timed: every key of the layer is
+    # read over the host link through the mapping (the same values are rewritten)
+    e_p0, e_p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_p0.record()
+    pool.update_summaries(0, [ntok0] * R)
+    e_p1.record()
+    torch.cuda.synchronize()
+    pre_bytes = R * ntok0 * Hkv * D * 2
+    prefill = {"bytes": pre_bytes, "us": 1e3 * e_p0.elapsed_time(e_p1),
+               "host_link_gbs": pre_bytes / (e_p0.elapsed_time(e_p1) / 1e3) / 1e9,
+               "note": "pi_update_summaries over one layer (keys of every request read through the mapping), "
+                       "CUDA events"}
+    numa.update(numa_pages({"host_store": (pool.host_kv_ptr(0, 0), host_layers * R * pool.region_bytes)}))
+    numa["gpu_numa_affinity"] = gpu_numa_affinity(local_rank)
     log(f"rank {rank}: host store {host_layers * R * region_bytes / 2**30:.1f} GiB filled + summarised in "
         f"{time.time() - t0:.1f} s")
 
@@ -515,15 +635,17 @@ def run_ours(args, cfg, rank, world, local_rank):
         kernels[k_]["share"] = timing[k_]["total_ms"] / tot_ms
     dom = max(kernels, key=lambda k_: timing[k_]["total_ms"])
     dk = kernels[dom]
+    traffic, traffic_note = (gather_traffic(recalled / max(timing["gather"]["launches"], 1), BB) if dom == "gather"
+                             else (None, {"reason": "no traffic record for this kernel"}))
     roofline = {"kernel": dom, "bound": dk["bound"], "achieved": dk["achieved_gbs"], "peak": dk["peak_gbs"],
-                "unit": "GB/s", "frac": dk["frac"], "traffic": None,
+                "unit": "GB/s", "frac": dk["frac"], "traffic": traffic, "traffic_note": traffic_note,
                 "peak_source": ("pinned host->device cudaMemcpyAsync measured in this run" if dk["bound"] == "h2d"
                                 else "MEASURED_PEAKS.json hbm_gbs (measured copy)"),
                 "kernels": kernels}
 
     # ---- pass C: end to end through the host-buffer entry point
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not extra:
         qh = torch.from_numpy(qs.view(np.int16)).pin_memory()
         knh = torch.from_numpy(kn.view(np.int16)).pin_memory()
         vnh = torch.from_numpy(vn.view(np.int16)).pin_memory()
@@ -600,7 +722,7 @@ def run_ours(args, cfg, rank, world, local_rank):
 
     # ---- the other eviction policy on the same pool: flush, warm up, time K steps
     variant = None
-    if not args.no_variant and fracs is None:
+    if not args.no_variant and fracs is None and not extra:
         other = "lru" if args.evict == "ascending" else "ascending"
         pool.flush()
         pool.set_evict(pi.PI_EVICT_LRU if other == "lru" else pi.PI_EVICT_ASCENDING)
@@ -626,7 +748,7 @@ def run_ours(args, cfg, rank, world, local_rank):
     # ---- CPU oracle baseline on a bounded sample (rank 0, N = 1)
     cpu = None
     cpu_all = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not extra:
         # the live host store has the appended tokens of the GPU steps; the oracle
         # sample starts from a fresh prefill region of the same seed instead
         cpu = cpu_baseline(cfg, seed, qs, max_blocks, None, budget_s=args.cpu_budget)
@@ -676,6 +798,8 @@ def run_ours(args, cfg, rank, world, local_rank):
         "kernel_timing": "per-kernel CUDA events over a second run of K pipelined steps (pass B)",
         "pass_b_tok_s": world * R * K / pass_b_s,
         "warmup_recall_blocks": [w["fragments"] for w in warm_stats],
+        "numa": numa,
+        "prefill_summaries": prefill,
     }
     pool.close()
     return line
@@ -896,6 +1020,22 @@ def run_reference(args, cfg):
             "e2e": {"value": tok_s, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def extra_summary(lx):
+    """The figures of an additional configuration kept in the headline line."""
+    roof = lx["roofline"]
+    iso = roof.get("isolated", {})
+    return {"workload": lx["config"]["workload"], "value": lx["value"], "unit": lx["unit"],
+            "ms_per_step": lx["ms_per_step"], "steps": lx["steps"], "warmup_steps_run": lx["warmup_steps_run"],
+            "recall": lx["recall"], "clocks": lx["clocks"], "gpu_launches": lx["gpu_launches"],
+            "prefill_summaries": lx["prefill_summaries"],
+            "roofline": {"kernel": roof["kernel"], "bound": roof["bound"], "achieved": roof["achieved"],
+                         "peak": roof["peak"], "unit": roof["unit"], "frac": roof["frac"], "traffic": roof["traffic"],
+                         "kernels": {k_: {kk: v_[kk] for kk in ("avg_us", "busy_us_per_launch", "share", "frac")}
+                                     for k_, v_ in roof["kernels"].items()},
+                         "isolated": {k_: {kk: v_[kk] for kk in ("avg_us", "bytes_per_launch", "achieved_gbs", "frac")}
+                                      for k_, v_ in iso.items() if isinstance(v_, dict)}}}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -904,7 +1044,11 @@ def main():
     ap.add_argument("--warmup-s", type=float, default=1.5,
                     help="warm-up also lasts at least this many seconds of pipelined steps")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", default="c2", choices=sorted(CONFIGS))
+    ap.add_argument("--config", default="c3", choices=sorted(CONFIGS),
+                    help="headline workload (default: the variable-recall stress, the largest single-GPU one)")
+    ap.add_argument("--extra-configs", default="c2,c4",
+                    help="workloads also run after the headline and reported under extra_configs of the same line "
+                         "(no e2e pass, CPU legs or eviction variant); empty: none")
     ap.add_argument("--method", default="uva", choices=["uva", "memcpy", "staged"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--gather-ctas", type=int, default=0)
@@ -983,6 +1127,19 @@ def main():
         torch.cuda.set_device(local_rank)
         torch.distributed.init_process_group("nccl")
     line = run_ours(args, cfg, rank, world, local_rank)
+    extras = {}
+    for name in [c for c in args.extra_configs.split(",") if c and c != args.config]:
+        import torch
+        torch.cuda.empty_cache()
+        cx = dict(CONFIGS[name])
+        if args.layers:
+            cx["layers"] = args.layers
+        if args.batch:
+            cx["batch"] = args.batch
+        lx = run_ours(args, cx, rank, world, local_rank, extra=True)
+        extras[name] = extra_summary(lx)
+    if extras:
+        line["extra_configs"] = extras
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -277,7 +277,8 @@ pi_status pi_pool_admission(pi_pool* p, double link_util, int* layer, int* pinne
  * Admission", "2. IO-Adaptive Offloading Admission" (the two utilisation
  * thresholds).
  * Errors: PI_ERR_INVALID (layers <= 0, a null array or output, link_util
- * negative or NaN). */
+ * negative or NaN, last_pinned >= layers, or last_pinned >= 0 naming a layer
+ * that is not pinnable or not pinned); outputs are untouched then. */
 pi_status pi_admission_decide(int layers, const int* pinnable, const int* pinned, int last_pinned, double link_util,
                               int* layer, int* pin);
 
@@ -332,12 +333,25 @@ pi_status pi_sparse_decode(pi_pool* p, int layer, const void* q, const int* sel,
  * PI_ERR_INVALID. The first call on a device resolves the array's address on
  * that device (make it before any stream capture). Every call shares the array:
  * each call clears what must start at zero, and calls that overlap on the GPU
- * (other streams, other threads) race. A table entry outside [0, n_slots) is
- * read as slot 0 and not reported. */
+ * (other streams, other threads) race. Problems found on the device are not
+ * returned by this call (it returns once the work is enqueued); they are
+ * recorded in a status word inside the array, which the call clears when it
+ * starts and pi_sparse_decode_noalloc_status reads: a table entry outside
+ * [0, n_slots) (that block is not read: its keys and values are skipped), nsel
+ * outside [0, cap] (the request's output is zeros) or a bounded wait that ran
+ * out (the output is partial). */
 pi_status pi_sparse_decode_noalloc(const void* kv_slots, long long n_slots, int batch, int hq, int hkv,
                                    int head_dim, int block_tokens, int cap, const void* q, const int* sel,
                                    const int* slot_table, const int* nsel, const int* ntok, void* out, float* lse,
                                    pi_stream s);
+
+/* The device-side outcome of the last pi_sparse_decode_noalloc call on the
+ * current device, read once the work enqueued on s has finished (synchronizes
+ * s; allocates nothing): PI_OK, PI_ERR_DEVICE (an out-of-range table entry or
+ * selection count), PI_ERR_TIMEOUT (a bounded wait ran out), PI_ERR_STATE (no
+ * call on this device yet). Like the entry point it has no counterpart in the
+ * pages. */
+pi_status pi_sparse_decode_noalloc_status(pi_stream s);
 
 /* Attention mass a block selection keeps: a diagnostic, off the decode path.
  * For request r and query head h (group g = h / G), with z_t = q_h . K_t /
@@ -437,6 +451,18 @@ pi_status pi_pool_set_fused(pi_pool* p, int on, int ctas);
  * default: one wave at the kernel's occupancy). Clamped to what the pool's
  * scratch holds. Results change only by floating-point summation order. */
 pi_status pi_pool_set_attention(pi_pool* p, int splits);
+
+/* Shape of the selection launch (pi_select_topk and the decode step's selection).
+ * cluster = 1 (the default): each unit (a request, or a request and KV head) is
+ * one thread-block cluster whose CTAs score a share of the candidates each and
+ * store the scores in the shared memory of the cluster's first CTA, which then
+ * runs the top-k and, in the decode step, the recall plan and the token append;
+ * ctas_per_unit = CTAs per cluster (1..16; 0 = about two CTAs per SM over the
+ * launch). cluster = 0: the earlier form, where the scores go through global
+ * memory and the unit's last CTA to finish runs the top-k. Results are
+ * identical. Library tuning; the pages have no counterpart. PI_ERR_INVALID
+ * unless cluster is 0 or 1 and 0 <= ctas_per_unit <= 16. */
+pi_status pi_pool_set_selection(pi_pool* p, int cluster, int ctas_per_unit);
 
 /* How the splits of one (request, KV head) combine. on = 1 (the default): when a
  * unit has 2..8 splits they are launched as one thread-block cluster and merge

@@ -65,6 +65,13 @@ def sparse_decode_noalloc(kv_slots, n_slots: int, batch: int, hq: int, hkv: int,
                                            _ptr(lse), _stream(stream))
 
 
+def sparse_decode_noalloc_status(stream=None) -> int:
+    """pi_sparse_decode_noalloc_status: the device-side outcome of the last
+    no-allocation call on the current device (synchronizes the stream). Returns
+    the pi_status code without raising."""
+    return load().pi_sparse_decode_noalloc_status(_stream(stream))
+
+
 class Pool:
     """One pi_pool: pinned host KV store + device block pool + summaries + maps."""
 
@@ -217,6 +224,9 @@ class Pool:
 
     def set_consensus_lambda(self, lam: float):
         check(self.lib.pi_pool_set_consensus_lambda(self.h, float(lam)), "pi_pool_set_consensus_lambda")
+
+    def set_selection(self, cluster: bool = True, ctas_per_unit: int = 0):
+        check(self.lib.pi_pool_set_selection(self.h, int(bool(cluster)), int(ctas_per_unit)), "pi_pool_set_selection")
 
     def set_attention_cluster(self, on: bool):
         check(self.lib.pi_pool_set_attention_cluster(self.h, int(bool(on))), "pi_pool_set_attention_cluster")

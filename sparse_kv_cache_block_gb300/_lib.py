@@ -77,6 +77,7 @@ _SIGS = {
     "pi_pool_set_pipeline": (c_int, [_P, c_int, c_int]),
     "pi_pool_set_attention": (c_int, [_P, c_int]),
     "pi_pool_set_attention_cluster": (c_int, [_P, c_int]),
+    "pi_pool_set_selection": (c_int, [_P, c_int, c_int]),
     "pi_pool_set_schedule": (c_int, [_P, c_int, c_int]),
     "pi_pool_set_copy_streams": (c_int, [_P, c_int]),
     "pi_pool_pin_layer": (c_int, [_P, c_int, c_int]),
@@ -89,6 +90,7 @@ _SIGS = {
     "pi_attention_mass": (c_int, [_P, c_int, _P, _P, _P, c_int, _P, _P]),
     "pi_sparse_decode_noalloc": (c_int, [_P, c_ll, c_int, c_int, c_int, c_int, c_int, c_int, _P, _P, _P, _P, _P,
                                          _P, _P, _P]),
+    "pi_sparse_decode_noalloc_status": (c_int, [_P]),
     "pi_decode_step": (c_int, [_P, _P, _P, _P, _P, c_int, _P, _P, _P, _P, ctypes.POINTER(pi_step_stats)]),
     "pi_decode_step_host": (c_int, [_P, _P, _P, _P, _P, c_int, _P, _P, _P, _P]),
     "pi_pool_set_timing": (c_int, [_P, c_int]),

@@ -93,6 +93,9 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
   int* s_slot = s_blk + S::kSelCap;   // and their pool slots
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == kConsumerWarps * 32) pi_tmap_prefetch(&tmap);
+  pi_grid_dep_wait();  // selections, tables and token counts of earlier kernels are visible from here on
+  pi_grid_dep_trigger();
   const int u = p.u0 + blockIdx.y;
   const int r = u / p.Hkv, g = u % p.Hkv;
   const int su = (p.U == 1) ? r : u;
@@ -179,7 +182,10 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
       const int b = s_blk[it];
       int nv = nt - b * B;
       nv = nv > B ? B : nv;
-      if (b < 0) nv = 0;
+      // a block whose slot is out of range was flagged by the producer, which
+      // loaded slot 0 in its place to keep the barriers whole: skip its tokens
+      const int sl = s_slot[it];
+      if (b < 0 || sl < 0 || sl >= Pr) nv = 0;
       const uint32_t ks_base = pi_smem_addr(smem + s * S::kStage);
       const uint32_t vs_base = ks_base + B * D * 2;
 #pragma unroll
@@ -228,8 +234,10 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
         m1 = mn1;
         const uint32_t x0 = pi_pack_bf16(p0, p1);  // tokens t0+gid:   heads 2tig, 2tig+1
         const uint32_t x1 = pi_pack_bf16(p2, p3);  // tokens t0+gid+8
-        l0 = l0 * al0 + (pi_bf16_lo(x0) + pi_bf16_lo(x1));
-        l1 = l1 * al1 + (pi_bf16_hi(x0) + pi_bf16_hi(x1));
+        // the row sums take the fp32 weights (the log-sum-exp keeps fp32 accuracy);
+        // only the PV product sees them rounded to bf16
+        l0 = l0 * al0 + (p0 + p2);
+        l1 = l1 * al1 + (p1 + p3);
         const uint32_t b0 = pi_movmatrix_trans(x0);
         const uint32_t b1 = pi_movmatrix_trans(x1);
         {
@@ -439,30 +447,25 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
 template <int D, int B>
 cudaError_t launch_attn(pi_pool* p, const AttnParams& ap, cudaStream_t s) {
   using S = AttnShape<D, B>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attn_kernel<D, B>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
-  dim3 grid(ap.splits, ap.nunits);
-  if (ap.cluster) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = S::kSmem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = ap.splits;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, attn_kernel<D, B>, p->tmap, ap);
-  }
-  attn_kernel<D, B><<<grid, kThreads, S::kSmem, s>>>(p->tmap, ap);
-  return cudaGetLastError();
+  cudaError_t e = pi_smem_optin(reinterpret_cast<const void*>(attn_kernel<D, B>), S::kSmem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ap.splits, ap.nunits);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = S::kSmem;
+  cfg.stream = s;
+  // programmatic dependent launch: the CTAs launch and prefetch while the
+  // previous kernel on the stream drains, and wait for it before any read
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = ap.splits;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = ap.cluster ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, attn_kernel<D, B>, p->tmap, ap);
 }
 
 int attn_smem_bytes(int D, int B) {
@@ -615,18 +618,33 @@ __global__ void noalloc_prepare_kernel(unsigned char* scratch, int batch, int un
 template <int D, int B>
 cudaError_t launch_attn_noalloc(const CUtensorMap& tmap, const AttnParams& ap, int units, cudaStream_t s) {
   using S = AttnShape<D, B>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(attn_kernel<D, B>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kSmem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  cudaError_t e = pi_smem_optin(reinterpret_cast<const void*>(attn_kernel<D, B>), S::kSmem);
+  if (e != cudaSuccess) return e;
   dim3 grid(ap.splits, units);
   attn_kernel<D, B><<<grid, kThreads, S::kSmem, s>>>(tmap, ap);
   return cudaGetLastError();
 }
 
 }  // namespace
+
+extern "C" pi_status pi_sparse_decode_noalloc_status(pi_stream stream) {
+  int dev = 0;
+  PI_CUDA_TRY(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return PI_ERR_INVALID;
+  unsigned char* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    scratch = g_noalloc_ptr[dev];
+  }
+  if (!scratch) return PI_ERR_STATE;  // no call on this device yet
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  unsigned w = 0;
+  PI_CUDA_TRY(cudaMemcpyAsync(&w, scratch + NoAllocLayout::status_off, sizeof(unsigned), cudaMemcpyDeviceToHost, s));
+  PI_CUDA_TRY(cudaStreamSynchronize(s));
+  if (w & PI_DEV_BAD_INDEX) return PI_ERR_DEVICE;
+  if (w & PI_DEV_TIMEOUT) return PI_ERR_TIMEOUT;
+  return PI_OK;
+}
 
 extern "C" pi_status pi_sparse_decode_noalloc(const void* kv_slots, long long n_slots, int batch, int hq, int hkv,
                                               int head_dim, int block_tokens, int cap, const void* q, const int* sel,

@@ -33,6 +33,12 @@ enum : unsigned {
 
 void pi_note_cuda_error(cudaError_t e, const char* what, const char* file, int line);
 
+// Opt kernel `fn` in to `bytes` of dynamic shared memory (above the default 48
+// KiB) on the current device. The attribute belongs to the device's context, so
+// it is set once per (kernel, device) and again only for a larger size; safe to
+// call from several host threads.
+cudaError_t pi_smem_optin(const void* fn, int bytes);
+
 // --------------------------------------------------------------- pool
 struct pi_pool {
   pi_config cfg{};
@@ -133,6 +139,8 @@ struct pi_pool {
   // to keep attention CTAs away)
   bool gather_exclusive = true;
   bool attn_cluster = true;       // splits 2..8 of a unit merge through DSMEM in a cluster
+  bool select_cluster_on = true;  // selection as one thread-block cluster per unit (else the last-CTA form)
+  int select_cluster_ctas = 0;    // CTAs per unit of the cluster form (0 = about two CTAs per SM)
   int attn_splits = 0;            // attention split count override (0 = one wave at full occupancy)
 
   // fused selection + gather (UVA arm of the decode step): one launch per layer (or
@@ -170,8 +178,12 @@ cudaError_t pi_launch_append(pi_pool* p, int layer, const void* k_new, const voi
 // fused_table != nullptr: the last CTA of each unit also writes the recall plan and the table
 // mode: PI_SHARED / PI_CONSENSUS ranking on pools of one block set per request
 // (U = 1), PI_HEADWISE on head-wise pools; -1 = the pool's own mode
+// k_new / v_new (optional, decode step with the UVA recall): this layer's new
+// tokens, appended by the selection launch itself where it can (else by the
+// append kernel first, with the host write-through left to the gather)
 cudaError_t pi_launch_select(pi_pool* p, int layer, const void* q, const int* k_per_req, int* sel, int* nsel,
-                             cudaStream_t s, int* fused_table = nullptr, int mode = -1, int r0 = 0, int nr = -1);
+                             cudaStream_t s, int* fused_table = nullptr, int mode = -1, int r0 = 0, int nr = -1,
+                             const void* k_new = nullptr, const void* v_new = nullptr);
 cudaError_t pi_launch_plan(pi_pool* p, int layer, const int* sel, const int* nsel, int* table, cudaStream_t s);
 // selection + plan + UVA gather of requests r0 .. r0+nr-1 in one launch (decode step)
 cudaError_t pi_launch_select_gather(pi_pool* p, int layer, const void* q, const int* k_per_req, int* sel, int* nsel,
@@ -282,6 +294,11 @@ __device__ __forceinline__ void pi_tma_load_2d(void* smem_dst, const CUtensorMap
       : "memory");
 }
 
+// Fetch a tensor map (kernel parameter) into the descriptor cache ahead of its first use.
+__device__ __forceinline__ void pi_tmap_prefetch(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
 // 1D bulk copy global -> this CTA's shared memory (both addresses 16-byte
 // aligned, size a multiple of 16), completing on an mbarrier's transaction count.
 __device__ __forceinline__ void pi_bulk_load(void* smem_dst, const void* src, unsigned bytes, uint64_t* bar) {
@@ -314,6 +331,20 @@ __device__ __forceinline__ float4 pi_ld_cluster_f4(uint32_t addr) {
                : "memory");
   return v;
 }
+__device__ __forceinline__ void pi_st_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+// Programmatic dependent launch: wait until the grids this one depends on have
+// completed and their writes are visible (a no-op for a launch without the
+// attribute), and let the next grid on the stream start its own launch.
+__device__ __forceinline__ void pi_grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pi_grid_dep_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+// 4-byte asynchronous global -> shared copies (both 4-byte aligned), waited for as a group
+__device__ __forceinline__ void pi_cp_async4(void* smem_dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(pi_smem_addr(smem_dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void pi_cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void pi_cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 __device__ __forceinline__ void pi_cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }

@@ -12,6 +12,9 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
 
 #include "pi_internal.cuh"
 
@@ -20,6 +23,21 @@ static thread_local char g_last_cuda_error[256];
 void pi_note_cuda_error(cudaError_t e, const char* what, const char* file, int line) {
   snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "%s: %s (%s:%d)", cudaGetErrorString(e), what, file, line);
   if (getenv("PI_VERBOSE")) fprintf(stderr, "[pi] %s\n", g_last_cuda_error);
+}
+
+cudaError_t pi_smem_optin(const void* fn, int bytes) {
+  if (bytes <= 48 * 1024) return cudaSuccess;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, int> done;  // (kernel, device) -> bytes set
+  std::lock_guard<std::mutex> lock(mu);
+  int& have = done[std::make_pair(fn, dev)];
+  if (have >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) have = bytes;
+  return e;
 }
 
 extern "C" int pi_abi_version(void) { return PI_ABI_VERSION; }
@@ -566,6 +584,9 @@ extern "C" pi_status pi_pool_pin_layer(pi_pool* p, int layer, int pinned) {
 extern "C" pi_status pi_admission_decide(int layers, const int* pinnable, const int* pinned, int last_pinned,
                                          double link_util, int* layer, int* pin) {
   if (layers <= 0 || !pinnable || !pinned || !layer || !pin || !(link_util >= 0.0)) return PI_ERR_INVALID;
+  // the layer named as pinned last must be a pinnable layer that is still pinned
+  if (last_pinned >= layers || (last_pinned >= 0 && (!pinnable[last_pinned] || !pinned[last_pinned])))
+    return PI_ERR_INVALID;
   *layer = -1;
   *pin = 0;
   if (link_util > 0.85) {
@@ -578,7 +599,7 @@ extern "C" pi_status pi_admission_decide(int layers, const int* pinnable, const 
         break;
       }
     }
-  } else if (link_util < 0.5 && last_pinned >= 0 && last_pinned < layers) {
+  } else if (link_util < 0.5 && last_pinned >= 0) {
     *layer = last_pinned;
     *pin = 0;
   }

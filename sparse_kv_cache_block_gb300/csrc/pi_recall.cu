@@ -158,7 +158,8 @@ cudaError_t pi_launch_plan(pi_pool* p, int layer, const int* sel, const int* nse
   pp.lru_p2 = lru ? p->lru_p2 : 0;
   pp.empty_first = p->pinned_h.empty() ? 0 : p->pinned_h[layer];
   const size_t smem = pi_plan::plan_smem_bytes(p->max_blocks, p->cap, pp.lru_p2);
-  if (smem > 48 * 1024) cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e0 = pi_smem_optin(reinterpret_cast<const void*>(plan_kernel), (int)smem);
+  if (e0 != cudaSuccess) return e0;
   plan_kernel<<<(unsigned)RU, kPlanThreads, smem, s>>>(pp);
   return cudaGetLastError();
 }
@@ -206,11 +207,8 @@ GatherParams pi_gather_params(pi_pool* p, int layer) {
 
 template <int DEPTH, int THREADS>
 static cudaError_t launch_gather_t(int ctas, size_t smem, const GatherParams& g, cudaStream_t s) {
-  if (smem > 48 * 1024) {
-    cudaError_t e =
-        cudaFuncSetAttribute(gather_kernel<DEPTH, THREADS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-  }
+  cudaError_t e = pi_smem_optin(reinterpret_cast<const void*>(gather_kernel<DEPTH, THREADS>), (int)smem);
+  if (e != cudaSuccess) return e;
   gather_kernel<DEPTH, THREADS><<<ctas, THREADS, smem, s>>>(g);
   return cudaGetLastError();
 }

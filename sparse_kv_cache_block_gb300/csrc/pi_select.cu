@@ -16,6 +16,10 @@
 // A selection is a set of work items (a chunk of one unit's candidates); the
 // stand-alone kernel runs one item per CTA, the fused select + gather kernel
 // lets a few CTAs claim the items one after another and then copy the recalls.
+#include <map>
+#include <mutex>
+#include <tuple>
+
 #include "pi_gather.cuh"
 #include "pi_internal.cuh"
 #include "pi_plan.cuh"
@@ -24,10 +28,12 @@ namespace {
 
 constexpr int kSelThreads = 256;
 
-__device__ __forceinline__ float bf16_at(const uint16_t* p) { return __uint_as_float((uint32_t)(*p) << 16); }
-
 // ------------------------------------------------------------------ a-1
 // grid (blocks in range, R); one thread per 8 consecutive elements of one head.
+// The keys come from the host store through the GPU's mapping (or from device
+// memory): each thread keeps eight 16-byte token rows in flight, then adds them
+// in token order, so the sum is the sequential fp32 sum.
+constexpr int kSumDepth = 8;
 __global__ void summaries_kernel(const uint8_t* __restrict__ src, long long src_req_stride,
                                  const int* __restrict__ ntok_new, int* __restrict__ ntok, float* __restrict__ kmean,
                                  float* __restrict__ tail_sum, int layer, int L, int Hkv, int B, int D, int max_blocks,
@@ -47,24 +53,34 @@ __global__ void summaries_kernel(const uint8_t* __restrict__ src, long long src_
   float s[8];
 #pragma unroll
   for (int j = 0; j < 8; j++) s[j] = 0.0f;
-  for (int t = 0; t < nv; t++) {
-    uint4 v = *reinterpret_cast<const uint4*>(row + (size_t)t * D * 2);
-    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  for (int t0 = 0; t0 < nv; t0 += kSumDepth) {
+    uint4 v[kSumDepth];
 #pragma unroll
-    for (int j = 0; j < 4; j++) {
-      s[2 * j] = __fadd_rn(s[2 * j], pi_bf16_lo(w[j]));
-      s[2 * j + 1] = __fadd_rn(s[2 * j + 1], pi_bf16_hi(w[j]));
+    for (int k = 0; k < kSumDepth; k++)
+      if (t0 + k < nv) v[k] = pi_ld_stream(reinterpret_cast<const uint4*>(row + (size_t)(t0 + k) * D * 2));
+#pragma unroll
+    for (int k = 0; k < kSumDepth; k++) {
+      if (t0 + k >= nv) break;
+      const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll
+      for (int j = 0; j < 4; j++) {
+        s[2 * j] = __fadd_rn(s[2 * j], pi_bf16_lo(w[j]));
+        s[2 * j + 1] = __fadd_rn(s[2 * j + 1], pi_bf16_hi(w[j]));
+      }
     }
   }
   const size_t rl = (size_t)r * L + layer;
   float* km = kmean + ((rl * max_blocks + b) * Hkv + g) * D + d;
   const float fn = (float)nv;
+  float m[8];
 #pragma unroll
-  for (int j = 0; j < 8; j++) km[j] = __fdiv_rn(s[j], fn);
+  for (int j = 0; j < 8; j++) m[j] = __fdiv_rn(s[j], fn);
+  reinterpret_cast<float4*>(km)[0] = make_float4(m[0], m[1], m[2], m[3]);
+  reinterpret_cast<float4*>(km)[1] = make_float4(m[4], m[5], m[6], m[7]);
   if (b == nb - 1) {
     float* ts = tail_sum + (rl * Hkv + g) * D + d;
-#pragma unroll
-    for (int j = 0; j < 8; j++) ts[j] = s[j];
+    reinterpret_cast<float4*>(ts)[0] = make_float4(s[0], s[1], s[2], s[3]);
+    reinterpret_cast<float4*>(ts)[1] = make_float4(s[4], s[5], s[6], s[7]);
   }
 }
 
@@ -176,6 +192,10 @@ struct SelParams {
   int ring_stages;       // consensus: bulk-copy stages of 8 blocks' summaries
   int dyn_plan_off;      // bytes of dynamic shared memory before the plan scratch (consensus: ring + c_g)
   int empty_first;       // the layer is held whole in HBM
+  int q_vec;             // q is 16-byte aligned: the query sums load 16 bytes at a time
+  int binned_off;        // last-CTA top-k by value bins: its scratch (keys, bins, list, state) at this
+                         // byte offset of dynamic shared memory, sized for binned_cap candidates (0: radix)
+  int binned_cap;
 };
 
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -300,41 +320,131 @@ __device__ __forceinline__ void stage_ints(int* dst, const int* src, int n) {
 // u's candidates; the CTA that finishes the unit's last chunk then runs its
 // top-k (and, with a table, its recall plan) and returns true. Every branch is
 // uniform across the CTA; a CTA may run several items one after another.
-__device__ __forceinline__ bool select_item(const SelParams& p, const int u, const int chunk, const int nchunks) {
+// Scores of unit u's candidates [b_begin, b_end): sink(b, score) once per block,
+// from one thread. Every branch is uniform across the CTA (it synchronises).
+template <class Sink>
+__device__ __forceinline__ void select_score(const SelParams& p, const int u, const int b_begin, const int b_end,
+                                             Sink&& sink) {
   __shared__ __align__(16) float qs[1024];
-  __shared__ int hist[512];
-  __shared__ int warp_sums[kSelThreads / 32];
-  __shared__ int bcast[4];
-  extern __shared__ __align__(16) uint32_t dyn[];  // plan scratch, then the slot-map cache
+  extern __shared__ __align__(16) uint32_t dyn[];  // consensus ring + group scores first
   const int r = u / p.U;
   const int g = (p.U == 1) ? 0 : u % p.U;
   const int E = (p.U == 1) ? p.Hkv * p.D : p.D;
   const int goff = (p.U == 1) ? 0 : g * p.D;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const size_t rl = (size_t)r * p.L + p.layer;
-  const int nt = p.ntok[rl];
-  const int nb = (nt + p.B - 1) / p.B;
-  const int ncand = max(0, nb - p.W);
+  constexpr int NW = kSelThreads / 32;
+
+  // mean-key scores of one block set per request may stream the candidates'
+  // summaries through a ring of bulk-copy stages (NW blocks per stage, one per
+  // warp): the first stages are in flight while the query sums are formed
+  const bool mk_ring = !p.consensus && p.ring_stages > 0;
+  const int mk_nblk = max(0, b_end - b_begin);
+  const int mk_nst = (mk_nblk + NW - 1) / NW;
+  const int mk_stage = NW * E * 4;
+  uint8_t* mk_ring_base = reinterpret_cast<uint8_t*>(dyn);
+  uint64_t* mk_full = reinterpret_cast<uint64_t*>(mk_ring_base + (size_t)p.ring_stages * mk_stage);
+  const float* mk_src = p.kmean + (rl * p.max_blocks + (size_t)b_begin) * E;
+  auto mk_issue = [&](int it) {
+    const int st = it % p.ring_stages;
+    const unsigned bytes = (unsigned)(min(NW, mk_nblk - it * NW) * E * 4);
+    pi_mbar_arrive_expect_tx(&mk_full[st], bytes);
+    pi_bulk_load(mk_ring_base + (size_t)st * mk_stage, mk_src + (size_t)it * NW * E, bytes, &mk_full[st]);
+  };
+  if (mk_ring && threadIdx.x == 0) {
+    for (int st = 0; st < p.ring_stages; st++) pi_mbar_init(&mk_full[st], 1);
+    pi_fence_barrier_init();
+    for (int it = 0; it < min(p.ring_stages, mk_nst); it++) mk_issue(it);
+  }
 
   // qsum[e] = sum over the group's query heads (ascending) of q[h][d], fp32
-  // (the mean-key score; the consensus ranking reads the heads one by one)
-  for (int e = threadIdx.x; e < E && !p.consensus; e += kSelThreads) {
-    const int gg = (p.U == 1) ? e / p.D : g;
-    const int d = e % p.D;
-    const uint16_t* qh = p.q + ((size_t)r * p.Hq + (size_t)gg * p.G) * p.D + d;
-    float s = 0.0f;
-    for (int j = 0; j < p.G; j++) s = __fadd_rn(s, bf16_at(qh + (size_t)j * p.D));
-    qs[e] = s;
+  // (the mean-key score; the consensus ranking reads the heads one by one). A
+  // thread takes 8 consecutive elements and loads each head's 16 bytes of them
+  // at once (every load in flight before the first sum); queries that are not
+  // 16-byte aligned take the element-wise loop.
+  if (!p.consensus && p.q_vec) {
+    const int e0 = threadIdx.x * 8;
+    if (e0 < E) {
+      const int gg = (p.U == 1) ? e0 / p.D : g;
+      const uint16_t* qh = p.q + ((size_t)r * p.Hq + (size_t)gg * p.G) * p.D + e0 % p.D;
+      uint4 v[8];
+#pragma unroll
+      for (int j = 0; j < 8; j++)
+        if (j < p.G) v[j] = *reinterpret_cast<const uint4*>(qh + (size_t)j * p.D);
+      float acc[8];
+#pragma unroll
+      for (int i = 0; i < 8; i++) acc[i] = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 8; j++) {
+        if (j >= p.G) break;
+        const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+          acc[2 * i] = __fadd_rn(acc[2 * i], pi_bf16_lo(w[i]));
+          acc[2 * i + 1] = __fadd_rn(acc[2 * i + 1], pi_bf16_hi(w[i]));
+        }
+      }
+      reinterpret_cast<float4*>(qs + e0)[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      reinterpret_cast<float4*>(qs + e0)[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    }
+  } else {
+    for (int e = threadIdx.x; e < E && !p.consensus; e += kSelThreads) {
+      const int gg = (p.U == 1) ? e / p.D : g;
+      const int d = e % p.D;
+      const uint16_t* qh = p.q + ((size_t)r * p.Hq + (size_t)gg * p.G) * p.D + d;
+      float s = 0.0f;
+      for (int j = 0; j < p.G; j++) s = __fadd_rn(s, __uint_as_float((uint32_t)qh[(size_t)j * p.D] << 16));
+      qs[e] = s;
+    }
   }
   __syncthreads();
 
   // scores of this CTA's candidates: one warp per block, canonical lane order,
-  // two blocks per pass so sixteen 16-byte loads per lane are in flight
-  const int b_begin = chunk * p.bpc;
-  const int b_end = min(ncand, b_begin + p.bpc);
-  float* sc = p.scores + (size_t)u * p.max_blocks;
+  // two blocks per pass so sixteen 16-byte loads per lane are in flight (or from
+  // the ring)
   const int chunks = (E + 127) / 128;
-  constexpr int NW = kSelThreads / 32;
+  if (mk_ring) {
+    float4 qv[8];  // this lane's query sums of chunk c: elements 128c + 4 lane .. +3
+#pragma unroll
+    for (int c = 0; c < 8; c++) {
+      const int e = 128 * c + 4 * lane;
+      qv[c] = (c < chunks && e < E) ? *reinterpret_cast<const float4*>(qs + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    bool ok = true;
+    for (int it = 0; it < mk_nst; it++) {
+      const int st = it % p.ring_stages;
+      if (!pi_mbar_wait_bounded(&mk_full[st], (it / p.ring_stages) & 1, p.status)) ok = false;
+      const int nb_it = min(NW, mk_nblk - it * NW);
+      if (ok && warp < nb_it) {
+        const float* kb = reinterpret_cast<const float*>(mk_ring_base + (size_t)st * mk_stage) + (size_t)warp * E;
+        float acc = 0.0f;
+#pragma unroll
+        for (int c = 0; c < 8; c++) {
+          const int e = 128 * c + 4 * lane;
+          if (c < chunks && e < E) {
+            const float4 k4 = *reinterpret_cast<const float4*>(kb + e);
+            acc = __fmaf_rn(qv[c].x, k4.x, acc);
+            acc = __fmaf_rn(qv[c].y, k4.y, acc);
+            acc = __fmaf_rn(qv[c].z, k4.z, acc);
+            acc = __fmaf_rn(qv[c].w, k4.w, acc);
+          }
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, off));
+        if (lane == 0) sink(b_begin + it * NW + warp, acc);
+      }
+      // every warp is done with stage st: refill it (a failed wait stops the ring)
+      ok = __syncthreads_and(ok) != 0;
+      if (!ok) break;
+      if (threadIdx.x == 0 && it + p.ring_stages < mk_nst) mk_issue(it + p.ring_stages);
+    }
+    if (!ok && threadIdx.x == 0)
+      for (int it = 0; it < mk_nst; it++) pi_mbar_wait_bounded(&mk_full[it % p.ring_stages], (it / p.ring_stages) & 1, p.status);
+    __syncthreads();
+    if (threadIdx.x == 0)
+      for (int st = 0; st < p.ring_stages; st++) pi_mbar_inval(&mk_full[st]);
+    return;
+  }
   if (p.consensus) {
     // ring of bulk-copy stages of NW blocks' summaries; then the groups' c_g
     // per block in shared memory, summed over the groups at the end
@@ -407,7 +517,7 @@ __device__ __forceinline__ bool select_item(const SelParams& p, const int u, con
     for (int bl = threadIdx.x; bl < nblk; bl += kSelThreads) {
       float total = 0.0f;
       for (int g2 = 0; g2 < p.Hkv; g2++) total = __fadd_rn(total, cg_s[(size_t)bl * p.Hkv + g2]);
-      sc[b_begin + bl] = total;
+      sink(b_begin + bl, total);
     }
   }
   for (int b = b_begin + warp; b < b_end && !p.consensus; b += 2 * NW) {
@@ -448,10 +558,426 @@ __device__ __forceinline__ bool select_item(const SelParams& p, const int u, con
       acc2 = __fadd_rn(acc2, __shfl_xor_sync(0xffffffffu, acc2, off));
     }
     if (lane == 0) {
-      sc[b] = acc;
-      if (two) sc[b2] = acc2;
+      sink(b, acc);
+      if (two) sink(b2, acc2);
     }
   }
+}
+
+// Top-k by value bins (used by the last CTA of a unit and by the cluster form):
+// the candidates' scores are spread over kBins equal-width bins between their
+// minimum and maximum; a bin index never decreases as the score grows, so only
+// the bin holding the k-th largest score needs resolving further.
+constexpr int kBins = kSelThreads;  // one bin per thread
+constexpr int kExactMax = 64;       // boundary candidates ranked directly
+constexpr int kBinLevels = 6;       // bin refinements before direct ranking regardless
+
+struct FoldArgs {
+  // the decode step's append of one token per request, done by the leader CTA
+  // (nullptr k_new: no append); its host write-through rides in the gather
+  const uint8_t* k_new;
+  const uint8_t* v_new;
+  uint8_t* pool;
+  const long long* slot_base;
+  float* tail_sum;
+  int* ntok_w;
+};
+
+struct ClusterArgs {
+  int keys_off, hist_off, list_off, state_off;  // leader's scratch in dynamic shared memory (bytes)
+  int cap_keys;                                 // candidates that scratch holds
+  FoldArgs f;
+};
+
+__device__ __forceinline__ int score_bin(float v, float lo, float inv) {
+  const float x = fminf(__fmul_rn(__fsub_rn(v, lo), inv), (float)(kBins - 1));
+  return x > 0.0f ? __float2int_rz(x) : 0;
+}
+
+// min and max score over the candidates still open (state 2)
+__device__ __forceinline__ void open_range(const float* s, const uint8_t* st, int n, float* red, float& lo,
+                                           float& hi) {
+  constexpr int NW = kSelThreads / 32;
+  float a = INFINITY, b = -INFINITY;
+  for (int j = threadIdx.x; j < n; j += kSelThreads)
+    if (st[j] == 2) {
+      a = fminf(a, s[j]);
+      b = fmaxf(b, s[j]);
+    }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    a = fminf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    b = fmaxf(b, __shfl_xor_sync(0xffffffffu, b, o));
+  }
+  if ((threadIdx.x & 31) == 0) {
+    red[threadIdx.x >> 5] = a;
+    red[NW + (threadIdx.x >> 5)] = b;
+  }
+  __syncthreads();
+  a = INFINITY;
+  b = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < NW; w++) {
+    a = fminf(a, red[w]);
+    b = fmaxf(b, red[NW + w]);
+  }
+  __syncthreads();
+  lo = a;
+  hi = b;
+}
+
+// The kk largest of s[0..n) (ties: lower index), written ascending to out.
+// st: n bytes of state (0 out, 1 taken, 2 open); hist: kBins ints per warp;
+// list: 2n ints (8-byte aligned). Every thread of the CTA calls it. Returns the
+// count written.
+__device__ int topk_binned(const float* s, int n, int kk, uint8_t* st, int* hist, int* list, int* warp_sums,
+                           int* bc, float* red, int* out) {
+  constexpr int NW = kSelThreads / 32;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint8_t init = (kk >= n) ? 1 : (kk <= 0 ? 0 : 2);
+  int need = (init == 2) ? kk : 0;
+  bool equal_open = false;  // every open candidate has the same score
+  // the state of every candidate and the range of the open ones in one pass
+  float lo, hi;
+  {
+    float a = INFINITY, b = -INFINITY;
+    for (int j = tid; j < n; j += kSelThreads) {
+      st[j] = init;
+      a = fminf(a, s[j]);
+      b = fmaxf(b, s[j]);
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      a = fminf(a, __shfl_xor_sync(0xffffffffu, a, o));
+      b = fmaxf(b, __shfl_xor_sync(0xffffffffu, b, o));
+    }
+    if (lane == 0) {
+      red[warp] = a;
+      red[NW + warp] = b;
+    }
+    __syncthreads();
+    a = INFINITY;
+    b = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NW; w++) {
+      a = fminf(a, red[w]);
+      b = fmaxf(b, red[NW + w]);
+    }
+    lo = a;
+    hi = b;
+    __syncthreads();  // red is reused below
+  }
+  for (int level = 0; need > 0; level++) {
+    if (level > 0) open_range(s, st, n, red, lo, hi);
+    if (!(lo < hi)) {
+      equal_open = true;
+      break;
+    }
+    if (level >= kBinLevels) break;
+    const float inv = __fdiv_rn((float)kBins, __fsub_rn(hi, lo));
+    // one histogram per warp (its atomics never queue behind another warp's),
+    // then thread b adds bin b over the warps
+#pragma unroll
+    for (int w = 0; w < NW; w++) hist[w * kBins + tid] = 0;
+    __syncthreads();
+    for (int j = tid; j < n; j += kSelThreads)
+      if (st[j] == 2) atomicAdd(&hist[warp * kBins + score_bin(s[j], lo, inv)], 1);
+    __syncthreads();
+    {
+      int c = 0;
+#pragma unroll
+      for (int w = 0; w < NW; w++) c += hist[w * kBins + tid];
+      hist[tid] = c;  // bin tid of warp 0's histogram, read only by this thread above
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // boundary bin: count(bins above) < need <= count(bins above) + its own;
+      // lane i holds bins 255-8i .. 248-8i (descending)
+      int cnt[8], own = 0;
+#pragma unroll
+      for (int t = 0; t < 8; t++) {
+        cnt[t] = hist[kBins - 1 - 8 * lane - t];
+        own += cnt[t];
+      }
+      int incl = own;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const unsigned hit = __ballot_sync(0xffffffffu, incl >= need);
+      if (lane == __ffs(hit) - 1) {
+        int acc = incl - own;
+#pragma unroll
+        for (int t = 0; t < 8; t++) {
+          if (acc + cnt[t] >= need) {
+            bc[0] = kBins - 1 - 8 * lane - t;
+            bc[1] = acc;
+            bc[2] = cnt[t];
+            break;
+          }
+          acc += cnt[t];
+        }
+      }
+    }
+    __syncthreads();
+    const int tb = bc[0], above = bc[1], m = bc[2];
+    for (int j = tid; j < n; j += kSelThreads)
+      if (st[j] == 2) {
+        const int bn = score_bin(s[j], lo, inv);
+        st[j] = (bn > tb) ? 1 : (bn == tb ? 2 : 0);
+      }
+    need -= above;
+    __syncthreads();  // bc and st are read by every thread before they change again
+    if (need == m) {
+      for (int j = tid; j < n; j += kSelThreads)
+        if (st[j] == 2) st[j] = 1;
+      need = 0;
+      __syncthreads();
+    }
+    if (m <= kExactMax) break;
+  }
+  const int per = (n + kSelThreads - 1) / kSelThreads;
+  const int j0 = min(n, tid * per), j1 = min(n, j0 + per);
+  if (need > 0 && equal_open) {
+    // equal scores: the lowest indices go first
+    int c = 0;
+    for (int j = j0; j < j1; j++) c += (st[j] == 2) ? 1 : 0;
+    int tot;
+    int before = pi_plan::cta_excl_scan<kSelThreads>(c, warp_sums, tot);
+    for (int j = j0; j < j1; j++)
+      if (st[j] == 2) st[j] = (before++ < need) ? 1 : 0;
+    __syncthreads();
+  } else if (need > 0) {
+    // few open candidates: rank each against the others directly, from a list
+    // of (score, index) pairs (one shared load per comparison, eight in flight)
+    if (tid == 0) bc[3] = 0;
+    __syncthreads();
+    float2* pairs = reinterpret_cast<float2*>(list);  // list holds 2n ints
+    for (int j = tid; j < n; j += kSelThreads)
+      if (st[j] == 2) pairs[atomicAdd(&bc[3], 1)] = make_float2(s[j], __int_as_float(j));
+    __syncthreads();
+    const int m = bc[3];
+    for (int i = tid; i < m; i += kSelThreads) {
+      const float2 me = pairs[i];
+      const int j = __float_as_int(me.y);
+      int rank = 0;
+      int x = 0;
+      for (; x + 8 <= m; x += 8) {
+        float2 o[8];
+#pragma unroll
+        for (int t = 0; t < 8; t++) o[t] = pairs[x + t];
+#pragma unroll
+        for (int t = 0; t < 8; t++)
+          rank += (o[t].x > me.x || (o[t].x == me.x && __float_as_int(o[t].y) < j)) ? 1 : 0;
+      }
+      for (; x < m; x++) {
+        const float2 o = pairs[x];
+        rank += (o.x > me.x || (o.x == me.x && __float_as_int(o.y) < j)) ? 1 : 0;
+      }
+      st[j] = (rank < need) ? 1 : 0;
+    }
+    __syncthreads();
+  }
+  // ascending output of the taken candidates
+  int c = 0;
+  for (int j = j0; j < j1; j++) c += (st[j] == 1) ? 1 : 0;
+  int tot;
+  int pos = pi_plan::cta_excl_scan<kSelThreads>(c, warp_sums, tot);
+  for (int j = j0; j < j1; j++)
+    if (st[j] == 1 && pos < kk) out[pos++] = j;
+  return tot;
+}
+
+// Candidates a thread keeps in registers in the register form of the top-k
+// (up to kRegKeys * kSelThreads = 4096 candidates).
+constexpr int kRegKeys = 16;
+
+// The same top-k with every candidate's score in registers: thread t owns
+// candidates [t*per, t*per + per) of [0, n) in v[0..per), so every pass over
+// the candidates is register work and the output is one scan. flag: n bytes;
+// pairs: n (score, index) pairs; hist: kBins ints per warp. Returns the count
+// written to out.
+__device__ int topk_regs(int n, int kk, const float (&v)[kRegKeys], int per, int* hist, float2* pairs,
+                         uint8_t* flag, int* warp_sums, int* bc, float* red, int* out) {
+  constexpr int NW = kSelThreads / 32;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int j0 = tid * per;
+  unsigned valid = 0;
+#pragma unroll
+  for (int i = 0; i < kRegKeys; i++)
+    if (i < per && j0 + i < n) valid |= 1u << i;
+  unsigned open = 0, taken = 0;
+  int need = 0;
+  if (kk >= n) {
+    taken = valid;
+  } else if (kk > 0) {
+    open = valid;
+    need = kk;
+  }
+  bool equal_open = false;
+  for (int level = 0; need > 0; level++) {
+    float a = INFINITY, b = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < kRegKeys; i++)
+      if (open & (1u << i)) {
+        a = fminf(a, v[i]);
+        b = fmaxf(b, v[i]);
+      }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      a = fminf(a, __shfl_xor_sync(0xffffffffu, a, o));
+      b = fmaxf(b, __shfl_xor_sync(0xffffffffu, b, o));
+    }
+    if (lane == 0) {
+      red[warp] = a;
+      red[NW + warp] = b;
+    }
+#pragma unroll
+    for (int w = 0; w < NW; w++) hist[w * kBins + tid] = 0;
+    __syncthreads();
+    float lo = INFINITY, hi = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NW; w++) {
+      lo = fminf(lo, red[w]);
+      hi = fmaxf(hi, red[NW + w]);
+    }
+    if (!(lo < hi)) {
+      equal_open = true;
+      break;
+    }
+    if (level >= kBinLevels) break;
+    const float inv = __fdiv_rn((float)kBins, __fsub_rn(hi, lo));
+    int bins[kRegKeys];
+#pragma unroll
+    for (int i = 0; i < kRegKeys; i++) {
+      bins[i] = score_bin(v[i], lo, inv);
+      if (open & (1u << i)) atomicAdd(&hist[warp * kBins + bins[i]], 1);
+    }
+    __syncthreads();
+    {
+      int c = 0;
+#pragma unroll
+      for (int w = 0; w < NW; w++) c += hist[w * kBins + tid];
+      hist[tid] = c;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      int cnt[8], own = 0;
+#pragma unroll
+      for (int t = 0; t < 8; t++) {
+        cnt[t] = hist[kBins - 1 - 8 * lane - t];
+        own += cnt[t];
+      }
+      int incl = own;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const unsigned hit = __ballot_sync(0xffffffffu, incl >= need);
+      if (lane == __ffs(hit) - 1) {
+        int acc = incl - own;
+#pragma unroll
+        for (int t = 0; t < 8; t++) {
+          if (acc + cnt[t] >= need) {
+            bc[0] = kBins - 1 - 8 * lane - t;
+            bc[1] = acc;
+            bc[2] = cnt[t];
+            break;
+          }
+          acc += cnt[t];
+        }
+      }
+    }
+    __syncthreads();
+    const int tb = bc[0], above = bc[1], m = bc[2];
+#pragma unroll
+    for (int i = 0; i < kRegKeys; i++)
+      if (open & (1u << i)) {
+        if (bins[i] > tb) taken |= 1u << i;
+        if (bins[i] != tb) open &= ~(1u << i);
+      }
+    need -= above;
+    __syncthreads();  // red, hist and bc are rewritten by the next level
+    if (need == m) {
+      taken |= open;
+      open = 0;
+      need = 0;
+    }
+    if (m <= kExactMax) break;
+  }
+  if (need > 0 && equal_open) {
+    // equal scores: the lowest indices go first
+    int tot;
+    int before = pi_plan::cta_excl_scan<kSelThreads>(__popc(open), warp_sums, tot);
+#pragma unroll
+    for (int i = 0; i < kRegKeys; i++)
+      if (open & (1u << i)) {
+        if (before < need) taken |= 1u << i;
+        before++;
+      }
+    open = 0;
+  } else if (need > 0) {
+    // few open candidates: rank each against the others directly
+    if (tid == 0) bc[3] = 0;
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < kRegKeys; i++)
+      if (open & (1u << i)) pairs[atomicAdd(&bc[3], 1)] = make_float2(v[i], __int_as_float(j0 + i));
+    __syncthreads();
+    const int m = bc[3];
+    for (int x0 = tid; x0 < m; x0 += kSelThreads) {
+      const float2 me = pairs[x0];
+      const int j = __float_as_int(me.y);
+      int rank = 0;
+      int x = 0;
+      for (; x + 8 <= m; x += 8) {
+        float2 o[8];
+#pragma unroll
+        for (int t = 0; t < 8; t++) o[t] = pairs[x + t];
+#pragma unroll
+        for (int t = 0; t < 8; t++)
+          rank += (o[t].x > me.x || (o[t].x == me.x && __float_as_int(o[t].y) < j)) ? 1 : 0;
+      }
+      for (; x < m; x++) {
+        const float2 o = pairs[x];
+        rank += (o.x > me.x || (o.x == me.x && __float_as_int(o.y) < j)) ? 1 : 0;
+      }
+      flag[j] = (rank < need) ? 1 : 0;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < kRegKeys; i++)
+      if ((open & (1u << i)) && flag[j0 + i]) taken |= 1u << i;
+  }
+  // ascending output of the taken candidates
+  int tot;
+  int pos = pi_plan::cta_excl_scan<kSelThreads>(__popc(taken), warp_sums, tot);
+#pragma unroll
+  for (int i = 0; i < kRegKeys; i++)
+    if ((taken & (1u << i)) && pos < kk) out[pos++] = j0 + i;
+  return tot;
+}
+
+__device__ __forceinline__ bool select_item(const SelParams& p, const int u, const int chunk, const int nchunks) {
+  __shared__ int hist[512];
+  __shared__ int warp_sums[kSelThreads / 32];
+  __shared__ int bcast[4];
+  extern __shared__ __align__(16) uint32_t dyn[];  // plan scratch, then the slot-map cache
+  const int r = u / p.U;
+  const int g = (p.U == 1) ? 0 : u % p.U;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const size_t rl = (size_t)r * p.L + p.layer;
+  const int nt = p.ntok[rl];
+  const int nb = (nt + p.B - 1) / p.B;
+  const int ncand = max(0, nb - p.W);
+  const int kreq_early = p.k_per_req[r];  // read now: the tail needs it right away
+
+  const int b_begin = chunk * p.bpc;
+  const int b_end = min(ncand, b_begin + p.bpc);
+  float* sc = p.scores + (size_t)u * p.max_blocks;
+  select_score(p, u, b_begin, b_end, [&](int b, float v) { sc[b] = v; });
 
   // the last CTA of this unit to finish runs the top-k
   __threadfence();
@@ -465,9 +991,7 @@ __device__ __forceinline__ bool select_item(const SelParams& p, const int u, con
   if (threadIdx.x == 0) p.counter[u] = 0;  // ready for the next call
   __threadfence();
 
-  int kreq = p.k_per_req[r];
-  kreq = max(0, min(kreq, p.k_max));
-  const int kk = min(kreq, ncand);
+  const int kk = min(max(0, min(kreq_early, p.k_max)), ncand);
   int* out = p.sel + (size_t)u * p.cap;
   // fused plan: read this unit's slot maps now (one round of loads, held in
   // registers, then stored), so the plan runs from shared memory
@@ -483,6 +1007,47 @@ __device__ __forceinline__ bool select_item(const SelParams& p, const int u, con
     stage_ints<kKeysPerThread>(sob_c, p.slot_of + rlu_m * p.max_blocks, nb);
     stage_ints<kKeysPerThread>(bos_c, p.block_of + rlu_m * p.p_max, P_r);
   }
+  int out_n = 0;
+  if (p.binned_off > 0 && ncand <= p.binned_cap && ncand <= kRegKeys * kSelThreads) {
+    // every score straight into registers (each thread a contiguous run), then
+    // the binned top-k on them
+    uint8_t* bsm = reinterpret_cast<uint8_t*>(dyn) + p.binned_off;
+    const int capk = (p.binned_cap + 3) & ~3;
+    constexpr size_t hist_bytes = (size_t)kBins * 4 * (kSelThreads / 32);
+    const int per = (((ncand + kSelThreads - 1) / kSelThreads) + 3) & ~3;
+    const int j0 = threadIdx.x * per;
+    float v[kRegKeys];
+#pragma unroll
+    for (int i = 0; i < kRegKeys; i++) v[i] = (i < per && j0 + i < ncand) ? __ldcg(sc + j0 + i) : 0.0f;
+    out_n = topk_regs(ncand, kk, v, per, reinterpret_cast<int*>(bsm + (size_t)capk * 4),
+                      reinterpret_cast<float2*>(bsm + (size_t)capk * 4 + hist_bytes),
+                      bsm + (size_t)capk * 4 + hist_bytes + (size_t)capk * 8, warp_sums, bcast,
+                      reinterpret_cast<float*>(hist), out);
+  } else if (p.binned_off > 0 && ncand <= p.binned_cap) {
+    // every score into shared memory in one round of loads, then the binned top-k
+    uint8_t* bsm = reinterpret_cast<uint8_t*>(dyn) + p.binned_off;
+    float* keys = reinterpret_cast<float*>(bsm);
+    const int capk = (p.binned_cap + 3) & ~3;
+    for (int base = 0; base < ncand; base += kSelThreads * 8) {
+      float v[8];
+#pragma unroll
+      for (int i = 0; i < 8; i++) {
+        const int b = base + threadIdx.x + i * kSelThreads;
+        v[i] = (b < ncand) ? __ldcg(sc + b) : 0.0f;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; i++) {
+        const int b = base + threadIdx.x + i * kSelThreads;
+        if (b < ncand) keys[b] = v[i];
+      }
+    }
+    __syncthreads();
+    constexpr size_t hist_bytes = (size_t)kBins * 4 * (kSelThreads / 32);
+    out_n = topk_binned(keys, ncand, kk, bsm + (size_t)capk * 4 + hist_bytes + (size_t)capk * 8,
+                        reinterpret_cast<int*>(bsm + (size_t)capk * 4),
+                        reinterpret_cast<int*>(bsm + (size_t)capk * 4 + hist_bytes), warp_sums, bcast,
+                        reinterpret_cast<float*>(hist), out);
+  } else {
   // candidate keys: up to kKeysPerThread per thread in registers, each thread
   // owning a contiguous run of block ids; more candidates than that are read
   // from the score buffer where they are used
@@ -579,7 +1144,6 @@ __device__ __forceinline__ bool select_item(const SelParams& p, const int u, con
   }
 
   // stable compaction in block order: all keys > T, then the first need_eq == T
-  int out_n = 0;
   if (kk > 0 && in_regs) {
     // one scan of (greater, equal) counts per thread, then each thread places
     // its own run in order
@@ -632,6 +1196,7 @@ __device__ __forceinline__ bool select_item(const SelParams& p, const int u, con
       eq_seen += eq_total;
     }
   }
+  }  // radix path
   // the W most recent blocks follow (they are the highest block ids)
   const int nrecent = nb - ncand;
   for (int j = threadIdx.x; j < nrecent; j += kSelThreads) out[kk + j] = ncand + j;
@@ -725,6 +1290,177 @@ __global__ void __launch_bounds__(kSelThreads) select_gather_kernel(SelParams p,
   }
 }
 
+// ------------------------------------------------------------------ a-2 in clusters
+// The selection of one unit as one thread-block cluster of cs CTAs: CTA c scores
+// candidates [c*bpc, (c+1)*bpc) and stores each score straight into the shared
+// memory of the cluster's first CTA (the leader); after one cluster barrier the
+// leader holds every score of the unit and runs the top-k (and, in the decode
+// step, the recall plan) from shared memory. Nothing goes through global memory
+// and no CTA has to find out it finished last.
+//
+// Top-k by value bins: the candidates' scores are spread over kBins equal-width
+// bins between their minimum and maximum; a bin index is a non-decreasing
+// function of the score (subtraction, multiplication and truncation rounded in
+// one direction), so every candidate in a bin above the one holding the k-th
+// largest score is taken, every one below is not, and only the boundary bin is
+// resolved further: again by bins, or, once few candidates are left, by ranking
+// them exactly by (score descending, block index ascending).
+// The decode step's append for request r (leader CTA): the token at position t
+// goes into its block's pool slot when that block is resident (a block recalled
+// in this step gets it from the gather instead), and the block's running key sum
+// and summary take it (the same fp32 arithmetic as the stand-alone append).
+__device__ __forceinline__ void fold_append(const SelParams& p, const FoldArgs& f, int r, size_t rl, int t) {
+  const int b = t / p.B, tp = t % p.B;
+  if (b >= p.max_blocks) {
+    if (threadIdx.x == 0) pi_flag(p.status, PI_DEV_BAD_INDEX);
+    return;
+  }
+  const size_t block_bytes = (size_t)p.Hkv * 2 * p.B * p.D * 2;
+  const int slot = p.slot_of[rl * p.max_blocks + b];
+  const int P_r = p.P[rl];
+  for (int e = threadIdx.x * 8; e < p.Hkv * p.D; e += kSelThreads * 8) {
+    const int g = e / p.D, d = e % p.D;
+    const uint4 kv = *reinterpret_cast<const uint4*>(f.k_new + (((size_t)r * p.Hkv + g) * p.D + d) * 2);
+    if (slot >= 0) {
+      if (slot >= P_r) {
+        pi_flag(p.status, PI_DEV_BAD_INDEX);
+      } else {
+        const uint4 vv = *reinterpret_cast<const uint4*>(f.v_new + (((size_t)r * p.Hkv + g) * p.D + d) * 2);
+        uint8_t* blk = f.pool + (size_t)(f.slot_base[rl] + slot) * block_bytes;
+        *reinterpret_cast<uint4*>(blk + ((((size_t)g * 2 + 0) * p.B + tp) * p.D + d) * 2) = kv;
+        *reinterpret_cast<uint4*>(blk + ((((size_t)g * 2 + 1) * p.B + tp) * p.D + d) * 2) = vv;
+      }
+    }
+    float* ts = f.tail_sum + (rl * p.Hkv + g) * p.D + d;
+    float* km = const_cast<float*>(p.kmean) + ((rl * p.max_blocks + b) * p.Hkv + g) * p.D + d;
+    const uint32_t w[4] = {kv.x, kv.y, kv.z, kv.w};
+    const float fn = (float)(tp + 1);
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+      float s0 = (tp == 0) ? 0.0f : ts[2 * j];
+      float s1 = (tp == 0) ? 0.0f : ts[2 * j + 1];
+      s0 = __fadd_rn(s0, pi_bf16_lo(w[j]));
+      s1 = __fadd_rn(s1, pi_bf16_hi(w[j]));
+      ts[2 * j] = s0;
+      ts[2 * j + 1] = s1;
+      km[2 * j] = __fdiv_rn(s0, fn);
+      km[2 * j + 1] = __fdiv_rn(s1, fn);
+    }
+  }
+}
+
+// grid (cs, units), cluster (cs, 1, 1): CTA blockIdx.x of unit p.u0 + blockIdx.y
+__global__ void __launch_bounds__(kSelThreads) select_cluster_kernel(SelParams p, ClusterArgs c) {
+  __shared__ int warp_sums[kSelThreads / 32];
+  __shared__ int bc[4];
+  __shared__ float red[2 * (kSelThreads / 32)];
+  extern __shared__ __align__(16) uint32_t dyn[];
+  pi_grid_dep_wait();  // what earlier kernels wrote (token counts, summaries, maps) is visible from here on
+  const int u = p.u0 + blockIdx.y;
+  const int rank = blockIdx.x;
+  const bool leader = rank == 0;
+  const int r = u / p.U;
+  const int g = (p.U == 1) ? 0 : u % p.U;
+  const size_t rl = (size_t)r * p.L + p.layer;
+  const bool fold = c.f.k_new != nullptr;
+  const int nt_old = p.ntok[rl];
+  const int nt = nt_old + (fold ? 1 : 0);
+  const int nb = (nt + p.B - 1) / p.B;
+  int ncand = max(0, nb - p.W);
+  if (ncand > c.cap_keys || ncand > (int)gridDim.x * p.bpc) {
+    // more candidates than the launch was sized for (a token count the host did
+    // not know of): flagged, and only the first ones compete
+    if (threadIdx.x == 0) pi_flag(p.status, PI_DEV_BAD_INDEX);
+    ncand = min(c.cap_keys, (int)gridDim.x * p.bpc);
+  }
+  uint8_t* sm = reinterpret_cast<uint8_t*>(dyn);
+  float* keys = reinterpret_cast<float*>(sm + c.keys_off);
+  const int kreq_early = leader ? p.k_per_req[r] : 0;  // read now: the tail needs it right away
+
+  // leader: this unit's slot maps into shared memory, in flight during the scoring
+  const size_t rlu = rl * p.U + g;
+  const int P_r = p.P[rl];
+  int* sob_c = nullptr;
+  int* bos_c = nullptr;
+  if (leader && p.table && p.map_cache_blocks >= nb && p.map_cache_slots >= P_r) {
+    uint8_t* after = sm + p.dyn_plan_off + pi_plan::plan_smem_bytes(p.max_blocks, p.cap, p.slot_stamp ? p.lru_p2 : 0);
+    sob_c = reinterpret_cast<int*>(after);
+    bos_c = sob_c + p.map_cache_blocks;
+    for (int i = threadIdx.x; i < nb; i += kSelThreads) pi_cp_async4(sob_c + i, p.slot_of + rlu * p.max_blocks + i);
+    for (int i = threadIdx.x; i < P_r; i += kSelThreads) pi_cp_async4(bos_c + i, p.block_of + rlu * p.p_max + i);
+    pi_cp_async_commit();
+  }
+  if (leader && fold) fold_append(p, c.f, r, rl, nt_old);
+
+  // this CTA's candidates, scored into the leader's key array
+  const int b_begin = rank * p.bpc;
+  const int b_end = min(ncand, b_begin + p.bpc);
+  const uint32_t keys_leader = pi_cluster_map(pi_smem_addr(keys), 0);
+  select_score(p, u, b_begin, b_end, [&](int b, float v) { pi_st_cluster_f32(keys_leader + 4u * (uint32_t)b, v); });
+  pi_grid_dep_trigger();
+  pi_cluster_sync();  // every score of the unit is in the leader's shared memory
+  if (!leader) return;
+  if (fold && threadIdx.x == 0) c.f.ntok_w[rl] = nt;  // every CTA of the unit has read the old count
+
+  const int kk = min(max(0, min(kreq_early, p.k_max)), ncand);
+  int* out = p.sel + (size_t)u * p.cap;
+  int out_n;
+  if (ncand <= kRegKeys * kSelThreads) {
+    // the keys into registers (a contiguous run per thread, 16-byte loads)
+    const int per = (((ncand + kSelThreads - 1) / kSelThreads) + 3) & ~3;
+    const int j0 = threadIdx.x * per;
+    float v[kRegKeys];
+#pragma unroll
+    for (int q4 = 0; q4 < kRegKeys / 4; q4++) {
+      float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (4 * q4 < per && j0 + 4 * q4 < ncand) f = *reinterpret_cast<const float4*>(keys + j0 + 4 * q4);
+      v[4 * q4] = f.x;
+      v[4 * q4 + 1] = f.y;
+      v[4 * q4 + 2] = f.z;
+      v[4 * q4 + 3] = f.w;
+    }
+    out_n = topk_regs(ncand, kk, v, per, reinterpret_cast<int*>(sm + c.hist_off),
+                      reinterpret_cast<float2*>(sm + c.list_off), reinterpret_cast<uint8_t*>(sm + c.state_off),
+                      warp_sums, bc, red, out);
+  } else {
+    out_n = topk_binned(keys, ncand, kk, reinterpret_cast<uint8_t*>(sm + c.state_off),
+                        reinterpret_cast<int*>(sm + c.hist_off), reinterpret_cast<int*>(sm + c.list_off), warp_sums,
+                        bc, red, out);
+  }
+  const int nrecent = min(nb, p.W);  // the W most recent blocks follow (the highest ids)
+  for (int j = threadIdx.x; j < nrecent; j += kSelThreads) out[kk + j] = nb - nrecent + j;
+  if (threadIdx.x == 0) {
+    if (out_n != kk) pi_flag(p.status, PI_DEV_BAD_INDEX);
+    p.nsel[u] = kk + nrecent;
+  }
+  if (p.table == nullptr) return;
+
+  // recall plan of this unit from shared memory
+  pi_cp_async_wait_all();
+  __syncthreads();  // the selection and the cached maps are visible to every thread
+  const int words = (p.max_blocks + 31) / 32;
+  unsigned char* plb = sm + p.dyn_plan_off;
+  unsigned long long* lkeys = reinterpret_cast<unsigned long long*>(plb);
+  uint32_t* pl = reinterpret_cast<uint32_t*>(plb + sizeof(unsigned long long) * (p.slot_stamp ? p.lru_p2 : 0));
+  pi_plan::UnitArgs a;
+  a.sel = out;
+  a.n = kk + nrecent;
+  a.sob = sob_c ? sob_c : p.slot_of + rlu * p.max_blocks;
+  a.bos = bos_c ? bos_c : p.block_of + rlu * p.p_max;
+  a.P = P_r;
+  a.max_blocks = p.max_blocks;
+  a.table = p.table + (size_t)u * p.cap;
+  a.plan = p.plan + (size_t)u * p.cap;
+  a.plan_n = p.plan_n + u;
+  a.counts = p.counts;
+  a.status = p.status;
+  a.stamp = p.slot_stamp ? p.slot_stamp + rlu * p.p_max : nullptr;
+  a.epoch = p.slot_stamp ? p.epoch + rlu : nullptr;
+  a.empty_first = p.empty_first;
+  pi_plan::plan_unit<kSelThreads>(a, pl, reinterpret_cast<int*>(pl) + words, reinterpret_cast<int*>(pl) + words + p.cap,
+                                  warp_sums, lkeys, p.lru_p2);
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------------- launchers
@@ -772,12 +1508,22 @@ cudaError_t pi_launch_append(pi_pool* p, int layer, const void* k_new, const voi
   return cudaGetLastError();
 }
 
+// Largest candidate count the binned top-k takes (every score, a state byte and
+// a list entry per candidate in shared memory).
+constexpr int kClusterMaxCand = 16384;
+// Up to this many candidates per unit the cluster form is used by default
+// (measured faster there); more candidates keep the last-CTA form, whose launch
+// spreads evenly over every SM (a unit's cluster holds at most 16 CTAs, so few
+// units with many candidates leave SMs idle or need a second wave of clusters).
+constexpr int kClusterFormMaxCand = 1024;
+
 // Parameters, chunk count and dynamic shared memory of a selection launch over
 // requests r0 .. r0+nr-1 whose grid should hold about `target` CTAs.
 static void prepare_select(pi_pool* p, int layer, const void* q, const int* k_per_req, int* sel, int* nsel,
                            int* fused_table, int mode, int r0, int nr, long long target, SelParams& sp, int& chunks,
-                           size_t& smem) {
+                           size_t& smem, int* ncand_out = nullptr) {
   sp.q = (const uint16_t*)q;
+  sp.q_vec = (reinterpret_cast<uintptr_t>(q) & 15) == 0 ? 1 : 0;
   sp.k_per_req = k_per_req;
   sp.sel = sel;
   sp.nsel = nsel;
@@ -806,6 +1552,7 @@ static void prepare_select(pi_pool* p, int layer, const void* q, const int* k_pe
     nb_max = max(nb_max, (nt + p->B - 1) / p->B);
   }
   const int ncand_max = max(0, nb_max - p->W);
+  if (ncand_out) *ncand_out = ncand_max;
   // about `target` CTAs, at least 8 blocks (one per warp) each (rounded down:
   // one more chunk per unit would spill into a second wave)
   const long long units_launch = (long long)nr * p->U;
@@ -837,6 +1584,13 @@ static void prepare_select(pi_pool* p, int layer, const void* q, const int* k_pe
     const int stage_bytes = 8 * p->Hkv * p->D * 4;
     sp.ring_stages = max(2, min(8, 65536 / stage_bytes));
     sp.dyn_plan_off = sp.ring_stages * stage_bytes + sp.ring_stages * 8 + ((bpc * p->Hkv * 4 + 15) & ~15);
+  } else if (p->U == 1) {
+    // mean-key scores: a ring of bulk-copy stages (about 96 KiB in flight per CTA,
+    // two CTAs per SM), so the loads of a CTA never wait for its arithmetic and
+    // an SM keeps enough bytes in flight to cover the latency of a loaded HBM
+    const int stage_bytes = 8 * p->Hkv * p->D * 4;
+    sp.ring_stages = max(2, min(8, 98304 / stage_bytes));
+    sp.dyn_plan_off = (sp.ring_stages * stage_bytes + sp.ring_stages * 8 + 15) & ~15;
   }
   smem = sp.dyn_plan_off;
   if (fused_table) smem += pi_plan::plan_smem_bytes(p->max_blocks, p->cap, sp.lru_p2);
@@ -849,24 +1603,172 @@ static void prepare_select(pi_pool* p, int layer, const void* q, const int* k_pe
     sp.map_cache_slots = (p->p_max + 3) & ~3;
     smem += sizeof(int) * (size_t)(sp.map_cache_blocks + sp.map_cache_slots);
   }
+  // the last CTA's top-k by value bins: keys, bins, list and state bytes, in the
+  // score ring when it is large enough (the ring is idle once the scores are
+  // written), else after everything else
+  sp.binned_off = 0;
+  sp.binned_cap = 0;
+  if (ncand_max <= kClusterMaxCand) {
+    const size_t capk = (size_t)((ncand_max + 3) & ~3);
+    const size_t need = capk * 4 + (size_t)kBins * 4 * (kSelThreads / 32) + capk * 8 + ((capk + 15) & ~(size_t)15);
+    sp.binned_cap = (int)capk;
+    if (sp.ring_stages > 0 && 16 + need <= (size_t)sp.dyn_plan_off - (size_t)sp.ring_stages * 8 -
+                                               (sp.consensus ? (size_t)((bpc * p->Hkv * 4 + 15) & ~15) : 0)) {
+      sp.binned_off = 16;  // offset 0 means "radix"
+    } else {
+      smem = (smem + 15) & ~(size_t)15;
+      if (smem == 0) smem = 16;
+      sp.binned_off = (int)smem;
+      smem += need;
+    }
+  }
   sp.u0 = r0 * p->U;
 }
 
+
+// How many clusters of cs CTAs with smem bytes each can be resident at once
+// (0: none), cached per device, cluster size and shared-memory size.
+static int select_cluster_capacity(int cs, size_t smem) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  static std::mutex mu;
+  static std::map<std::tuple<int, int, size_t>, int> known;
+  std::lock_guard<std::mutex> lock(mu);
+  auto key = std::make_tuple(dev, cs, smem);
+  auto it = known.find(key);
+  if (it != known.end()) return it->second;
+  int n = 0;
+  bool ok = pi_smem_optin(reinterpret_cast<const void*>(select_cluster_kernel), (int)smem) == cudaSuccess;
+  if (ok && cs > 8)
+    ok = cudaFuncSetAttribute(select_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+         cudaSuccess;
+  if (ok) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cs, 1);
+    cfg.blockDim = dim3(kSelThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, select_cluster_kernel, &cfg) != cudaSuccess) n = 0;
+  }
+  cudaGetLastError();  // a refused size is not an error of the next call
+  known[key] = n;
+  return n;
+}
+
 cudaError_t pi_launch_select(pi_pool* p, int layer, const void* q, const int* k_per_req, int* sel, int* nsel,
-                             cudaStream_t s, int* fused_table, int mode, int r0, int nr) {
+                             cudaStream_t s, int* fused_table, int mode, int r0, int nr, const void* k_new,
+                             const void* v_new) {
   if (mode < 0) mode = p->mode;
   if (nr < 0) nr = p->R;
   if (nr == 0) return cudaSuccess;
   SelParams sp;
-  int chunks = 1;
+  int chunks = 1, ncand_max = 0;
   size_t smem = 0;
   // enough CTAs to cover every SM twice
-  prepare_select(p, layer, q, k_per_req, sel, nsel, fused_table, mode, r0, nr, 2LL * p->num_sms, sp, chunks, smem);
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  prepare_select(p, layer, q, k_per_req, sel, nsel, fused_table, mode, r0, nr, 2LL * p->num_sms, sp, chunks, smem,
+                 &ncand_max);
+  const long long units = (long long)nr * p->U;
+  // the append folds into the cluster launch for one block set per request with a
+  // recent window (the new token's block is then never a candidate); otherwise
+  // the append kernel runs first
+  const bool fold = k_new && p->U == 1 && p->W >= 1;
+  if (k_new && !fold) {
+    cudaError_t e = pi_launch_append(p, layer, k_new, v_new, s, false, r0, nr);
     if (e != cudaSuccess) return e;
   }
-  dim3 grid(chunks, (unsigned)(nr * p->U));
+  if (p->select_cluster_on &&
+      ncand_max <= (p->select_cluster_ctas > 0 ? kClusterMaxCand : kClusterFormMaxCand)) {
+    const int cap_c = (ncand_max + 3) & ~3;
+    SelParams sc = sp;
+    ClusterArgs ca;
+    ca.cap_keys = cap_c;
+    ca.f.k_new = fold ? (const uint8_t*)k_new : nullptr;
+    ca.f.v_new = fold ? (const uint8_t*)v_new : nullptr;
+    ca.f.pool = p->pool;
+    ca.f.slot_base = p->slot_base;
+    ca.f.tail_sum = p->tail_sum;
+    ca.f.ntok_w = p->ntok;
+    // mean-key scores of one block set per request stream through a ring of
+    // bulk-copy stages of 8 blocks (about 160 KiB in flight: one CTA per SM);
+    // the consensus score (G x the arithmetic) and head-wise units (strided
+    // summary rows) keep two CTAs per SM
+    const bool ring = !sc.consensus && p->U == 1;
+    const int stage_bytes = 8 * p->Hkv * p->D * 4;
+    if (ring) sc.ring_stages = max(2, min(8, 163840 / stage_bytes));
+    const long long per_sm = ring ? 1 : 2;
+    // dynamic shared memory for bpc candidates per CTA: the score ring (and the
+    // consensus group scores, sized by bpc), the plan scratch and slot-map cache
+    // (leader), then the leader's keys, bins, list and state
+    auto layout = [&](int bpc_) -> size_t {
+      sc.bpc = bpc_;
+      size_t off = 0;
+      if (sc.consensus) {
+        sc.dyn_plan_off = sc.ring_stages * stage_bytes + sc.ring_stages * 8 + ((bpc_ * p->Hkv * 4 + 15) & ~15);
+        off = sc.dyn_plan_off;
+      } else if (ring) {
+        sc.dyn_plan_off = (sc.ring_stages * stage_bytes + sc.ring_stages * 8 + 15) & ~15;
+        off = sc.dyn_plan_off;
+      }
+      if (fused_table) off += pi_plan::plan_smem_bytes(p->max_blocks, p->cap, sc.lru_p2);
+      off += sizeof(int) * (size_t)(sc.map_cache_blocks + sc.map_cache_slots);
+      off = (off + 15) & ~(size_t)15;
+      ca.keys_off = (int)off;
+      off += (size_t)cap_c * 4;
+      ca.hist_off = (int)off;
+      off += (size_t)kBins * 4 * (kSelThreads / 32);
+      ca.list_off = (int)off;
+      off += (size_t)cap_c * 8;
+      ca.state_off = (int)off;
+      off += ((size_t)cap_c + 15) & ~(size_t)15;
+      return off;
+    };
+    // one cluster of cs CTAs per unit: cs up to 16 with the launch's CTAs about
+    // per_sm per SM and at least 8 candidates per CTA, then as large as still
+    // lets every cluster of the launch be resident at once (the clusters need
+    // no second wave)
+    int cs = 1;
+    while (cs < 16 && units * (cs * 2) <= per_sm * p->num_sms && (cs * 2) * 8 <= ncand_max) cs *= 2;
+    if (p->select_cluster_ctas > 0) cs = max(1, min(p->select_cluster_ctas, (ncand_max + 7) / 8));
+    for (; cs >= 1; cs = (cs > 1 ? cs / 2 : 0)) {
+      const int bpc = ((((max(ncand_max, 1) + cs - 1) / cs) + 7) / 8) * 8;
+      const int cs_used = max(1, (ncand_max + bpc - 1) / bpc);
+      const size_t dsm = layout(bpc);
+      if (dsm > 220 * 1024) continue;
+      const int cap_clusters = select_cluster_capacity(cs_used, dsm);
+      if (cap_clusters <= 0) continue;
+      // a launch larger than one wave of clusters is still correct (clusters
+      // wait for room); prefer a smaller cluster that fits in one wave
+      if (cs_used > 1 && units > cap_clusters && p->select_cluster_ctas == 0) continue;
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(cs_used, (unsigned)units);
+      cfg.blockDim = dim3(kSelThreads);
+      cfg.dynamicSmemBytes = dsm;
+      cfg.stream = s;
+      cudaLaunchAttribute attr[2];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = cs_used;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[1].val.programmaticStreamSerializationAllowed = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 2;
+      return cudaLaunchKernelEx(&cfg, select_cluster_kernel, sc, ca);
+    }
+  }
+  if (fold) {
+    cudaError_t e = pi_launch_append(p, layer, k_new, v_new, s, false, r0, nr);
+    if (e != cudaSuccess) return e;
+  }
+  cudaError_t e0 = pi_smem_optin(reinterpret_cast<const void*>(select_kernel), (int)smem);
+  if (e0 != cudaSuccess) return e0;
+  dim3 grid(chunks, (unsigned)units);
   select_kernel<<<grid, kSelThreads, smem, s>>>(sp);
   return cudaGetLastError();
 }
@@ -897,11 +1799,8 @@ cudaError_t pi_launch_select_gather(pi_pool* p, int layer, const void* q, const 
   f.claim_base = p->fused_base[ci];
   f.ready = p->fused_ready + (size_t)layer * p->R * p->U;
   f.epoch = ++p->fused_epoch[layer];
-  if (smem > 48 * 1024) {
-    cudaError_t e =
-        cudaFuncSetAttribute(select_gather_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-  }
+  cudaError_t e0 = pi_smem_optin(reinterpret_cast<const void*>(select_gather_kernel), (int)smem);
+  if (e0 != cudaSuccess) return e0;
   select_gather_kernel<<<ctas, kSelThreads, smem, s>>>(sp, g, f);
   cudaError_t e = cudaGetLastError();
   // every CTA claims until a claim fails: the counter grows by the items plus one per CTA

@@ -71,16 +71,21 @@ static pi_status step_impl(pi_pool* p, const uint8_t* q_all, const uint8_t* k_ne
   // fused: selection, plan and gather of a layer run as one launch on the copy
   // stream (the compute stream keeps only the append)
   const bool fused = uva && p->fused_on;
+  // UVA arm, separate selection: the selection launch appends the new tokens
+  // itself (its leader CTAs), so the compute stream's chain starts with it
+  const bool fold = append && uva && !fused;
   auto select = [&](int l) -> pi_status {
-    if (append) {
+    if (append && !fold)
       PI_TIMED(l, PI_K_APPEND, cs,
                pi_launch_append(p, l, k_new_all + (size_t)l * kv_bytes, v_new_all + (size_t)l * kv_bytes, cs, !uva));
+    if (append)
       for (int r = 0; r < p->R; r++) p->ntok_h[(size_t)r * p->L + l] += 1;
-    }
     if (!fused)
       PI_TIMED(l, PI_K_SELECT, cs,
                pi_launch_select(p, l, q_all + (size_t)l * q_bytes, k_budget + (size_t)l * p->R, sel_of(l), nsel_of(l),
-                                cs, uva ? tab_of(l) : nullptr));
+                                cs, uva ? tab_of(l) : nullptr, -1, 0, -1,
+                                fold ? k_new_all + (size_t)l * kv_bytes : nullptr,
+                                fold ? v_new_all + (size_t)l * kv_bytes : nullptr));
     PI_CUDA_TRY(cudaEventRecord(p->ev_sel[l], cs));
     return PI_OK;
   };
@@ -386,6 +391,13 @@ extern "C" pi_status pi_pool_set_schedule(pi_pool* p, int dependent, int groups)
 extern "C" pi_status pi_pool_set_attention_cluster(pi_pool* p, int on) {
   if (!p || (on != 0 && on != 1)) return PI_ERR_INVALID;
   p->attn_cluster = on != 0;
+  return PI_OK;
+}
+
+extern "C" pi_status pi_pool_set_selection(pi_pool* p, int cluster, int ctas_per_unit) {
+  if (!p || (cluster != 0 && cluster != 1) || ctas_per_unit < 0 || ctas_per_unit > 16) return PI_ERR_INVALID;
+  p->select_cluster_on = cluster != 0;
+  p->select_cluster_ctas = ctas_per_unit;
   return PI_OK;
 }
 

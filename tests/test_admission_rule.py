@@ -76,3 +76,14 @@ def test_invalid_arguments(lib):
     a = (ctypes.c_int * 2)(1, 1)
     assert lib.pi_admission_decide(2, ctypes.cast(a, ctypes.c_void_p), None, -1, 0.9, ctypes.byref(layer),
                                    ctypes.byref(pin)) == pi.PI_ERR_INVALID
+
+
+def test_stale_last_pinned_layer_is_rejected(lib):
+    """A controller that names as pinned last a layer that is not pinned (or has
+    no reserved room, or does not exist) gets PI_ERR_INVALID, not a release."""
+    pinnable = [1, 1, 0, 1]
+    assert decide(lib, pinnable, [1, 0, 0, 0], 1, 0.1)[0] == pi.PI_ERR_INVALID   # layer 1 is not pinned
+    assert decide(lib, pinnable, [1, 0, 1, 0], 2, 0.1)[0] == pi.PI_ERR_INVALID   # layer 2 has no room
+    assert decide(lib, pinnable, [1, 0, 0, 0], 4, 0.1)[0] == pi.PI_ERR_INVALID   # no layer 4
+    assert decide(lib, pinnable, [1, 0, 0, 0], 1, 0.9)[0] == pi.PI_ERR_INVALID   # checked whatever the load
+    assert decide(lib, pinnable, [1, 0, 0, 0], 0, 0.1) == (pi.PI_OK, 0, 0)
