@@ -371,8 +371,13 @@ def cpu_baseline_all_cores(cfg, seed, max_blocks, budget_s=10.0, units_per_proc=
 # x 32 B and dram__bytes_read.sum + dram__bytes_write.sum, divided by the blocks
 # the captured launches recalled), valid only for the kernel sources whose hash
 # is recorded with it: a changed kernel reports null until it is captured again.
-GATHER_SOURCES = ["pi_gather.cuh", "pi_recall.cu", "pi_internal.cuh"]
-GATHER_TRAFFIC = None  # filled from a capture: {"sha": ..., "host_link_bytes_per_block": ..., ...}
+GATHER_SOURCES = ["pi_gather.cuh", "pi_recall.cu"]
+GATHER_TRAFFIC = {
+    # ncu --set full of two gather launches of the variable-recall workload (2 layers,
+    # batch 8): 999424 and 1302528 host-link read sectors for 122 and 159 recalled
+    # 256 KiB blocks; DRAM 0.29 and 1.21 MB (the blocks land in L2)
+    "sha": "9a4d8195ce0349e6", "block_bytes": 262144, "host_link_bytes_per_block": 262144.0,
+    "dram_bytes_per_block": 1499648 / 281, "capture": "profiles/gather_kernel_uva_variable_recall.md"}
 
 
 def sources_sha(names):
@@ -474,16 +479,19 @@ def run_ours(args, cfg, rank, world, local_rank, extra=False):
     torch.cuda.synchronize()
     # prefill summaries (row a-1) of layer 0 again, timed: every key of the layer is
     # read over the host link through the mapping (the same values are rewritten)
-    e_p0, e_p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e_p0.record()
-    pool.update_summaries(0, [ntok0] * R)
-    e_p1.record()
-    torch.cuda.synchronize()
+    pre_ms = []
+    for _ in range(3):
+        e_p0, e_p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e_p0.record()
+        pool.update_summaries(0, [ntok0] * R)
+        e_p1.record()
+        torch.cuda.synchronize()
+        pre_ms.append(e_p0.elapsed_time(e_p1))
     pre_bytes = R * ntok0 * Hkv * D * 2
-    prefill = {"bytes": pre_bytes, "us": 1e3 * e_p0.elapsed_time(e_p1),
-               "host_link_gbs": pre_bytes / (e_p0.elapsed_time(e_p1) / 1e3) / 1e9,
+    prefill = {"bytes": pre_bytes, "us": 1e3 * min(pre_ms), "us_all": [1e3 * x for x in pre_ms],
+               "host_link_gbs": pre_bytes / (min(pre_ms) / 1e3) / 1e9,
                "note": "pi_update_summaries over one layer (keys of every request read through the mapping), "
-                       "CUDA events"}
+                       "CUDA events, best of 3"}
     numa.update(numa_pages({"host_store": (pool.host_kv_ptr(0, 0), host_layers * R * pool.region_bytes)}))
     numa["gpu_numa_affinity"] = gpu_numa_affinity(local_rank)
     log(f"rank {rank}: host store {host_layers * R * region_bytes / 2**30:.1f} GiB filled + summarised in "
