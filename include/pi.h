@@ -144,6 +144,9 @@ typedef struct pi_pool_views {
                                 the room of a pinned layer) */
   const int* capacity_rl;    /* host [batch][layers]: slots reserved for (r, l) */
   long long total_slots;     /* slots of the whole pool */
+  const unsigned* dev_status;/* device: the sticky status word's raw bits (1 an index out of
+                                range, 2 a bounded wait ran out, 4 a pool too small, 8 more work
+                                than a launch was sized for); pi_get_device_status maps them */
 } pi_pool_views;
 
 /* ------------------------------------------------------------------ lifetime */
@@ -501,7 +504,10 @@ pi_status pi_pool_get_timing(pi_pool* p, pi_kernel_timing* out);
 
 /* ------------------------------------------------------------------ status */
 /* Synchronizes the device, returns PI_OK or the first device-side error
- * (PI_ERR_DEVICE, PI_ERR_TIMEOUT, PI_ERR_POOL_FULL) recorded since the last clear. */
+ * (PI_ERR_DEVICE, PI_ERR_TIMEOUT, PI_ERR_POOL_FULL) recorded since the last clear.
+ * PI_ERR_DEVICE covers an index read from memory out of range and a kernel that
+ * met more work than its launch was sized for (in both cases the excess is
+ * skipped, never accessed). */
 pi_status pi_get_device_status(pi_pool* p);
 pi_status pi_clear_device_status(pi_pool* p);
 

@@ -150,6 +150,12 @@ class Pool:
         """Slots (r, l) uses now: P_r, or every block of a pinned layer."""
         return self._views.slots_rl[r * self.L + l]
 
+    def device_status_bits(self) -> int:
+        """The raw bits of the device status word (synchronizes the device)."""
+        import torch
+        torch.cuda.synchronize()
+        return int(device_view(self._views.dev_status, (1,), "int32").cpu()[0]) & 0xFFFFFFFF
+
     def view_kmean(self):
         return device_view(self._views.kmean, (self.R, self.L, self.max_blocks, self.Hkv, self.D), "float32")
 

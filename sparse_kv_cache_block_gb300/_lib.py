@@ -48,7 +48,7 @@ class pi_pool_views(ctypes.Structure):
                 ("p_max", c_int), ("step_sel", c_void_p), ("step_nsel", c_void_p), ("step_table", c_void_p),
                 ("block_bytes", c_size_t), ("frag_bytes", c_size_t), ("host_region_bytes", c_size_t),
                 ("slot_stamp", c_void_p), ("slots_rl", ctypes.POINTER(c_int)), ("capacity_rl", ctypes.POINTER(c_int)),
-                ("total_slots", c_ll)]
+                ("total_slots", c_ll), ("dev_status", c_void_p)]
 
 
 class pi_kernel_timing(ctypes.Structure):

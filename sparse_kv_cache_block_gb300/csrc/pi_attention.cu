@@ -445,7 +445,7 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
 }
 
 template <int D, int B>
-cudaError_t launch_attn(pi_pool* p, const AttnParams& ap, cudaStream_t s) {
+cudaError_t launch_attn(pi_pool* p, const AttnParams& ap, cudaStream_t s, bool pdl) {
   using S = AttnShape<D, B>;
   cudaError_t e = pi_smem_optin(reinterpret_cast<const void*>(attn_kernel<D, B>), S::kSmem);
   if (e != cudaSuccess) return e;
@@ -457,14 +457,21 @@ cudaError_t launch_attn(pi_pool* p, const AttnParams& ap, cudaStream_t s) {
   // programmatic dependent launch: the CTAs launch and prefetch while the
   // previous kernel on the stream drains, and wait for it before any read
   cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = ap.splits;
-  attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = 1;
+  int na = 0;
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    na++;
+  }
+  if (ap.cluster) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = ap.splits;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    na++;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = ap.cluster ? 2 : 1;
+  cfg.numAttrs = na;
   return cudaLaunchKernelEx(&cfg, attn_kernel<D, B>, p->tmap, ap);
 }
 
@@ -491,9 +498,31 @@ int attn_smem_bytes(int D, int B) {
 
 int pi_attention_smem(int D, int B) { return attn_smem_bytes(D, B); }
 
+// Load every attention kernel on the current device and opt it in to its shared
+// memory once, when a pool is created (no kernel loads or attribute changes
+// while a decode step is in flight).
+cudaError_t pi_prepare_attention_kernels() {
+  cudaError_t e = cudaSuccess;
+  auto one = [&](const void* fn, int bytes) {
+    if (e != cudaSuccess) return;
+    cudaFuncAttributes a;
+    e = cudaFuncGetAttributes(&a, fn);
+    if (e == cudaSuccess) e = pi_smem_optin(fn, bytes);
+  };
+  one(reinterpret_cast<const void*>(attn_kernel<128, 16>), AttnShape<128, 16>::kSmem);
+  one(reinterpret_cast<const void*>(attn_kernel<128, 32>), AttnShape<128, 32>::kSmem);
+  one(reinterpret_cast<const void*>(attn_kernel<128, 64>), AttnShape<128, 64>::kSmem);
+  one(reinterpret_cast<const void*>(attn_kernel<128, 128>), AttnShape<128, 128>::kSmem);
+  one(reinterpret_cast<const void*>(attn_kernel<64, 16>), AttnShape<64, 16>::kSmem);
+  one(reinterpret_cast<const void*>(attn_kernel<64, 32>), AttnShape<64, 32>::kSmem);
+  one(reinterpret_cast<const void*>(attn_kernel<64, 64>), AttnShape<64, 64>::kSmem);
+  one(reinterpret_cast<const void*>(attn_kernel<64, 128>), AttnShape<64, 128>::kSmem);
+  return e;
+}
+
 cudaError_t pi_launch_attention(pi_pool* p, int layer, const void* q, const int* sel, const int* table,
                                 const int* nsel, void* out, float* lse, float* logits, cudaStream_t s, int r0,
-                                int nr) {
+                                int nr, bool pdl) {
   if (nr < 0) nr = p->R;
   if (nr == 0) return cudaSuccess;
   AttnParams ap;
@@ -539,17 +568,17 @@ cudaError_t pi_launch_attention(pi_pool* p, int layer, const void* q, const int*
   ap.scale_log2 = ap.scale * 1.4426950408889634f;
   if (p->D == 128) {
     switch (p->B) {
-      case 16: return launch_attn<128, 16>(p, ap, s);
-      case 32: return launch_attn<128, 32>(p, ap, s);
-      case 64: return launch_attn<128, 64>(p, ap, s);
-      case 128: return launch_attn<128, 128>(p, ap, s);
+      case 16: return launch_attn<128, 16>(p, ap, s, pdl);
+      case 32: return launch_attn<128, 32>(p, ap, s, pdl);
+      case 64: return launch_attn<128, 64>(p, ap, s, pdl);
+      case 128: return launch_attn<128, 128>(p, ap, s, pdl);
     }
   } else if (p->D == 64) {
     switch (p->B) {
-      case 16: return launch_attn<64, 16>(p, ap, s);
-      case 32: return launch_attn<64, 32>(p, ap, s);
-      case 64: return launch_attn<64, 64>(p, ap, s);
-      case 128: return launch_attn<64, 128>(p, ap, s);
+      case 16: return launch_attn<64, 16>(p, ap, s, pdl);
+      case 32: return launch_attn<64, 32>(p, ap, s, pdl);
+      case 64: return launch_attn<64, 64>(p, ap, s, pdl);
+      case 128: return launch_attn<64, 128>(p, ap, s, pdl);
     }
   }
   return cudaErrorInvalidValue;

@@ -20,6 +20,7 @@ enum : unsigned {
   PI_DEV_BAD_INDEX = 1u,   // an index read from memory was out of range (access skipped)
   PI_DEV_TIMEOUT = 2u,     // a bounded wait ran out
   PI_DEV_POOL_FULL = 4u,   // plan found fewer free slots than missing units
+  PI_DEV_LAUNCH_SIZE = 8u, // a kernel met more work than its launch was sized for (the excess skipped)
 };
 
 #define PI_CUDA_TRY(expr)                                   \
@@ -181,9 +182,11 @@ cudaError_t pi_launch_append(pi_pool* p, int layer, const void* k_new, const voi
 // k_new / v_new (optional, decode step with the UVA recall): this layer's new
 // tokens, appended by the selection launch itself where it can (else by the
 // append kernel first, with the host write-through left to the gather)
+// pdl: launch with programmatic dependent launch (the stand-alone calls; the
+// decode step, whose launches are separated by stream events, does not)
 cudaError_t pi_launch_select(pi_pool* p, int layer, const void* q, const int* k_per_req, int* sel, int* nsel,
                              cudaStream_t s, int* fused_table = nullptr, int mode = -1, int r0 = 0, int nr = -1,
-                             const void* k_new = nullptr, const void* v_new = nullptr);
+                             const void* k_new = nullptr, const void* v_new = nullptr, bool pdl = true);
 cudaError_t pi_launch_plan(pi_pool* p, int layer, const int* sel, const int* nsel, int* table, cudaStream_t s);
 // selection + plan + UVA gather of requests r0 .. r0+nr-1 in one launch (decode step)
 cudaError_t pi_launch_select_gather(pi_pool* p, int layer, const void* q, const int* k_per_req, int* sel, int* nsel,
@@ -194,8 +197,11 @@ cudaError_t pi_launch_gather(pi_pool* p, int layer, const uint8_t* stage_src, bo
                              int nr = -1, bool paired = false);
 cudaError_t pi_launch_attention(pi_pool* p, int layer, const void* q, const int* sel, const int* table,
                                 const int* nsel, void* out, float* lse, float* logits, cudaStream_t s, int r0 = 0,
-                                int nr = -1);
+                                int nr = -1, bool pdl = true);
 bool pi_make_tmap(pi_pool* p);
+// load the selection / attention kernels and set their shared-memory opt-in once
+cudaError_t pi_prepare_select_kernels();
+cudaError_t pi_prepare_attention_kernels();
 int pi_attention_smem(int D, int B);  // dynamic shared memory of one attention CTA
 
 // --------------------------------------------------------------- device helpers

@@ -339,6 +339,13 @@ extern "C" pi_status pi_pool_create(const pi_config* cfg, pi_pool** out) {
     pool_free(p);
     return PI_ERR_CUDA;
   }
+  // every kernel of the decode path loaded and opted in to its shared memory now,
+  // not in the middle of a decode
+  if (pi_prepare_select_kernels() != cudaSuccess || pi_prepare_attention_kernels() != cudaSuccess) {
+    cudaGetLastError();
+    pool_free(p);
+    return PI_ERR_CUDA;
+  }
   if (cudaDeviceSynchronize() != cudaSuccess) {
     pool_free(p);
     return PI_ERR_CUDA;
@@ -368,6 +375,7 @@ extern "C" pi_status pi_pool_get_views(pi_pool* p, pi_pool_views* v) {
   v->slots_rl = p->P_rl_h.data();
   v->capacity_rl = p->cap_rl_h.data();
   v->total_slots = p->total_slots;
+  v->dev_status = p->dev_status;
   v->kmean = p->kmean;
   v->ntok = p->ntok;
   v->slot_of_block = p->slot_of;
@@ -399,7 +407,7 @@ extern "C" pi_status pi_get_device_status(pi_pool* p) {
   PI_CUDA_TRY(cudaDeviceSynchronize());
   unsigned w = 0;
   PI_CUDA_TRY(cudaMemcpy(&w, p->dev_status, sizeof(unsigned), cudaMemcpyDeviceToHost));
-  if (w & PI_DEV_BAD_INDEX) return PI_ERR_DEVICE;
+  if (w & (PI_DEV_BAD_INDEX | PI_DEV_LAUNCH_SIZE)) return PI_ERR_DEVICE;
   if (w & PI_DEV_TIMEOUT) return PI_ERR_TIMEOUT;
   if (w & PI_DEV_POOL_FULL) return PI_ERR_POOL_FULL;
   return PI_OK;

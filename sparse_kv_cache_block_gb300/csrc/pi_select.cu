@@ -351,6 +351,11 @@ __device__ __forceinline__ void select_score(const SelParams& p, const int u, co
     pi_mbar_arrive_expect_tx(&mk_full[st], bytes);
     pi_bulk_load(mk_ring_base + (size_t)st * mk_stage, mk_src + (size_t)it * NW * E, bytes, &mk_full[st]);
   };
+  if (mk_ring && b_begin + mk_nblk > p.max_blocks) {
+    // a range past the unit's summaries is never copied (recorded, nothing scored)
+    if (threadIdx.x == 0) pi_flag(p.status, PI_DEV_LAUNCH_SIZE);
+    return;
+  }
   if (mk_ring && threadIdx.x == 0) {
     for (int st = 0; st < p.ring_stages; st++) pi_mbar_init(&mk_full[st], 1);
     pi_fence_barrier_init();
@@ -970,8 +975,15 @@ __device__ __forceinline__ bool select_item(const SelParams& p, const int u, con
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const size_t rl = (size_t)r * p.L + p.layer;
   const int nt = p.ntok[rl];
-  const int nb = (nt + p.B - 1) / p.B;
-  const int ncand = max(0, nb - p.W);
+  int nb = (nt + p.B - 1) / p.B;
+  int ncand = max(0, nb - p.W);
+  if (ncand > nchunks * p.bpc || nb > p.max_blocks) {
+    // more candidates than the launch was sized for (a token count the host did
+    // not know of): flagged, and only the candidates the launch covers compete
+    if (threadIdx.x == 0) pi_flag(p.status, PI_DEV_LAUNCH_SIZE);
+    nb = min(nb, p.max_blocks);
+    ncand = min(max(0, nb - p.W), nchunks * p.bpc);
+  }
   const int kreq_early = p.k_per_req[r];  // read now: the tail needs it right away
 
   const int b_begin = chunk * p.bpc;
@@ -1370,7 +1382,7 @@ __global__ void __launch_bounds__(kSelThreads) select_cluster_kernel(SelParams p
   if (ncand > c.cap_keys || ncand > (int)gridDim.x * p.bpc) {
     // more candidates than the launch was sized for (a token count the host did
     // not know of): flagged, and only the first ones compete
-    if (threadIdx.x == 0) pi_flag(p.status, PI_DEV_BAD_INDEX);
+    if (threadIdx.x == 0) pi_flag(p.status, PI_DEV_LAUNCH_SIZE);
     ncand = min(c.cap_keys, (int)gridDim.x * p.bpc);
   }
   uint8_t* sm = reinterpret_cast<uint8_t*>(dyn);
@@ -1639,9 +1651,6 @@ static int select_cluster_capacity(int cs, size_t smem) {
   if (it != known.end()) return it->second;
   int n = 0;
   bool ok = pi_smem_optin(reinterpret_cast<const void*>(select_cluster_kernel), (int)smem) == cudaSuccess;
-  if (ok && cs > 8)
-    ok = cudaFuncSetAttribute(select_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
-         cudaSuccess;
   if (ok) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(cs, 1);
@@ -1663,7 +1672,7 @@ static int select_cluster_capacity(int cs, size_t smem) {
 
 cudaError_t pi_launch_select(pi_pool* p, int layer, const void* q, const int* k_per_req, int* sel, int* nsel,
                              cudaStream_t s, int* fused_table, int mode, int r0, int nr, const void* k_new,
-                             const void* v_new) {
+                             const void* v_new, bool pdl) {
   if (mode < 0) mode = p->mode;
   if (nr < 0) nr = p->R;
   if (nr == 0) return cudaSuccess;
@@ -1758,7 +1767,7 @@ cudaError_t pi_launch_select(pi_pool* p, int layer, const void* q, const int* k_
       attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
       attr[1].val.programmaticStreamSerializationAllowed = 1;
       cfg.attrs = attr;
-      cfg.numAttrs = 2;
+      cfg.numAttrs = pdl ? 2 : 1;
       return cudaLaunchKernelEx(&cfg, select_cluster_kernel, sc, ca);
     }
   }
@@ -1846,4 +1855,28 @@ extern "C" pi_status pi_select_topk(pi_pool* p, int layer, const void* q, const 
   if (reinterpret_cast<uintptr_t>(q) & 3) return PI_ERR_INVALID;
   PI_CUDA_TRY(pi_launch_select(p, layer, q, k_per_req, sel, nsel, reinterpret_cast<cudaStream_t>(s), nullptr, mode));
   return PI_OK;
+}
+
+// Load the selection kernels on the current device and give each the largest
+// dynamic shared memory the device allows, once, when a pool is created: a
+// later launch then never loads a kernel or changes an attribute while other
+// work of the pool is in flight (the cluster form's size changes as the
+// context grows; the last-CTA form may first run many steps into a decode).
+cudaError_t pi_prepare_select_kernels() {
+  int dev = 0, optin = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e != cudaSuccess) return e;
+  const void* fns[] = {reinterpret_cast<const void*>(summaries_kernel), reinterpret_cast<const void*>(append_kernel),
+                       reinterpret_cast<const void*>(select_kernel), reinterpret_cast<const void*>(select_gather_kernel),
+                       reinterpret_cast<const void*>(select_cluster_kernel)};
+  for (const void* fn : fns) {
+    cudaFuncAttributes a;
+    e = cudaFuncGetAttributes(&a, fn);
+    if (e != cudaSuccess) return e;
+    e = pi_smem_optin(fn, optin - (int)a.sharedSizeBytes);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaFuncSetAttribute(select_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
 }

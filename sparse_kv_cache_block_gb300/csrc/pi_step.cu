@@ -85,7 +85,7 @@ static pi_status step_impl(pi_pool* p, const uint8_t* q_all, const uint8_t* k_ne
                pi_launch_select(p, l, q_all + (size_t)l * q_bytes, k_budget + (size_t)l * p->R, sel_of(l), nsel_of(l),
                                 cs, uva ? tab_of(l) : nullptr, -1, 0, -1,
                                 fold ? k_new_all + (size_t)l * kv_bytes : nullptr,
-                                fold ? v_new_all + (size_t)l * kv_bytes : nullptr));
+                                fold ? v_new_all + (size_t)l * kv_bytes : nullptr, false));
     PI_CUDA_TRY(cudaEventRecord(p->ev_sel[l], cs));
     return PI_OK;
   };
@@ -120,7 +120,7 @@ static pi_status step_impl(pi_pool* p, const uint8_t* q_all, const uint8_t* k_ne
     PI_TIMED(l, PI_K_ATTENTION, as,
              pi_launch_attention(p, l, q_all + (size_t)l * q_bytes, sel_of(l), tab_of(l), nsel_of(l),
                                  out_all + (size_t)l * q_bytes, lse_all ? lse_all + (size_t)l * p->R * p->Hq : nullptr,
-                                 nullptr, as));
+                                 nullptr, as, 0, -1, false));
     return PI_OK;
   };
   pi_status st = PI_OK;
@@ -164,7 +164,7 @@ static pi_status step_impl(pi_pool* p, const uint8_t* q_all, const uint8_t* k_ne
         } else {
           PI_TIMED_G(l, g, PI_K_SELECT, s,
                      pi_launch_select(p, l, q_all + (size_t)l * q_bytes, k_budget + (size_t)l * p->R, sel_of(l),
-                                      nsel_of(l), s, tab_of(l), -1, r0[g], nr[g]));
+                                      nsel_of(l), s, tab_of(l), -1, r0[g], nr[g], nullptr, nullptr, false));
           PI_CUDA_TRY(cudaEventRecord(ev[0], s));
           PI_CUDA_TRY(cudaStreamWaitEvent(ys, ev[0], 0));
           PI_TIMED_G(l, g, PI_K_GATHER, ys, pi_launch_gather(p, l, nullptr, true, true, ys, kn, vn, r0[g], nr[g]));
@@ -175,7 +175,7 @@ static pi_status step_impl(pi_pool* p, const uint8_t* q_all, const uint8_t* k_ne
                    pi_launch_attention(p, l, q_all + (size_t)l * q_bytes, sel_of(l), tab_of(l), nsel_of(l),
                                        out_all + (size_t)l * q_bytes,
                                        lse_all ? lse_all + (size_t)l * p->R * p->Hq : nullptr, nullptr, s, r0[g],
-                                       nr[g]));
+                                       nr[g], false));
       }
     // the caller's compute stream completes after every group's last attention
     for (int g = 1; g < M; g++) {
