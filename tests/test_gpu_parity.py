@@ -230,6 +230,49 @@ def test_multistep_pipeline_8b_shape(method, evict, ahead, placement):
             assert st["selected"] == sum(int(nsel_v[l].sum()) for l in range(L))
 
 
+@pytest.mark.parametrize("mode", [pi.PI_SHARED, pi.PI_CONSENSUS], ids=["shared", "consensus"])
+def test_selection_form_changes_during_decode(mode):
+    """A pool whose candidate count crosses 1024 during the decode (1024 at the
+    first step, 1025 from the second): the selection runs as one cluster per
+    request, then as the last-CTA form, with the token append folded into the
+    first and done by the append kernel in the second; every layer of every step
+    against the oracle, with preloaded residency and per-request budgets."""
+    B = 16
+    ntok = (1024 + 2) * B - 1  # 1026 blocks (the last one holds 15 tokens): 1024 candidates
+    w = Workload(layers=2, batch=3, hq=8, hkv=2, head_dim=64, block_tokens=B, ntok=[ntok, ntok - 400, ntok], k=24,
+                 window=2, pool_slots=40, steps=4, rho=0.9, heavy_frac=0.05, seed=91, select_mode=mode,
+                 slots_per_req=[40, 60, 40])
+    L, R = w.layers, w.batch
+    with make_pool(w) as pool:
+        prefill(pool, w)
+        om = OracleModel(w)
+        for l in range(L):
+            blocks = synth.sample_sorted(w.seed, synth.KIND_RESIDENT, l, 0, 1026, 30)
+            pool.preload(l, 0, blocks)
+            om.preload(l, 0, blocks)
+        qs = queries(w)
+        for step in range(w.steps):
+            kn, vn = new_tokens(w, step)
+            kbud = np.full((L, R), w.k, dtype=np.int32)
+            kbud[1, 2] = 5
+            out = torch.empty((L, R, w.hq, w.head_dim), dtype=torch.int16, device="cuda")
+            lse = torch.empty((L, R, w.hq), dtype=torch.float32, device="cuda")
+            pool.decode_step(dev(qs[step]), dev(kn), dev(vn), dev(kbud), out, lse)
+            torch.cuda.synchronize()
+            assert pool.device_status() == pi.PI_OK
+            sel_v, nsel_v, tab_v = pool.view_step()
+            for l in range(L):
+                om.append(l, kn[l], vn[l])
+                ref_sel = om.select(l, qs[step][l], kbud[l])
+                check_selection(sel_v[l], nsel_v[l], ref_sel, 1)
+                ref_tab = om.recall(l, ref_sel)
+                check_tables_maps_bytes(pool, om, w, l, ref_sel, ref_tab, tab_v[l])
+                ref_out, ref_lse, _ = om.attention(l, qs[step][l], ref_sel)
+                check_attention(out[l], lse[l], ref_out, ref_lse)
+            check_kmean(pool, om, w)
+        assert om.nb(0, 0) - w.window == 1025  # the last steps ran with more than 1024 candidates
+
+
 @pytest.mark.parametrize("evict", [0, 1])
 def test_headwise_arm(evict):
     """Per-KV-head selection (the fragmenting comparison arm): own top-k per head,
