@@ -356,11 +356,15 @@ __device__ __forceinline__ void select_score(const SelParams& p, const int u, co
     if (threadIdx.x == 0) pi_flag(p.status, PI_DEV_LAUNCH_SIZE);
     return;
   }
-  if (mk_ring && threadIdx.x == 0) {
-    for (int st = 0; st < p.ring_stages; st++) pi_mbar_init(&mk_full[st], 1);
-    pi_fence_barrier_init();
-    for (int it = 0; it < min(p.ring_stages, mk_nst); it++) mk_issue(it);
-  }
+  // the ring's first stages are issued right after this thread's query loads (below),
+  // so the few query bytes do not queue behind the summaries
+  auto mk_start = [&]() {
+    if (mk_ring && threadIdx.x == 0) {
+      for (int st = 0; st < p.ring_stages; st++) pi_mbar_init(&mk_full[st], 1);
+      pi_fence_barrier_init();
+      for (int it = 0; it < min(p.ring_stages, mk_nst); it++) mk_issue(it);
+    }
+  };
 
   // qsum[e] = sum over the group's query heads (ascending) of q[h][d], fp32
   // (the mean-key score; the consensus ranking reads the heads one by one). A
@@ -376,6 +380,7 @@ __device__ __forceinline__ void select_score(const SelParams& p, const int u, co
 #pragma unroll
       for (int j = 0; j < 8; j++)
         if (j < p.G) v[j] = *reinterpret_cast<const uint4*>(qh + (size_t)j * p.D);
+      mk_start();
       float acc[8];
 #pragma unroll
       for (int i = 0; i < 8; i++) acc[i] = 0.0f;
@@ -391,8 +396,11 @@ __device__ __forceinline__ void select_score(const SelParams& p, const int u, co
       }
       reinterpret_cast<float4*>(qs + e0)[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
       reinterpret_cast<float4*>(qs + e0)[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    } else {
+      mk_start();
     }
   } else {
+    mk_start();
     for (int e = threadIdx.x; e < E && !p.consensus; e += kSelThreads) {
       const int gg = (p.U == 1) ? e / p.D : g;
       const int d = e % p.D;
