@@ -1717,7 +1717,9 @@ cudaError_t pi_launch_select(pi_pool* p, int layer, const void* q, const int* k_
     // summary rows) keep two CTAs per SM
     const bool ring = !sc.consensus && p->U == 1;
     const int stage_bytes = 8 * p->Hkv * p->D * 4;
-    if (ring) sc.ring_stages = max(2, min(8, 163840 / stage_bytes));
+    const int ring_big = max(2, min(8, 163840 / stage_bytes));   // one CTA per SM
+    const int ring_small = max(2, min(8, 65536 / stage_bytes));  // two CTAs per SM
+    if (ring) sc.ring_stages = ring_big;
     const long long per_sm = ring ? 1 : 2;
     // dynamic shared memory for bpc candidates per CTA: the score ring (and the
     // consensus group scores, sized by bpc), the plan scratch and slot-map cache
@@ -1755,13 +1757,22 @@ cudaError_t pi_launch_select(pi_pool* p, int layer, const void* q, const int* k_
     for (; cs >= 1; cs = (cs > 1 ? cs / 2 : 0)) {
       const int bpc = ((((max(ncand_max, 1) + cs - 1) / cs) + 7) / 8) * 8;
       const int cs_used = max(1, (ncand_max + bpc - 1) / bpc);
-      const size_t dsm = layout(bpc);
-      if (dsm > 220 * 1024) continue;
-      const int cap_clusters = select_cluster_capacity(cs_used, dsm);
-      if (cap_clusters <= 0) continue;
-      // a launch larger than one wave of clusters is still correct (clusters
-      // wait for room); prefer a smaller cluster that fits in one wave
-      if (cs_used > 1 && units > cap_clusters && p->select_cluster_ctas == 0) continue;
+      // the large ring first; when its clusters would not all be resident at
+      // once, the small ring (two CTAs per SM) before a smaller cluster
+      bool fits = false;
+      size_t dsm = 0;
+      for (int attempt = 0; attempt < (ring ? 2 : 1) && !fits; attempt++) {
+        if (ring) sc.ring_stages = attempt == 0 ? ring_big : ring_small;
+        dsm = layout(bpc);
+        if (dsm > 220 * 1024) continue;
+        const int cap_clusters = select_cluster_capacity(cs_used, dsm);
+        if (cap_clusters <= 0) continue;
+        // a launch larger than one wave of clusters is still correct (clusters
+        // wait for room); prefer a smaller cluster that fits in one wave
+        if (cs_used > 1 && units > cap_clusters && p->select_cluster_ctas == 0) continue;
+        fits = true;
+      }
+      if (!fits) continue;
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(cs_used, (unsigned)units);
       cfg.blockDim = dim3(kSelThreads);
