@@ -356,10 +356,13 @@ __device__ __forceinline__ void select_score(const SelParams& p, const int u, co
     if (threadIdx.x == 0) pi_flag(p.status, PI_DEV_LAUNCH_SIZE);
     return;
   }
-  // the ring's first stages are issued right after this thread's query loads (below),
-  // so the few query bytes do not queue behind the summaries
+  // the ring's first stages are issued at once by the first thread that has no
+  // query elements to load (with 16-byte query loads, thread E/8), so neither
+  // waits for the other; without such a thread, thread 0 issues them right
+  // after its query loads
+  const int ring_thread = (!p.consensus && p.q_vec && E / 8 < kSelThreads) ? E / 8 : 0;
   auto mk_start = [&]() {
-    if (mk_ring && threadIdx.x == 0) {
+    if (mk_ring && threadIdx.x == ring_thread) {
       for (int st = 0; st < p.ring_stages; st++) pi_mbar_init(&mk_full[st], 1);
       pi_fence_barrier_init();
       for (int it = 0; it < min(p.ring_stages, mk_nst); it++) mk_issue(it);

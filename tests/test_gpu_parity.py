@@ -842,6 +842,53 @@ def test_large_selection_sizes(mode):
 
 
 @pytest.mark.parametrize("mode", [pi.PI_SHARED, pi.PI_CONSENSUS], ids=["shared", "consensus"])
+@pytest.mark.parametrize("ncands", [[1, 31, 300, 701, 1024], [1500, 2000]], ids=["cluster_form", "last_cta_form"])
+def test_selection_ties_and_signed_zeros(ncands, mode):
+    """Every block's keys are one constant from {-1, -1/2, -0, +0, 1/2, 1} (exact
+    in bf16) and the query is all ones, so every score is an exact multiple of
+    its block's constant: five distinct scores among up to 2 000 candidates, and
+    blocks of -0 keys tie with blocks of +0 keys. At every budget from 0 to all
+    candidates the selection must be the oracle's (equal scores by lower index),
+    in both launch forms: up to 1 024 candidates a
+    cluster per request with the one-warp top-k (1, 31, 300, 701 and 1 024
+    candidates: one, one, two and four registers per lane, and the full 32), above
+    that the last CTA of each request. Ragged last blocks."""
+    hq, hkv, D, B, W, lam = 32, 8, 128, 16, 2, 0.5
+    R = len(ncands)
+    ntok = [B * (n + W) - 5 for n in ncands]
+    nbs = [-(-t // B) for t in ntok]
+    assert nbs == [n + W for n in ncands]
+    mb = max(nbs) + 2
+    kmax = max(ncands)
+    pool = pi.Pool(1, R, hq, hkv, D, B, mb, kmax + W, kmax, W, select_mode=mode, host_layers=1)
+    try:
+        if mode == pi.PI_CONSENSUS:
+            pool.set_consensus_lambda(lam)
+        rng = np.random.default_rng(101 + R)
+        vals = np.array([0xBF80, 0xBF00, 0x8000, 0x0000, 0x3F00, 0x3F80], dtype=np.uint16)
+        kms = []
+        for r in range(R):
+            reg = pool.host_kv(0, r)
+            reg[:] = vals[rng.integers(0, len(vals), size=mb)][:, None, None, None, None]
+            kms.append(oracle.region_summaries(reg.copy(), ntok[r]))
+        pool.update_summaries(0, ntok)
+        torch.cuda.synchronize()
+        q = np.full((R, hq, D), 0x3F80, dtype=np.uint16)
+        for k in sorted({0, 1, 17, 31, 32, 33, 64, 300, 701, kmax}):
+            sel = torch.full((R, kmax + W), -7, dtype=torch.int32, device="cuda")
+            nsel = torch.full((R,), -7, dtype=torch.int32, device="cuda")
+            pool.select_topk(0, dev(q), dev(np.full(R, k, dtype=np.int32)), sel, nsel, mode=mode)
+            if mode == pi.PI_CONSENSUS:
+                ref = [oracle.select_consensus(q[r], kms[r], k, W, lam) for r in range(R)]
+            else:
+                ref = [oracle.select_shared(q[r], kms[r], k, W) for r in range(R)]
+            check_selection(sel, nsel, ref, 1)
+        assert pool.device_status() == pi.PI_OK
+    finally:
+        pool.close()
+
+
+@pytest.mark.parametrize("mode", [pi.PI_SHARED, pi.PI_CONSENSUS], ids=["shared", "consensus"])
 @pytest.mark.parametrize("hq", [32, 64], ids=["G4_llama8b", "G8_llama70b"])
 def test_gpu_selection_matches_exact_arithmetic(mode, hq):
     """The GPU's selection against the formula evaluated exactly, not only
