@@ -575,8 +575,11 @@ def run_ours(args, cfg, rank, world, local_rank, extra=False):
         admission = {"pin_layers": args.pin_layers, "pinned": pinned_layers, "decisions": decisions}
         log(f"rank {rank}: admission pinned layers {pinned_layers} after {len(decisions)} windows")
 
-    # ---- pass A: headline, device time over K steps, no per-kernel events
+    # ---- pass A: headline, device time over K steps, no per-kernel events; the
+    # device's recall counters (read after the timed region) give the blocks these
+    # very steps recalled, so the link floor below is pass A's own
     barrier()
+    pool.recall_totals(reset=True)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local_rank) as clocks:
@@ -585,6 +588,7 @@ def run_ours(args, cfg, rank, world, local_rank, extra=False):
             run_step()
         e1.record(compute)
         torch.cuda.synchronize()
+    recalled_a, hits_a = pool.recall_totals(reset=True)
     barrier()
     elapsed = e0.elapsed_time(e1) / 1e3
     elapsed_max = reduce_max(elapsed, world, dev)
@@ -793,7 +797,14 @@ def run_ours(args, cfg, rank, world, local_rank, extra=False):
                    "frac_of_h2d_peak": (recall_gbs / h2d_peak) if recall_gbs else None,
                    "bytes_per_step": recalled * BB / K, "blocks_per_step": recalled / K,
                    "selected_per_step": selected / K,
-                   "pipelined_link_gbs": recalled * BB / pass_b_s / 1e9},
+                   "pipelined_link_gbs": recalled * BB / pass_b_s / 1e9,
+                   # the timed steps themselves (pass A): their recalled bytes over the
+                   # pinned H2D peak is the least time the host link allows per step
+                   "pass_a": {"blocks_per_step": recalled_a / K, "hits_per_step": hits_a / K,
+                              "bytes_per_step": recalled_a * BB / K,
+                              "link_floor_ms_per_step": 1e3 * recalled_a * BB / K / (h2d_peak * 1e9),
+                              "link_gbs": recalled_a * BB / elapsed_max / 1e9,
+                              "frac_of_link_floor": (recalled_a * BB / (h2d_peak * 1e9)) / elapsed_max}},
         "roofline": roofline,
         "evict_variant": variant,
         "cpu_baseline": cpu,

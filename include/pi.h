@@ -285,6 +285,15 @@ pi_status pi_pool_admission(pi_pool* p, double link_util, int* layer, int* pinne
 pi_status pi_admission_decide(int layers, const int* pinnable, const int* pinned, int last_pinned, double link_util,
                               int* layer, int* pin);
 
+/* Recall counters the device accumulates over every recall plan (the decode
+ * step's selections with plan, pi_recall) since the pool was created or last
+ * reset, summed over layers: *recalled = blocks copied into the pool (misses),
+ * *hits = selected blocks found resident. A decode step with statistics
+ * (pi_decode_step with stats) zeroes them at its start. Synchronizes the
+ * device; reset = 1 zeroes them after reading. Errors: PI_ERR_INVALID (null
+ * pool or output, reset not 0 or 1). */
+pi_status pi_pool_recall_totals(pi_pool* p, long long* recalled, long long* hits, int reset);
+
 /* Weight lambda of the group mean in the consensus score (default 0.5, the
  * guide's "typical" value; its worked example uses 1). Applies to later
  * PI_CONSENSUS selections. PI_ERR_INVALID unless 0 <= lambda <= 1e30. */

@@ -228,6 +228,13 @@ class Pool:
               "pi_pool_admission")
         return layer.value, bool(pinned.value)
 
+    def recall_totals(self, reset: bool = False) -> tuple[int, int]:
+        """(blocks recalled, hits) accumulated on the device since creation or the last reset."""
+        m, h = ctypes.c_longlong(), ctypes.c_longlong()
+        check(self.lib.pi_pool_recall_totals(self.h, ctypes.byref(m), ctypes.byref(h), int(bool(reset))),
+              "pi_pool_recall_totals")
+        return m.value, h.value
+
     def set_consensus_lambda(self, lam: float):
         check(self.lib.pi_pool_set_consensus_lambda(self.h, float(lam)), "pi_pool_set_consensus_lambda")
 

@@ -82,6 +82,7 @@ _SIGS = {
     "pi_pool_set_copy_streams": (c_int, [_P, c_int]),
     "pi_pool_pin_layer": (c_int, [_P, c_int, c_int]),
     "pi_pool_admission": (c_int, [_P, c_double, ctypes.POINTER(c_int), ctypes.POINTER(c_int)]),
+    "pi_pool_recall_totals": (c_int, [_P, ctypes.POINTER(c_ll), ctypes.POINTER(c_ll), c_int]),
     "pi_pool_set_consensus_lambda": (c_int, [_P, ctypes.c_float]),
     "pi_pool_set_fused": (c_int, [_P, c_int, c_int]),
     "pi_admission_decide": (c_int, [c_int, _P, _P, c_int, ctypes.c_double, _P, _P]),

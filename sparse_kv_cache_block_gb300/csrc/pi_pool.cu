@@ -15,6 +15,7 @@
 #include <map>
 #include <mutex>
 #include <utility>
+#include <vector>
 
 #include "pi_internal.cuh"
 
@@ -611,6 +612,22 @@ extern "C" pi_status pi_admission_decide(int layers, const int* pinnable, const 
     *layer = last_pinned;
     *pin = 0;
   }
+  return PI_OK;
+}
+
+extern "C" pi_status pi_pool_recall_totals(pi_pool* p, long long* recalled, long long* hits, int reset) {
+  if (!p || !recalled || !hits || (reset != 0 && reset != 1)) return PI_ERR_INVALID;
+  PI_CUDA_TRY(cudaDeviceSynchronize());
+  std::vector<long long> c((size_t)4 * p->L);
+  PI_CUDA_TRY(cudaMemcpy(c.data(), p->recall_counts, sizeof(long long) * c.size(), cudaMemcpyDeviceToHost));
+  long long m = 0, h = 0;
+  for (int l = 0; l < p->L; l++) {
+    m += c[(size_t)l * 4 + 0];
+    h += c[(size_t)l * 4 + 1];
+  }
+  if (reset) PI_CUDA_TRY(cudaMemset(p->recall_counts, 0, sizeof(long long) * c.size()));
+  *recalled = m;
+  *hits = h;
   return PI_OK;
 }
 

@@ -54,6 +54,7 @@ def test_host_only_calls(lib):
         "pi_pool_pin_layer": (None, 0, 1),
         "pi_pool_set_consensus_lambda": (None, 0.5),
         "pi_pool_set_attention_cluster": (None, 1),
+        "pi_pool_recall_totals": (None, None, None, 0),
     }
     for name, args in null_calls.items():
         assert getattr(lib, name)(*args) == pi.PI_ERR_INVALID, name

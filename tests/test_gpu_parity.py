@@ -359,6 +359,41 @@ def test_preload_then_recall_counts_hits(evict):
             assert stats["hits"] + stats["fragments"] == sum(len(s) for s in ref_sel)
 
 
+def test_recall_totals_accumulate_across_steps():
+    """pi_pool_recall_totals (blocks recalled and hits, summed over layers on the
+    device): over 4 decode steps without statistics they equal the sums of what
+    the per-step statistics report for the same steps on a second pool (the two
+    pools make the same selections); a reset zeroes them."""
+    w = Workload(layers=2, batch=2, hq=32, hkv=8, head_dim=128, block_tokens=64, ntok=[4000, 2500], k=8, window=2,
+                 pool_slots=14, steps=4, rho=0.9, heavy_frac=0.05, heavy_shift=2.0, seed=5)
+    L, R = w.layers, w.batch
+    qs = queries(w)
+    sums = [0, 0]
+    totals = None
+    for use_stats in (True, False):
+        with make_pool(w) as pool:
+            prefill(pool, w)
+            pool.recall_totals(reset=True)
+            compute, copy = torch.cuda.Stream(), torch.cuda.Stream()
+            for step in range(w.steps):
+                kn, vn = new_tokens(w, step)
+                kbud = np.full((L, R), w.k, dtype=np.int32)
+                out = torch.empty((L, R, w.hq, w.head_dim), dtype=torch.int16, device="cuda")
+                lse = torch.empty((L, R, w.hq), dtype=torch.float32, device="cuda")
+                st = pool.decode_step(dev(qs[step]), dev(kn), dev(vn), dev(kbud), out, lse, compute=compute,
+                                      copy=copy, stats=use_stats)
+                torch.cuda.synchronize()
+                if use_stats:
+                    sums[0] += st["fragments"]
+                    sums[1] += st["hits"]
+            if not use_stats:
+                totals = pool.recall_totals(reset=True)
+                assert pool.recall_totals() == (0, 0)
+            assert pool.device_status() == pi.PI_OK
+    assert sums[0] > 0 and sums[1] > 0
+    assert totals == (sums[0], sums[1])
+
+
 def test_decode_step_host_matches_device_inputs():
     w = Workload(layers=2, batch=2, hq=16, hkv=4, head_dim=128, block_tokens=32, ntok=[3000, 2100], k=6, window=2,
                  pool_slots=10, steps=2, seed=13)
