@@ -20,6 +20,7 @@
 // global partial buffer, finalised by the last CTA of the unit.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstdio>
 #include <mutex>
 
@@ -47,6 +48,8 @@ struct AttnParams {
   unsigned* status;
   int layer, L, Hq, Hkv, G, U, cap, splits, splits_max, bps;
   int cluster;        // 1: the splits of a unit form one thread-block cluster and merge through DSMEM
+  int push;           // with cluster: every split stores its partial into the first CTA's shared memory
+                      // (after the regular layout), which merges them alone
   int u0, nunits;     // the launch covers units u0 .. u0+nunits-1 (grid.y)
   float scale, scale_log2;
 };
@@ -303,6 +306,30 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
         }
         store_out(p, r, g * p.G + h, d, D, acc, lsum, M);
       }
+    } else if (p.cluster && p.push) {
+      // this CTA's partial goes straight into the first CTA's push region, slot =
+      // split: [splits][G][D] fp32, then [splits][G] (m, l); the cluster barrier
+      // below orders these stores before the first CTA reads them
+      const uint32_t region = pi_cluster_map(pi_smem_addr(smem_raw + S::kSmem), 0);
+      const uint32_t po_r = region + (uint32_t)(split * p.G * D) * 4u;
+      const uint32_t ml_r = region + (uint32_t)(p.splits * p.G * D) * 4u + (uint32_t)(split * p.G) * 8u;
+      for (int e = threadIdx.x; e < p.G * D; e += 128) {
+        const int h = e / D, d = e % D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; w++) M = fmaxf(M, mlw[(w * p.G + h) * 2]);
+        float acc = 0.0f, lsum = 0.0f;
+        if (M != -INFINITY) {
+#pragma unroll
+          for (int w = 0; w < kConsumerWarps; w++) {
+            const float f = pi_exp2(mlw[(w * p.G + h) * 2] - M);
+            acc += f * ow[(w * p.G + h) * D + d];
+            lsum += f * mlw[(w * p.G + h) * 2 + 1];
+          }
+        }
+        pi_st_cluster_f32(po_r + (uint32_t)e * 4u, acc);
+        if (d == 0) pi_st_cluster_f2(ml_r + (uint32_t)h * 8u, make_float2(M, lsum));
+      }
     } else if (p.cluster) {
       // this CTA's partial stays in its own shared memory; the cluster merges below
       float* cpo = reinterpret_cast<float*>(smem + S::kClusterPart);  // [G][D]
@@ -406,7 +433,39 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
     }  // more than one split
   }
   __syncthreads();
-  if (p.cluster) {
+  if (p.cluster && p.push) {
+    // the first CTA merges every split's partial from its own shared memory, in
+    // split order (the same arithmetic as the pulled merge below)
+    pi_cluster_sync();
+    if (split != 0) return;
+    const int G = p.G, ns = p.splits;
+    const float* po_s = reinterpret_cast<const float*>(smem_raw + S::kSmem);  // [ns][G][D]
+    const float2* ml_s = reinterpret_cast<const float2*>(po_s + ns * G * D);   // [ns][G]
+    for (int e4 = threadIdx.x; e4 < G * D / 4; e4 += kThreads) {
+      const int h = (4 * e4) / D, d = (4 * e4) % D;
+      float M = -INFINITY;
+      for (int c = 0; c < ns; c++) M = fmaxf(M, ml_s[c * G + h].x);
+      float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      float lsum = 0.0f;
+      if (M != -INFINITY) {
+        for (int c = 0; c < ns; c++) {
+          const float2 ml = ml_s[c * G + h];
+          const float f = pi_exp2(ml.x - M);
+          const float4 v = reinterpret_cast<const float4*>(po_s + (size_t)c * G * D)[e4];
+          acc.x += f * v.x;
+          acc.y += f * v.y;
+          acc.z += f * v.z;
+          acc.w += f * v.w;
+          lsum += f * ml.y;
+        }
+      }
+      const int hq = g * G + h;
+      store_out(p, r, hq, d, D, acc.x, lsum, M);
+      store_out(p, r, hq, d + 1, D, acc.y, lsum, M);
+      store_out(p, r, hq, d + 2, D, acc.z, lsum, M);
+      store_out(p, r, hq, d + 3, D, acc.w, lsum, M);
+    }
+  } else if (p.cluster) {
     // every CTA of the cluster (the unit's splits, rank = split) merges a slice of
     // the output from all the partials, read from the peers' shared memory
     pi_cluster_sync();
@@ -444,15 +503,24 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(const __grid_constant__ 
   }
 }
 
+// Bytes of the first CTA's push region: every split's partial [G][D] fp32 and (m, l).
+int push_bytes(int splits, int G, int D) { return splits * (G * D * 4 + G * 8); }
+
 template <int D, int B>
-cudaError_t launch_attn(pi_pool* p, const AttnParams& ap, cudaStream_t s, bool pdl) {
+cudaError_t launch_attn(pi_pool* p, AttnParams ap, cudaStream_t s, bool pdl) {
   using S = AttnShape<D, B>;
-  cudaError_t e = pi_smem_optin(reinterpret_cast<const void*>(attn_kernel<D, B>), S::kSmem);
+  // the push merge takes shared memory beyond the regular layout; it is used
+  // only where that keeps the kernel's CTAs per SM
+  const int smem0 = S::kSmem;
+  const int smem1 = S::kSmem + push_bytes(ap.splits, ap.G, D);
+  ap.push = (ap.cluster && (228 * 1024) / (smem1 + 1024) >= (228 * 1024) / (smem0 + 1024)) ? 1 : 0;
+  const int smem = ap.push ? smem1 : smem0;
+  cudaError_t e = pi_smem_optin(reinterpret_cast<const void*>(attn_kernel<D, B>), smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ap.splits, ap.nunits);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = S::kSmem;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   // programmatic dependent launch: the CTAs launch and prefetch while the
   // previous kernel on the stream drains, and wait for it before any read
@@ -498,16 +566,19 @@ int attn_smem_bytes(int D, int B) {
 
 int pi_attention_smem(int D, int B) { return attn_smem_bytes(D, B); }
 
-// Load every attention kernel on the current device and opt it in to its shared
-// memory once, when a pool is created (no kernel loads or attribute changes
-// while a decode step is in flight).
+// Load every attention kernel on the current device and opt it in to the
+// device's largest dynamic shared memory once, when a pool is created (the
+// regular layout and any push region of the cluster merge fit under it, so no
+// kernel loads or attribute changes happen while a decode step is in flight).
 cudaError_t pi_prepare_attention_kernels() {
-  cudaError_t e = cudaSuccess;
+  int dev = 0, optin = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   auto one = [&](const void* fn, int bytes) {
     if (e != cudaSuccess) return;
     cudaFuncAttributes a;
     e = cudaFuncGetAttributes(&a, fn);
-    if (e == cudaSuccess) e = pi_smem_optin(fn, bytes);
+    if (e == cudaSuccess) e = pi_smem_optin(fn, std::max(bytes, optin - (int)a.sharedSizeBytes));
   };
   one(reinterpret_cast<const void*>(attn_kernel<128, 16>), AttnShape<128, 16>::kSmem);
   one(reinterpret_cast<const void*>(attn_kernel<128, 32>), AttnShape<128, 32>::kSmem);
@@ -771,6 +842,7 @@ extern "C" pi_status pi_sparse_decode_noalloc(const void* kv_slots, long long n_
   ap.u0 = 0;
   ap.nunits = (int)units;
   ap.cluster = 0;
+  ap.push = 0;
   ap.scale = 1.0f / sqrtf((float)head_dim);
   ap.scale_log2 = ap.scale * 1.4426950408889634f;
   cudaError_t e = cudaErrorInvalidValue;

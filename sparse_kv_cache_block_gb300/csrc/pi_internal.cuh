@@ -340,6 +340,9 @@ __device__ __forceinline__ float4 pi_ld_cluster_f4(uint32_t addr) {
 __device__ __forceinline__ void pi_st_cluster_f32(uint32_t addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
+__device__ __forceinline__ void pi_st_cluster_f2(uint32_t addr, float2 v) {
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(v.x), "f"(v.y) : "memory");
+}
 // Programmatic dependent launch: wait until the grids this one depends on have
 // completed and their writes are visible (a no-op for a launch without the
 // attribute), and let the next grid on the stream start its own launch.
