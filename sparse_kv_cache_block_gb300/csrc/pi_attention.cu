@@ -16,8 +16,12 @@
 //   O^T[d][h]   += V^T[d][tok] . P^T[tok][h]     (P in bf16, fp32 accumulate)
 // P^T's operand fragment is the register transpose (movmatrix) of S^T's
 // accumulator fragment, so P never touches shared memory. Online softmax in the
-// log2 domain, fp32. Warps merge in shared memory; splits merge through a small
-// global partial buffer, finalised by the last CTA of the unit.
+// log2 domain, fp32. Warps merge in shared memory. The 2..8 splits of a unit run
+// as one thread-block cluster: each stores its partial (m, l, O) into the first
+// CTA's shared memory, which merges them (or, where that extra shared memory
+// would cost occupancy, every CTA merges a slice from its peers' partials);
+// other split counts merge through a small global partial buffer, finalised by
+// the last CTA of the unit.
 #include <cudaTypedefs.h>
 
 #include <algorithm>

@@ -1715,9 +1715,10 @@ cudaError_t pi_launch_select(pi_pool* p, int layer, const void* q, const int* k_
     ca.f.tail_sum = p->tail_sum;
     ca.f.ntok_w = p->ntok;
     // mean-key scores of one block set per request stream through a ring of
-    // bulk-copy stages of 8 blocks (about 160 KiB in flight: one CTA per SM);
-    // the consensus score (G x the arithmetic) and head-wise units (strided
-    // summary rows) keep two CTAs per SM
+    // bulk-copy stages of 8 blocks (about 160 KiB in flight: one CTA per SM, or
+    // 64 KiB and two CTAs per SM when the large ring's clusters would not all be
+    // resident at once); the consensus score (G x the arithmetic) and head-wise
+    // units (strided summary rows) keep two CTAs per SM
     const bool ring = !sc.consensus && p->U == 1;
     const int stage_bytes = 8 * p->Hkv * p->D * 4;
     const int ring_big = max(2, min(8, 163840 / stage_bytes));   // one CTA per SM
