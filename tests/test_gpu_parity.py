@@ -529,6 +529,24 @@ def test_attention_every_shape_and_split(D, B, splits, cluster):
         run_layer(pool, om, w, 0, queries(w)[0][0], [w.k, 5, 0], pi.PI_RECALL_UVA)
 
 
+@pytest.mark.parametrize("splits,cluster", [(2, 1), (3, 1), (8, 1), (2, 0)],
+                         ids=["two_push", "three_pull", "eight_pull", "two_global"])
+def test_attention_cluster_merges_group_of_eight(splits, cluster):
+    """Llama-3-70B heads (64 q / 8 KV, G = 8 fills the mma's N), d 128, blocks of 64:
+    two splits merge by pushing their partials into the first CTA's shared memory,
+    three and eight pull slices from their peers (the push region would lower the
+    CTAs per SM), and two without a cluster through the global buffer; ragged
+    tails, a short request, a budget of 0."""
+    w = Workload(layers=1, batch=3, hq=64, hkv=8, head_dim=128, block_tokens=64, ntok=[6000, 2300, 100], k=14,
+                 window=2, pool_slots=16, steps=1, seed=61 + splits)
+    with make_pool(w) as pool:
+        pool.set_attention(splits)
+        pool.set_attention_cluster(bool(cluster))
+        prefill(pool, w)
+        om = OracleModel(w)
+        run_layer(pool, om, w, 0, queries(w)[0][0], [w.k, 9, 0], pi.PI_RECALL_UVA)
+
+
 @pytest.mark.parametrize("splits", [0, 1], ids=["one_wave", "one_cta"])
 def test_empty_selection_gives_zero_output(splits):
     """No recent window and a budget of 0: nothing is selected for that request;
