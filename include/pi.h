@@ -97,7 +97,10 @@ typedef struct pi_config {
                                 the block selected longest ago); placed before host_alloc */
   int host_alloc;            /* host store allocation: 0 = cudaHostAlloc (pinned,
                                 mapped); 1 = anonymous mmap advised for transparent huge
-                                pages, then cudaHostRegister (pinned, mapped) */
+                                pages, then cudaHostRegister (pinned, mapped); measured
+                                on GB300: the UVA gather's scattered block reads run
+                                about 4x slower through mapping 1, sequential reads
+                                alike, so 0 is the one to use */
   int pin_layers;            /* layers that can be held whole in HBM (IO-adaptive
                                 admission): the first ceil(n/2) and the last
                                 floor(n/2) layers get room for max_blocks blocks per
